@@ -1,0 +1,92 @@
+"""Plant plausible mistakes in a copy of the CPU oracle and check that the pins catch each.
+
+Each mutant is one textual change to oracle/specdec_ref.c (a dropped term, a wrong sign,
+a transposed operand, an off-by-one, a wrong tie rule ...). The copy is compiled into a
+temporary directory; the committed oracle is never touched.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+import _pins
+
+SRC_DIR = os.path.dirname(oracle.__file__)
+
+MUTANTS = {
+    "accept_le_instead_of_lt": ("if ((double)c->uniforms[t] < alpha)", "if ((double)c->uniforms[t] <= alpha)"),
+    "residual_transposed": ("double r = c->p[i] - (double)c->q[d * (int64_t)c->V + i];",
+                            "double r = (double)c->q[d * (int64_t)c->V + i] - c->p[i];"),
+    "model_free_residual_keeps_draft": ("wi = (i == x) ? 0.0 : c->p[i];", "wi = c->p[i];"),
+    "temperature_dropped": ("double e = (c->z[i] > -INFINITY) ? exp(c->z[i] / T - m) : 0.0;",
+                            "double e = (c->z[i] > -INFINITY) ? exp(c->z[i] - m * T) : 0.0;"),
+    "greedy_ties_to_highest_index": ("if (c->z[i] > bz) { bz = c->z[i]; best = i; }",
+                                     "if (c->z[i] >= bz) { bz = c->z[i]; best = i; }"),
+    "race_multiplies_noise": ("s = c->w[i] / (double)E[i];", "s = c->w[i] * (double)E[i];"),
+    "ratio_inverted": ("return px / qx;", "return qx / px;"),
+    "mask_bit_order_reversed": ("return (int)((word >> (i & 31)) & 1u);",
+                                "return (int)((word >> (31 - (i & 31))) & 1u);"),
+    "counters_I_D_swapped": ("c->counters[1] += (uint64_t)(k - g);", "c->counters[1] += (uint64_t)g;"),
+    "accepted_counter_off_by_one": ("c->counters[3] += (uint64_t)a;", "c->counters[3] += (uint64_t)(a + 1);"),
+    "bonus_is_argmax": ("for (int32_t i = 0; i < c->V; ++i) c->w[i] = c->p[i];\n            emitted = exponential_race(c, t, b);",
+                        "double zz; emitted = greedy_token(c, &zz);"),
+    "grammar_prefix_from_last_invalid": ("if (g == k && (!ok || !grammar_allows(c, row0 + j, x))) g = j;",
+                                         "if (!ok || !grammar_allows(c, row0 + j, x)) g = j;"),
+    "bonus_row_skipped": ("for (int32_t j = 0; j <= k; ++j) {\n        const int64_t t = row0 + j;",
+                          "for (int32_t j = 0; j < k; ++j) {\n        const int64_t t = row0 + j;"),
+    "softmax_not_normalised": ("for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;", "(void)0;"),
+    "empty_row_not_flagged": ("if (live == 0) {", "if (live < 0) {"),
+    "model_free_alpha_is_one": ("if (!qmode) return px;", "if (!qmode) return 1.0;"),
+    "no_stop_at_rejection": ("        a = j;\n        emitted = exponential_race(c, t, b);\n        break;",
+                             "        a = j;\n        emitted = exponential_race(c, t, b);\n        c->out_tokens[t] = emitted;\n        continue;"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    search, repl = MUTANTS[name]
+    src = open(os.path.join(SRC_DIR, "specdec_ref.c")).read()
+    assert src.count(search) == 1, f"mutant {name}: search text must occur exactly once"
+    d = tmp_path / name
+    d.mkdir()
+    shutil.copy(os.path.join(SRC_DIR, "specdec_ref.h"), d / "specdec_ref.h")
+    (d / "specdec_ref.c").write_text(src.replace(search, repl))
+    return oracle.build(src=str(d / "specdec_ref.c"), out=str(d / "libmutant.so"))
+
+
+# fast versions of the pins (the chi-square at 2e5 trials is still far past any of these mutants)
+def _run_pins(lib):
+    failures = []
+    checks = [
+        ("worked_counter_example", lambda: _pins.check_worked_counter_example(lib)),
+        ("strict_accept_comparison", lambda: _pins.check_strict_accept_comparison(lib)),
+        ("edge_cases", lambda: _pins.check_edge_cases(lib)),
+        ("residual_excludes_draft", lambda: _pins.check_residual_excludes_draft(lib)),
+        ("p_equals_q", lambda: _pins.check_p_equals_q_accepts_all(lib, B=100)),
+        ("greedy_brute_force", lambda: _pins.check_greedy_brute_force(lib, cases=30)),
+        ("grammar_invariants", lambda: _pins.check_grammar_invariants(lib)),
+        ("softmax_library", lambda: _pins.check_softmax_matches_library(lib)),
+        ("chi_square", lambda: _pins.check_chi_square(lib, n=200_000)),
+    ]
+    for name, fn in checks:
+        try:
+            fn()
+        except Exception as e:  # noqa: BLE001 - any failure counts as caught
+            failures.append(f"{name}: {type(e).__name__}")
+    return failures
+
+
+def test_unmutated_copy_passes(tmp_path):
+    d = tmp_path / "clean"
+    d.mkdir()
+    shutil.copy(os.path.join(SRC_DIR, "specdec_ref.h"), d / "specdec_ref.h")
+    shutil.copy(os.path.join(SRC_DIR, "specdec_ref.c"), d / "specdec_ref.c")
+    lib = oracle.build(src=str(d / "specdec_ref.c"), out=str(d / "libclean.so"))
+    assert _run_pins(lib) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    lib = _build_mutant(tmp_path, name)
+    failures = _run_pins(lib)
+    assert failures, f"mutant {name} passed every pin"
