@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark of the batched speculative-decoding verify step on GB300.
+
+One step = one verify call (the whole hot path) over one batch of synthetic input.
+Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+value      verified draft tokens / s (R per step / kernel time), inputs resident in HBM,
+           L2 flushed between steps, CUDA events on the launching stream; under torchrun
+           the tokens of all ranks / the slowest rank's time (each rank verifies its own
+           batch: requests are independent, no collective in the data path).
+e2e        the same metric through the public API with page-locked HOST buffers: every step
+           copies the step's inputs host->device, verifies, and reads the outputs back.
+roofline   algorithmic bytes per launch / mean kernel time, against the measured HBM copy
+           bandwidth.
+cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_specdec_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verified draft tokens/s (HBM GB/s and fraction of GB300 peak in roofline)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_specdec_gb300", "csrc", "specdec_verify.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=4, help="workload recipe index (default: the large mixed batch)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in (KERNEL_SRC, os.path.join(ROOT, "include", "specdec.h")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_for(cfg: int, rank: int) -> W.Workload:
+    # rank 0 verifies the recipe's own seeded batch; other ranks verify independent batches
+    return W.config(cfg, seed=cfg + 1000 * rank)
+
+
+# ------------------------------------------------------------------------------------------
+# algorithmic bytes: what the method must read / write given the accepted lengths
+# ------------------------------------------------------------------------------------------
+
+def _sector_bytes(allowed_row: np.ndarray) -> int:
+    """32-byte sectors of an fp32 row that hold at least one allowed id."""
+    V = allowed_row.size
+    pad = (-V) % 8
+    a = np.concatenate([allowed_row, np.zeros(pad, dtype=bool)]).reshape(-1, 8)
+    return int(a.any(axis=1).sum()) * 32
+
+
+def algorithmic_bytes(w: W.Workload, acc: np.ndarray, status: np.ndarray) -> dict:
+    """Per-launch bytes the verify must move: logits and mask words of rows 0..a_b; for random
+    requests the exponential noise of the draw row, and on a rejected draft-model row its q row
+    plus q(x) of every tested draft; for masked rows the noise / q reads count only the 32-byte
+    sectors holding an allowed id; plus the small per-request arrays and the outputs."""
+    es = 2 if w.logits_dtype == W.BF16 else 4
+    V, Wd = w.V, w.W
+    cu = w.cu_num_draft
+    temps = w.temperature
+    greedy = ~((temps > 0) & np.isfinite(temps) & (temps >= np.float32(1.17549435e-38)))
+    qmode = np.zeros(w.B, dtype=bool)
+    if w.draft_probs is not None:
+        qmode[:] = True if w.has_q is None else (w.has_q != 0)
+    logits = mask = noise = q = small = 0
+    for b in range(w.B):
+        k = int(cu[b + 1] - cu[b])
+        if status[b] & (8 | 16):
+            continue
+        a = int(acc[b])
+        rows = a + 1
+        logits += rows * V * es
+        if w.bitmask is not None:
+            mask += rows * 4 * Wd
+        small += 4 * 2 + 4 + 4 * k + 4 * (k + 1) + 4   # cu, temperature, ids, out_tokens, out_num_accepted
+        if greedy[b]:
+            continue
+        small += 4 * min(rows, k)                       # uniforms of the tested drafts
+        t = int(cu[b]) + b + a
+        if w.bitmask is not None and not (w.bitmask[t] == -1).all():
+            row_bytes = _sector_bytes(W.unpack_mask_rows(w.bitmask[t], V)[0])
+        else:
+            row_bytes = 4 * V
+        noise += row_bytes
+        if qmode[b]:
+            q += 4 * min(rows, k)
+            if a < k:
+                q += row_bytes
+    total = logits + mask + noise + q + small + 32
+    return {"total": total, "logits": logits, "mask": mask, "noise": noise, "q": q, "small": small}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        t0, t1 = (self.t0 or 0) - 0.3, (self.t1 or time.time()) + 0.3
+        rows = [l for (ts, l) in self.lines if t0 <= ts <= t1] or [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle baseline (test infrastructure; timed here as a reported baseline)
+# ------------------------------------------------------------------------------------------
+
+def cpu_oracle_sample(w: W.Workload, budget_s: float):
+    import oracle
+
+    oracle.load()
+    order = np.arange(w.B)
+    # grow the sample until it fills the budget (rough), then time it once
+    n = 8
+    while True:
+        sub = w.subset(order[: min(n, w.B)])
+        t0 = time.perf_counter()
+        oracle.verify(sub)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or n >= w.B:
+            break
+        n = min(w.B, int(n * max(2.0, (budget_s / 3) / max(dt, 1e-3))))
+    sub = w.subset(order[: min(n, w.B)])
+    t0 = time.perf_counter()
+    oracle.verify(sub)
+    dt = time.perf_counter() - t0
+    return sub, dt
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores, each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    w = workload_for(args.config, 0)
+    oracle.load()
+    budget_total = 150.0
+    per_step = max(0.05, min(5.0, budget_total / max(1, args.steps + args.warmup)))
+    # size the per-step sample
+    n = 1
+    while True:
+        sub = w.subset(np.arange(min(n, w.B)))
+        t0 = time.perf_counter()
+        oracle.verify(sub)
+        dt = time.perf_counter() - t0
+        if dt >= per_step / 2 or n >= w.B:
+            break
+        n = min(w.B, n * 2)
+    sub = w.subset(np.arange(min(n, w.B)))
+    for _ in range(args.warmup):
+        oracle.verify(sub)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.verify(sub)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = sub.N * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "requests_per_step": sub.B, "drafts_per_step": sub.N,
+                   "note": "CPU oracle (plain C, fp64, single thread) on the first requests of the workload"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {sub.B} of {w.B} requests ({sub.N} drafts) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------
+
+def traffic_from_profiles(config_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(config_name)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+
+    from speculative_decoding_verification_specdec_gb300 import _native, build, device
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+        pg = dist
+    if rank == 0 and build.needs_rebuild():
+        build.build_library()
+    if pg:
+        pg.barrier()
+    _native.load()
+
+    w = workload_for(args.config, rank)
+    host = device.host_tensors(w)
+    dev_in = device.device_tensors(w, dev, host)
+    out = device.alloc_outputs(w, dev, diag=False)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    # warm-up
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        device.verify(w, dev_in, out, stream=stream)
+    torch.cuda.synchronize()
+    out.counters.zero_()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush between timed steps (outside the events)
+        starts[i].record(stream)
+        device.verify(w, dev_in, out, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    if pg:
+        pg.barrier()
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    tot_ms = float(sum(kernel_ms))
+    res = out.numpy()
+    ctr = res["counters"]
+    R_per_step = int(ctr[0]) // args.steps
+    assert R_per_step == w.N, (R_per_step, w.N)
+    if pg:
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        max_ms = float(t.item())
+        r = torch.tensor([w.N], dtype=torch.float64, device=dev)
+        pg.all_reduce(r)
+        R_all = float(r.item())
+    else:
+        max_ms, R_all = tot_ms, float(w.N)
+    value = R_all * args.steps / (max_ms / 1e3)
+    clocks = sampler.stop() if rank == 0 else None
+
+    # roofline of the (single) kernel
+    ab = algorithmic_bytes(w, res["out_num_accepted"], res["status"])
+    mean_s = (tot_ms / args.steps) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = ab["total"] / mean_s / 1e9
+    traffic = traffic_from_profiles(w.name)
+
+    # e2e through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = device.host_tensors(w, pin=True)
+        out_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                 for k, v in (("out_tokens", out.out_tokens), ("out_num_accepted", out.out_num_accepted),
+                              ("counters", out.counters), ("status", out.status))}
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values() if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+
+        def e2e_step():
+            for f, t in pinned.items():
+                if t is not None:
+                    dev_in[f].copy_(t, non_blocking=True)
+            device.verify(w, dev_in, out, stream=stream)
+            out_h["out_tokens"].copy_(out.out_tokens, non_blocking=True)
+            out_h["out_num_accepted"].copy_(out.out_num_accepted, non_blocking=True)
+            out_h["counters"].copy_(out.counters, non_blocking=True)
+            out_h["status"].copy_(out.status, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": R_all * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sub, dt = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": sub.N / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {sub.B} of {w.B} requests ({sub.N} drafts), one pass, {dt:.1f} s"}
+
+    if rank == 0:
+        shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.logits_dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "V": w.V, "drafts_per_step": w.N, "rows": w.T,
+                       "l2": "flushed between timed steps (268 MB write)",
+                       "launch": {"grid_ctas": w.B * shape["ctas_per_request"], **shape},
+                       "per_rank": "independent batch per rank (requests shard with no exchange)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": ab},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "kernel_ms": {"median": statistics.median(kernel_ms), "min": min(kernel_ms), "max": max(kernel_ms)},
+            "counters_per_step": [int(c) // args.steps for c in ctr],
+            "kernel_hash": kernel_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+/*
+ * specdec.h -- C ABI of libspecdec.so: batched speculative-decoding verification on
+ * one GB300 (sm_103a).
+ *
+ * One call verifies a ragged batch of draft tokens against the target model's logits:
+ * it applies each position's packed grammar bitmask, takes the temperature softmax,
+ * accepts each draft with probability min(1, p/q) (or by argmax equality for greedy
+ * requests), stops at the first rejection, draws the recovered token there from the
+ * residual distribution, emits a bonus token when every draft is accepted, and
+ * accumulates the raw / grammar-invalidated / eligible / accepted counters.
+ *
+ * Sources for the operation:
+ *   - "vLLM tour part 2" (pyshine.com/vllm-2), section "Verification: rejection sampling
+ *     on the GPU": target logits for every draft position plus one bonus position, cast
+ *     to float32, temperature applied; acceptance where the target probability of the
+ *     draft token beats a uniform draw; recovered token from the target probabilities
+ *     minus the draft probabilities clamped at zero; greedy variant for temperature 0.
+ *   - same page, section "Grammar gates: structured output": one bitmask row per request
+ *     and per speculative position; masked tokens cannot be produced.
+ *   - "5.2 Draft models and model-free methods" (infra-guide), section 4.3: a draft with
+ *     no probabilities is a one-hot q -- accept with probability p(x), residual = p with x
+ *     removed, renormalised.
+ *   - "Structured output speculative decoding acceptance" (fanout.sh), section "Name the
+ *     three counters": R raw drafts, I grammar-invalidated, D = R - I eligible, A accepted.
+ *
+ * Layout conventions (all calls):
+ *   B requests; cu_num_draft[B+1] is an exclusive prefix sum, cu[0] = 0, non-decreasing;
+ *   request b has k_b = cu[b+1] - cu[b] drafts; N = cu[B].
+ *   Draft slot d(b,j) = cu[b] + j, j in [0, k_b).
+ *   Logit row t(b,j) = cu[b] + b + j, j in [0, k_b]; row j = k_b is the bonus row;
+ *   T = N + B rows.  W = ceil(V / 32) mask words per row.
+ *   A request is greedy iff temperature[b] == 0. It is a draft-model request iff
+ *   draft_probs != NULL and (has_q == NULL or has_q[b] != 0); otherwise model-free.
+ */
+#ifndef SPECDEC_H
+#define SPECDEC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECDEC_KMAX 32           /* largest supported max_k (drafts per request) */
+
+typedef enum {
+    SPECDEC_OK = 0,
+    SPECDEC_ERR_INVALID_ARG = 1,   /* a NULL required pointer, a bad size or a misaligned pointer */
+    SPECDEC_ERR_UNSUPPORTED = 2,   /* dtype unknown, or a row too wide for on-chip staging */
+    SPECDEC_ERR_CUDA = 3,          /* a CUDA runtime error at launch (or from specdec_wait) */
+    SPECDEC_ERR_TIMEOUT = 4        /* specdec_wait gave up */
+} specdec_status_t;
+
+typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
+
+/* Per-request status bits written to status[b] (0 = clean). The kernel never traps. */
+#define SPECDEC_ST_BAD_DRAFT_ID    1u   /* a draft id outside [0, V): counted invalid, never accepted */
+#define SPECDEC_ST_EMPTY_MASK_ROW  2u   /* a row read allows no finite logit: -1 emitted there, request stops */
+#define SPECDEC_ST_BAD_TEMPERATURE 4u   /* not 0 and not a positive normal finite float: verified greedily */
+#define SPECDEC_ST_K_TOO_LARGE     8u   /* k_b > max_k: skipped, -1 in its rows, no counters */
+#define SPECDEC_ST_BAD_OFFSETS    16u   /* cu[0] != 0 or cu[b] > cu[b+1] or cu[b+1] > cu[B]: skipped */
+#define SPECDEC_ST_DEVICE_TIMEOUT 32u   /* an on-chip copy did not land within its time limit */
+
+/*
+ * specdec_verify -- verify one batch (stream-ordered, asynchronous).
+ *
+ * Pointers are device pointers to caller-owned memory on the current device; the
+ * library allocates nothing and keeps no state between calls.
+ *
+ *   target_logits  [T, V] row-major, fp32 or bf16 (logits_dtype); 4- resp. 2-byte aligned.
+ *   draft_ids      [N] int32.
+ *   draft_probs    [N, V] fp32 draft distributions q, or NULL (every request model-free).
+ *                  Only q(x) of each tested draft and the q row of a rejected position are read.
+ *   has_q          [B] uint8 or NULL (NULL: every request is a draft-model request iff
+ *                  draft_probs != NULL).
+ *   cu_num_draft   [B+1] int32 exclusive prefix of draft counts.
+ *   B, V, max_k    B >= 0, V >= 1, 0 <= max_k <= SPECDEC_KMAX (every k_b must be <= max_k).
+ *   bitmask        [T, W] int32 or NULL (unconstrained). Bit (i & 31) of word i >> 5 is 1
+ *                  when token i is allowed; bits at or above V are ignored.
+ *   temperature    [B] fp32; 0 means greedy.
+ *   uniforms       [T] fp32 in [0, 1); draft j of request b is accepted iff
+ *                  uniforms[t(b,j)] < alpha (strict). Entries at bonus rows are unused.
+ *   exp_noise      [T, V] fp32 Exp(1) samples > 0; the token drawn from weights w at row t
+ *                  is argmax_i w_i / exp_noise[t, i] (lowest index on ties). Read only at
+ *                  the one row per random request that draws a token.
+ *   out_tokens     [T] int32: the accepted drafts, then the recovered or bonus token,
+ *                  then -1 for every later position of the request.
+ *   out_num_accepted [B] int32: accepted drafts a_b per request.
+ *   counters       [4] uint64 (R, I, D, A), ADDED to (never cleared by the library).
+ *   status         [B] uint32 per-request status bits (written, not accumulated), or NULL.
+ *   diag_accept_prob [N] fp32 or NULL: alpha of every draft that was tested, NaN otherwise.
+ *   diag_row_stats [T, 2] fp32 or NULL: for every row read, (m, S) with m = max_i z_i / T
+ *                  and S = sum_i exp(z_i / T - m) on random requests, (max_i z_i, NaN) on
+ *                  greedy ones; (NaN, NaN) for rows not read.
+ *   stream         a cudaStream_t (NULL = legacy default stream).
+ *
+ * Rows after a request's first rejection are never read.
+ * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
+ * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
+ * pointer, B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
+ * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype or a row wider than the on-chip
+ * staging allows (V * element size > 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
+ */
+specdec_status_t specdec_verify(
+    const void* target_logits, specdec_dtype_t logits_dtype,
+    const int32_t* draft_ids,
+    const float* draft_probs,
+    const uint8_t* has_q,
+    const int32_t* cu_num_draft,
+    int32_t B, int32_t V, int32_t max_k,
+    const int32_t* bitmask,
+    const float* temperature,
+    const float* uniforms,
+    const float* exp_noise,
+    int32_t* out_tokens,
+    int32_t* out_num_accepted,
+    unsigned long long* counters,
+    uint32_t* status,
+    float* diag_accept_prob,
+    float* diag_row_stats,
+    void* stream);
+
+/*
+ * specdec_wait -- block the calling host thread until all work queued on `stream` has
+ * finished, or until timeout_ms milliseconds have passed (polling; timeout_ms < 0 waits
+ * without limit). Returns SPECDEC_OK, SPECDEC_ERR_TIMEOUT, or SPECDEC_ERR_CUDA when the
+ * stream reports an error.
+ */
+specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
+
+/* Human-readable name of a status code (static storage). */
+const char* specdec_status_string(specdec_status_t status);
+
+/*
+ * specdec_launch_config -- the launch shape specdec_verify uses for a vocabulary size and
+ * dtype (host arithmetic only; no GPU needed): CTAs per request (a thread-block cluster that
+ * splits each vocabulary row into contiguous slices), threads per CTA, dynamic shared memory
+ * per CTA in bytes, and vocabulary ids per slice. Any output pointer may be NULL.
+ * Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED like specdec_verify.
+ */
+specdec_status_t specdec_launch_config(int32_t V, specdec_dtype_t logits_dtype,
+                                       int32_t* ctas_per_request, int32_t* threads_per_cta,
+                                       int32_t* smem_bytes, int32_t* slice_ids);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_H */

@@ -1,0 +1,130 @@
+"""ctypes binding of libspecdec.so (include/specdec.h). Argument marshalling only:
+every step of the verify runs in the CUDA library. There is no fallback; a missing
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libspecdec.so")
+
+SPECDEC_OK = 0
+SPECDEC_ERR_INVALID_ARG = 1
+SPECDEC_ERR_UNSUPPORTED = 2
+SPECDEC_ERR_CUDA = 3
+SPECDEC_ERR_TIMEOUT = 4
+SPECDEC_F32 = 0
+SPECDEC_BF16 = 1
+SPECDEC_KMAX = 32
+
+ST_BAD_DRAFT_ID = 1
+ST_EMPTY_MASK_ROW = 2
+ST_BAD_TEMPERATURE = 4
+ST_K_TOO_LARGE = 8
+ST_BAD_OFFSETS = 16
+ST_DEVICE_TIMEOUT = 32
+
+EXPORTED = ("specdec_verify", "specdec_wait", "specdec_status_string", "specdec_launch_config")
+
+_lib = None
+
+
+class SpecdecError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    lib.specdec_verify.restype = ctypes.c_int
+    lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
+                                   vp, vp, vp, vp, vp, vp, vp]
+    lib.specdec_wait.restype = ctypes.c_int
+    lib.specdec_wait.argtypes = [vp, i32]
+    lib.specdec_status_string.restype = ctypes.c_char_p
+    lib.specdec_status_string.argtypes = [ctypes.c_int]
+    lib.specdec_launch_config.restype = ctypes.c_int
+    lib.specdec_launch_config.argtypes = [i32, ctypes.c_int, vp, vp, vp, vp]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().specdec_status_string(int(status)).decode()
+
+
+def launch_config(V: int, dtype: int) -> dict:
+    c, t, s, w = (ctypes.c_int32() for _ in range(4))
+    rc = load().specdec_launch_config(int(V), int(dtype), ctypes.byref(c), ctypes.byref(t),
+                                      ctypes.byref(s), ctypes.byref(w))
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_launch_config")
+    return {"ctas_per_request": c.value, "threads_per_cta": t.value, "smem_bytes": s.value,
+            "slice_ids": w.value}
+
+
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+
+
+def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
+                   bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
+                   status=None, diag_accept_prob=None, diag_row_stats=None, stream=None, logits_dtype=None) -> None:
+    """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
+    (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
+    non-zero status."""
+    import torch
+
+    if logits_dtype is None:
+        if target_logits.dtype == torch.bfloat16:
+            logits_dtype = SPECDEC_BF16
+        elif target_logits.dtype == torch.float32:
+            logits_dtype = SPECDEC_F32
+        else:
+            raise SpecdecError(SPECDEC_ERR_UNSUPPORTED, f"logits dtype {target_logits.dtype}")
+    for name, t in (("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
+                    ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
+                    ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
+                    ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
+                    ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats)):
+        if t is not None and hasattr(t, "is_cuda"):
+            if not t.is_cuda:
+                raise ValueError(f"{name} must be a CUDA tensor")
+            if not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous")
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load().specdec_verify(
+        _p(target_logits), int(logits_dtype), _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
+        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
+        _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
+        _p(diag_row_stats), stream)
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_verify")
+
+
+def specdec_wait(stream=None, timeout_ms: int = -1) -> None:
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load().specdec_wait(stream, int(timeout_ms))
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_wait")

@@ -1,0 +1,874 @@
+/*
+ * specdec_verify.cu -- fused speculative-decoding verify kernel for GB300 (sm_103a) and
+ * the C-ABI launcher declared in include/specdec.h.
+ *
+ * What it computes (see include/specdec.h for the passages): per request, rows
+ * j = 0, 1, ... of the target logits in order -- grammar bitmask, temperature softmax
+ * statistics, acceptance of draft j (uniform draw below min(1, p/q), p(x) for a one-hot
+ * model-free draft, argmax equality when greedy) -- until the first rejection or the
+ * bonus row; there one more pass draws the recovered / bonus token as
+ * argmax_i w_i / E_i (exponential race) with w = max(p - q, 0), p without the draft
+ * token, or p. Rows after the stop row are never read.
+ *
+ * GB300 mapping:
+ *   - one thread-block cluster per request; its G CTAs split every vocabulary row into
+ *     contiguous slices of `slice_units * 128` ids;
+ *   - a CTA stages its slice of a row in shared memory with bulk async copies
+ *     (cp.async.bulk, the TMA engine) in kChunks pieces, each completing on its own
+ *     mbarrier, so arithmetic starts as soon as the first piece lands; the slice stays
+ *     on chip for the draw pass, so the stop row is read from HBM once;
+ *   - per-row results (max/sum of the online softmax, the argmax, the draft's logit) are
+ *     combined across the cluster through distributed shared memory, and every CTA
+ *     takes the same accept/reject decision;
+ *   - the draw pass streams only the exponential noise (and q on a rejected draft-model
+ *     row) with 128-bit loads, and skips 16-byte groups the bitmask fully forbids.
+ * No tensor cores: nothing here is a contraction. Everything is fp32 (bf16 logits are
+ * widened exactly); exp uses the ex2.approx hardware instruction on pre-scaled inputs.
+ *
+ * Every wait on an mbarrier is bounded in time; on expiry the request gets
+ * SPECDEC_ST_DEVICE_TIMEOUT and the kernel runs to completion without hanging.
+ */
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <cstdlib>
+#include <ctime>
+#include <mutex>
+
+#include "specdec.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnit = 128;                    // slice granularity in ids (4 mask words)
+constexpr int kChunks = 4;                    // bulk copies / mbarriers per row slice
+constexpr int kMaxCluster = 16;
+constexpr int kTargetSliceBytes = 32 * 1024;
+constexpr int kMaxSliceBytes = 192 * 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+enum : int { kDrawP = 0, kDrawResidualQ = 1, kDrawResidualOneHot = 2 };
+
+struct Args {
+    const void* logits;
+    const int32_t* draft_ids;
+    const float* q;
+    const uint8_t* has_q;
+    const int32_t* cu;
+    const int32_t* bitmask;
+    const float* temperature;
+    const float* uniforms;
+    const float* noise;
+    int32_t* out_tokens;
+    int32_t* out_num_accepted;
+    unsigned long long* counters;
+    uint32_t* status;
+    float* diag_alpha;
+    float* diag_row;
+    int32_t B, V, max_k, W;
+    int32_t slice_units;    // kUnit blocks per CTA slice
+    int32_t G;              // CTAs per request (cluster size)
+    int32_t bulk;           // 1: rows staged with bulk async copies; 0: plain loads
+    int32_t vec_noise;      // 1: noise / q rows are 16-byte aligned (128-bit loads)
+};
+
+// Partial result of one row pass, combined thread -> warp -> CTA -> cluster.
+struct Part {
+    float m;      // running max of the unscaled logits (random rows)
+    float S;      // sum of exp2((z - m) * c)
+    float zx;     // logit of the draft token (only the CTA owning it sets it)
+    float best;   // argmax value (greedy: logit; draw: w / E)
+    int idx;      // argmax index (lowest on ties), INT_MAX if none
+    int flag;     // draw pass: some weight was positive
+};
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for phase `parity` of an mbarrier. Returns false when the time limit expired.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ Part part_identity()
+{
+    Part p;
+    p.m = -INFINITY; p.S = 0.f; p.zx = -INFINITY; p.best = -INFINITY; p.idx = INT_MAX; p.flag = 0;
+    return p;
+}
+
+// Combine b into a. c = log2(e) / T scales logit differences for the softmax sum.
+__device__ __forceinline__ void combine(Part& a, const Part& b, float c)
+{
+    if (b.m > a.m) {
+        a.S = b.S + (a.m == -INFINITY ? 0.f : a.S * ex2((a.m - b.m) * c));
+        a.m = b.m;
+    } else if (b.m > -INFINITY) {
+        a.S += b.S * ex2((b.m - a.m) * c);
+    }
+    a.zx = fmaxf(a.zx, b.zx);
+    if (b.best > a.best || (b.best == a.best && b.idx < a.idx)) { a.best = b.best; a.idx = b.idx; }
+    a.flag |= b.flag;
+}
+
+__device__ __forceinline__ Part shfl_part(const Part& p, int off)
+{
+    Part o;
+    o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
+    o.S = __shfl_xor_sync(0xffffffffu, p.S, off);
+    o.zx = __shfl_xor_sync(0xffffffffu, p.zx, off);
+    o.best = __shfl_xor_sync(0xffffffffu, p.best, off);
+    o.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
+    o.flag = __shfl_xor_sync(0xffffffffu, p.flag, off);
+    return o;
+}
+
+__device__ __forceinline__ Part warp_reduce(Part p, float c)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Part o = shfl_part(p, off);
+        combine(p, o, c);
+    }
+    return p;
+}
+
+struct Shared {
+    uint64_t bars[kChunks];
+    Part wpart[kWarps];
+    Part red[2];
+    Part res;
+    int32_t xs[SPECDEC_KMAX];
+    float us[SPECDEC_KMAX];
+    float qxs[SPECDEC_KMAX];
+    int32_t k, g, skip, greedy, qmode, timed_out;
+    uint32_t st;
+};
+
+// Reduce one Part per thread over the whole cluster; every thread of every CTA gets the
+// same (bitwise identical) result. `slot` alternates so one cluster barrier per reduction
+// suffices: a slot is rewritten only after the next reduction's barrier, which every CTA
+// reaches after it has finished reading the slot.
+__device__ __forceinline__ Part cluster_reduce(Part p, float c, Shared& sh, int slot, int G)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    p = warp_reduce(p, c);
+    if (lane == 0) sh.wpart[warp] = p;
+    __syncthreads();
+    if (warp == 0) {
+        Part q = lane < kWarps ? sh.wpart[lane] : part_identity();
+        q = warp_reduce(q, c);
+        if (lane == 0) sh.red[slot] = q;
+    }
+    cluster_sync_all();
+    if (warp == 0) {
+        Part q = part_identity();
+        if (lane < G) {
+            const uint32_t base = map_to_rank(smem_addr(&sh.red[slot]), (uint32_t)lane);
+            q.m = __uint_as_float(ld_cluster_u32(base + 0));
+            q.S = __uint_as_float(ld_cluster_u32(base + 4));
+            q.zx = __uint_as_float(ld_cluster_u32(base + 8));
+            q.best = __uint_as_float(ld_cluster_u32(base + 12));
+            q.idx = (int)ld_cluster_u32(base + 16);
+            q.flag = (int)ld_cluster_u32(base + 20);
+        }
+        q = warp_reduce(q, c);
+        if (lane == 0) sh.res = q;
+    }
+    __syncthreads();
+    return sh.res;
+}
+
+// ---------------------------------------------------------------------------------------------
+// element access
+// ---------------------------------------------------------------------------------------------
+
+template <typename ET> struct Elem;
+
+template <> struct Elem<float> {
+    static constexpr int VE = 4;        // elements per 16-byte vector
+    __device__ static __forceinline__ void load(const unsigned char* s, int v, float z[VE])
+    {
+        const float4 f = reinterpret_cast<const float4*>(s)[v];
+        z[0] = f.x; z[1] = f.y; z[2] = f.z; z[3] = f.w;
+    }
+};
+
+template <> struct Elem<uint16_t> {       // bf16 bit patterns
+    static constexpr int VE = 8;
+    __device__ static __forceinline__ void load(const unsigned char* s, int v, float z[VE])
+    {
+        const uint4 u = reinterpret_cast<const uint4*>(s)[v];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            z[2 * i] = __uint_as_float(w[i] << 16);
+            z[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// Allowed-bits of vector v (VE ids) of the slice; all ones when there is no bitmask.
+template <int VE>
+__device__ __forceinline__ uint32_t vec_bits(const uint32_t* smask, bool has_mask, int v)
+{
+    if (!has_mask) return (1u << VE) - 1u;
+    const int e0 = v * VE;
+    return (smask[e0 >> 5] >> (e0 & 31)) & ((1u << VE) - 1u);
+}
+
+// Stage slice [lo, lo + n) of row t (and its mask words) into shared memory.
+template <typename ET>
+__device__ __forceinline__ void stage_row(const Args& a, Shared& sh, unsigned char* slice, uint32_t* smask,
+                                          int64_t t, int64_t lo, int n, int nvec, int nw, uint32_t ph)
+{
+    constexpr int VE = Elem<ET>::VE;
+    const ET* src = reinterpret_cast<const ET*>(a.logits) + t * (int64_t)a.V + lo;
+    const int32_t* msrc = a.bitmask ? a.bitmask + t * (int64_t)a.W + (lo >> 5) : nullptr;
+    if (a.bulk) {
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();
+            const int cv = (nvec + kChunks - 1) / kChunks;
+            for (int c = 0; c < kChunks; ++c) {
+                const int vb = min(nvec, c * cv), ve = min(nvec, (c + 1) * cv);
+                const uint32_t bytes = (uint32_t)(ve - vb) * 16u;
+                const uint32_t mbytes = (c == 0 && msrc) ? (uint32_t)nw * 4u : 0u;
+                const uint32_t bar = smem_addr(&sh.bars[c]);
+                mbar_arrive_expect_tx(bar, bytes + mbytes);
+                if (bytes) bulk_copy_g2s(smem_addr(slice) + (uint32_t)vb * 16u,
+                                         reinterpret_cast<const unsigned char*>(src) + (size_t)vb * 16u, bytes, bar);
+                if (mbytes) bulk_copy_g2s(smem_addr(smask), msrc, mbytes, bar);
+            }
+        }
+        (void)ph;
+    } else {
+        ET* dst = reinterpret_cast<ET*>(slice);
+        ET pad;
+        if constexpr (sizeof(ET) == 4) pad = -INFINITY;
+        else pad = (ET)0xFF80u;                    // bf16 -inf
+        for (int e = threadIdx.x; e < nvec * VE; e += kThreads) dst[e] = e < n ? src[e] : pad;
+        if (msrc)
+            for (int w = threadIdx.x; w < nw; w += kThreads) smask[w] = (uint32_t)msrc[w];
+        __syncthreads();
+    }
+}
+
+// Wait for piece c of the staged row (bulk path).
+__device__ __forceinline__ void wait_piece(const Args& a, Shared& sh, int c, uint32_t ph)
+{
+    if (!a.bulk) return;
+    if (!mbar_wait_bounded(smem_addr(&sh.bars[c]), ph)) sh.timed_out = 1;
+}
+
+// One pass over a staged row: greedy argmax, or the online-softmax (max, sum).
+template <typename ET, bool kGreedy>
+__device__ __forceinline__ Part row_pass(const Args& a, Shared& sh, const unsigned char* slice,
+                                         const uint32_t* smask, int64_t lo, int nvec, float c, uint32_t ph)
+{
+    constexpr int VE = Elem<ET>::VE;
+    const bool has_mask = a.bitmask != nullptr;
+    Part p = part_identity();
+    const int cv = (nvec + kChunks - 1) / kChunks;
+    for (int ch = 0; ch < kChunks; ++ch) {
+        wait_piece(a, sh, ch, ph);
+        const int vb = min(nvec, ch * cv), ve = min(nvec, (ch + 1) * cv);
+        for (int v = vb + (int)threadIdx.x; v < ve; v += kThreads) {
+            const uint32_t bits = vec_bits<VE>(smask, has_mask, v);
+            if (bits == 0u) continue;
+            float z[VE];
+            Elem<ET>::load(slice, v, z);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
+            if (kGreedy) {
+#pragma unroll
+                for (int e = 0; e < VE; ++e)
+                    if (z[e] > p.best) { p.best = z[e]; p.idx = (int)(lo + (int64_t)v * VE + e); }
+            } else {
+                float vm = z[0];
+#pragma unroll
+                for (int e = 1; e < VE; ++e) vm = fmaxf(vm, z[e]);
+                if (vm == -INFINITY) continue;
+                if (vm > p.m) {
+                    p.S = (p.m == -INFINITY) ? 0.f : p.S * ex2((p.m - vm) * c);
+                    p.m = vm;
+                }
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < VE; ++e) s += ex2((z[e] - p.m) * c);
+                p.S += s;
+            }
+        }
+    }
+    return p;
+}
+
+// Draw pass on the staged stop / bonus row: argmax_i w_i / E_i.
+template <typename ET>
+__device__ __forceinline__ Part draw_pass(const Args& a, const unsigned char* slice, const uint32_t* smask,
+                                          int64_t lo, int n, int nvec, int64_t t, int64_t d, int mode, int x,
+                                          float m, float c, float invS)
+{
+    constexpr int VE = Elem<ET>::VE;
+    const bool has_mask = a.bitmask != nullptr;
+    const float* E = a.noise + t * (int64_t)a.V + lo;
+    const float* Q = (mode == kDrawResidualQ) ? a.q + d * (int64_t)a.V + lo : nullptr;
+    Part p = part_identity();
+    for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
+        const uint32_t bits = vec_bits<VE>(smask, has_mask, v);
+        if (bits == 0u) continue;
+        float z[VE], ev[VE], qv[VE];
+        Elem<ET>::load(slice, v, z);
+        const int e0 = v * VE;
+        if (a.vec_noise) {
+            // n is a multiple of 4 here, so each 4-id quarter is wholly inside or outside the row
+#pragma unroll
+            for (int h = 0; h < VE / 4; ++h) {
+                float4 f = make_float4(1.f, 1.f, 1.f, 1.f), g = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e0 + 4 * h < n) {
+                    f = __ldcs(reinterpret_cast<const float4*>(E + e0) + h);
+                    if (Q) g = __ldcs(reinterpret_cast<const float4*>(Q + e0) + h);
+                }
+                ev[4 * h] = f.x; ev[4 * h + 1] = f.y; ev[4 * h + 2] = f.z; ev[4 * h + 3] = f.w;
+                qv[4 * h] = g.x; qv[4 * h + 1] = g.y; qv[4 * h + 2] = g.z; qv[4 * h + 3] = g.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const bool in = e0 + e < n;
+                ev[e] = in ? E[e0 + e] : 1.f;
+                qv[e] = (in && Q) ? Q[e0 + e] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+            if (!((bits >> e) & 1u) || !(z[e] > -INFINITY)) continue;
+            const int i = (int)(lo + e0 + e);
+            const float pe = ex2((z[e] - m) * c) * invS;
+            float w = pe;
+            if (mode == kDrawResidualQ) w = fmaxf(pe - qv[e], 0.f);
+            else if (mode == kDrawResidualOneHot && i == x) w = 0.f;
+            if (w > 0.f) {
+                p.flag = 1;
+                const float s = w / ev[e];
+                if (s > p.best) { p.best = s; p.idx = i; }
+            }
+        }
+    }
+    return p;
+}
+
+template <typename ET>
+__global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
+{
+    constexpr int VE = Elem<ET>::VE;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ Shared sh;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = (int)cluster_ctarank();
+    const int b = (int)cluster_id_x();
+    const int64_t lo = (int64_t)rank * a.slice_units * kUnit;
+    const int64_t hi = min((int64_t)a.V, lo + (int64_t)a.slice_units * kUnit);
+    const int n = (int)max((int64_t)0, hi - lo);
+    const int nvec = (n + VE - 1) / VE;
+    const int nw = (n + 31) / 32;
+    unsigned char* slice = dsm;
+    uint32_t* smask = reinterpret_cast<uint32_t*>(dsm + (size_t)a.slice_units * kUnit * sizeof(ET));
+    const bool writer = (rank == 0 && tid == 0);
+
+    if (tid == 0) {
+        for (int c = 0; c < kChunks; ++c) mbar_init(smem_addr(&sh.bars[c]), 1);
+        fence_mbar_init();
+        sh.timed_out = 0;
+    }
+
+    // ---- a1 ragged decode + a4 grammar-valid prefix (warp 0)
+    const int32_t d0 = a.cu[b];
+    const int64_t row0 = (int64_t)d0 + b;
+    if (warp == 0) {
+        const int32_t d1 = a.cu[b + 1], ntot = a.cu[a.B];
+        const bool bad_off = a.cu[0] != 0 || d0 < 0 || d1 < d0 || d1 > ntot;
+        const int k = d1 - d0;
+        const float T = a.temperature[b];
+        const bool tvalid = (T == 0.f) || (T >= FLT_MIN && T <= FLT_MAX);
+        const bool greedy = !(T > 0.f) || !tvalid;
+        const bool qmode = a.q != nullptr && (a.has_q == nullptr || a.has_q[b] != 0);
+        int skip = 0, g = bad_off ? 0 : k;
+        uint32_t st = 0;
+        if (bad_off) { skip = 1; st = SPECDEC_ST_BAD_OFFSETS; }
+        else if (k > a.max_k) { skip = 2; st = SPECDEC_ST_K_TOO_LARGE; }
+        else {
+            bool ok = true, allowed = true;
+            if (lane < k) {
+                const int32_t x = a.draft_ids[d0 + lane];
+                ok = x >= 0 && x < a.V;
+                allowed = ok;
+                if (ok && a.bitmask)
+                    allowed = ((uint32_t)a.bitmask[(row0 + lane) * (int64_t)a.W + (x >> 5)] >> (x & 31)) & 1u;
+                sh.xs[lane] = x;
+                sh.us[lane] = a.uniforms[row0 + lane];
+                sh.qxs[lane] = (qmode && ok && !greedy) ? a.q[(int64_t)(d0 + lane) * a.V + x] : 0.f;
+            }
+            const unsigned inval = __ballot_sync(0xffffffffu, lane < k && !allowed);
+            const unsigned badid = __ballot_sync(0xffffffffu, lane < k && !ok);
+            if (inval) g = __ffs(inval) - 1;
+            if (badid) st |= SPECDEC_ST_BAD_DRAFT_ID;
+            if (!tvalid) st |= SPECDEC_ST_BAD_TEMPERATURE;
+        }
+        if (lane == 0) {
+            sh.k = k; sh.g = g; sh.skip = skip; sh.greedy = greedy; sh.qmode = qmode; sh.st = st;
+        }
+    }
+    __syncthreads();
+
+    const int k = sh.k, g = sh.g, skip = sh.skip;
+    const bool greedy = sh.greedy != 0, qmode = sh.qmode != 0;
+    uint32_t st = sh.st;
+    const float T = a.temperature[b];
+    const float c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);   // log2(e) / T
+
+    if (writer && a.status) a.status[b] = 0u;      // bits are OR-ed in at the end
+    if (writer && skip != 1) {
+        if (a.diag_alpha) for (int j = 0; j < k; ++j) a.diag_alpha[d0 + j] = NAN;
+        if (a.diag_row) for (int j = 0; j <= k; ++j) { a.diag_row[2 * (row0 + j)] = NAN; a.diag_row[2 * (row0 + j) + 1] = NAN; }
+    }
+
+    int acc_len = 0, emitted = -1;
+    uint32_t ph = 0;
+    int slot = 0;
+    if (skip == 0) {
+        acc_len = k;
+        for (int j = 0; j <= k; ++j) {
+            const int64_t t = row0 + j;
+            const int64_t d = (int64_t)d0 + j;
+            const bool bonus = (j == k);
+            const int x = bonus ? -1 : sh.xs[j];
+
+            // ---- a2/a3: stage the row slice (logits + mask words)
+            stage_row<ET>(a, sh, slice, smask, t, lo, n, nvec, nw, ph);
+
+            // ---- a5/a6: one pass over the slice
+            Part p = greedy ? row_pass<ET, true>(a, sh, slice, smask, lo, nvec, c, ph)
+                            : row_pass<ET, false>(a, sh, slice, smask, lo, nvec, c, ph);
+            ph ^= 1u;
+            if (!greedy && !bonus && tid == 0 && x >= lo && x < hi) {
+                float z[VE];
+                Elem<ET>::load(slice, (int)((x - lo) / VE), z);
+                p.zx = z[(x - lo) % VE];
+            }
+            const Part r = cluster_reduce(p, c, sh, slot, a.G);
+            slot ^= 1;
+
+            if (greedy) {
+                if (r.idx == INT_MAX) {                       // nothing allowed in this row
+                    st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
+                    acc_len = j; emitted = -1;
+                    break;
+                }
+                if (writer && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
+                if (bonus) { emitted = r.idx; break; }
+                const bool accept = (j < g) && (x == r.idx);
+                if (writer && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
+                if (accept) { if (writer) a.out_tokens[t] = x; continue; }
+                acc_len = j; emitted = r.idx;                 // recovered = target argmax
+                break;
+            }
+
+            if (r.m == -INFINITY) {
+                st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
+                acc_len = j; emitted = -1;
+                break;
+            }
+            const float m = r.m, S = r.S;
+            if (writer && a.diag_row) { a.diag_row[2 * t] = m / T; a.diag_row[2 * t + 1] = S; }
+            int mode = kDrawP;
+            if (!bonus) {
+                // ---- a7: acceptance probability, a8: strict comparison with the draw
+                float alpha = 0.f;
+                if (j < g) {
+                    const float px = (r.zx > -INFINITY) ? ex2((r.zx - m) * c) / S : 0.f;
+                    if (qmode) {
+                        const float qx = sh.qxs[j];
+                        alpha = (px <= 0.f) ? 0.f : (qx <= px ? 1.f : px / qx);
+                    } else {
+                        alpha = px;
+                    }
+                }
+                if (writer && a.diag_alpha) a.diag_alpha[d] = alpha;
+                if (sh.us[j] < alpha) { if (writer) a.out_tokens[t] = x; continue; }
+                mode = qmode ? kDrawResidualQ : kDrawResidualOneHot;
+            }
+            // ---- a9/a10: recovered or bonus token by exponential race over the staged slice
+            const float invS = 1.f / S;
+            Part dp = draw_pass<ET>(a, slice, smask, lo, n, nvec, t, d, mode, x, m, c, invS);
+            Part dr = cluster_reduce(dp, c, sh, slot, a.G);
+            slot ^= 1;
+            if (mode == kDrawResidualQ && !dr.flag) {        // empty residual: fall back to p
+                dp = draw_pass<ET>(a, slice, smask, lo, n, nvec, t, d, kDrawP, x, m, c, invS);
+                dr = cluster_reduce(dp, c, sh, slot, a.G);
+                slot ^= 1;
+            }
+            emitted = dr.idx == INT_MAX ? -1 : dr.idx;
+            acc_len = j;
+            break;
+        }
+    }
+
+    // ---- a11: emit, count
+    if (writer) {
+        if (skip == 0) {
+            a.out_tokens[row0 + acc_len] = emitted;
+            for (int j = acc_len + 1; j <= k; ++j) a.out_tokens[row0 + j] = -1;
+            atomicAdd(&a.counters[0], (unsigned long long)k);
+            atomicAdd(&a.counters[1], (unsigned long long)(k - g));
+            atomicAdd(&a.counters[2], (unsigned long long)g);
+            atomicAdd(&a.counters[3], (unsigned long long)acc_len);
+        } else if (skip == 2) {
+            for (int j = 0; j <= k; ++j) a.out_tokens[row0 + j] = -1;
+        }
+        a.out_num_accepted[b] = skip == 0 ? acc_len : 0;
+    }
+    __syncthreads();
+    if (sh.timed_out) {
+        st |= SPECDEC_ST_DEVICE_TIMEOUT;
+        // copies that missed their deadline: wait once more (bounded) before the CTA exits
+        if (tid == 0)
+            for (int ch = 0; ch < kChunks; ++ch) (void)mbar_wait_bounded(smem_addr(&sh.bars[ch]), ph ^ 1u);
+    }
+    if (a.status && tid == 0) {
+        if (rank == 0) atomicOr(&a.status[b], st & ~SPECDEC_ST_DEVICE_TIMEOUT);
+        if (st & SPECDEC_ST_DEVICE_TIMEOUT) atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
+    }
+    // no CTA leaves while another may still read its shared memory
+    cluster_sync_all();
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+
+struct LaunchShape {
+    int G, slice_units, smem;
+};
+
+specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, LaunchShape* out)
+{
+    if (V <= 0) return SPECDEC_ERR_INVALID_ARG;
+    if (dt != SPECDEC_F32 && dt != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
+    const int es = dt == SPECDEC_F32 ? 4 : 2;
+    const long long units = ((long long)V + kUnit - 1) / kUnit;
+    const long long row_bytes = (long long)V * es;
+    long long G = (row_bytes + kTargetSliceBytes - 1) / kTargetSliceBytes;
+    if (const char* env = std::getenv("SPECDEC_CTAS_PER_REQUEST")) {     // tuning sweeps
+        const long long forced = std::atoll(env);
+        if (forced >= 1) G = forced;
+    }
+    if (G < 1) G = 1;
+    if (G > kMaxCluster) G = kMaxCluster;
+    if (G > units) G = units;
+    const long long su = (units + G - 1) / G;
+    G = (units + su - 1) / su;                      // no CTA with an empty slice
+    const long long slice_bytes = su * kUnit * es;
+    if (slice_bytes > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
+    out->G = (int)G;
+    out->slice_units = (int)su;
+    out->smem = (int)(slice_bytes + su * (kUnit / 32) * 4);
+    return SPECDEC_OK;
+}
+
+template <typename ET>
+cudaError_t configure_kernel_once()
+{
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(specdec_verify_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxSliceBytes + kMaxSliceBytes / 32 + 1024);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(specdec_verify_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    });
+    return err;
+}
+
+// Largest cluster size <= G that the device can co-schedule with this shared memory.
+template <typename ET>
+int schedulable_cluster(int G, int smem, cudaStream_t stream)
+{
+    for (; G > 1; --G) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)G, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)G;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, specdec_verify_kernel<ET>, &cfg) == cudaSuccess && n > 0) return G;
+        (void)cudaGetLastError();
+    }
+    return 1;
+}
+
+template <typename ET>
+specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream)
+{
+    if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
+    {
+        // the cluster size actually used, cached per (G, smem) request
+        static std::mutex mu;
+        static int cached_req = -1, cached_smem = -1, cached_G = -1;
+        std::lock_guard<std::mutex> lock(mu);
+        if (cached_req != sh.G || cached_smem != sh.smem) {
+            cached_G = schedulable_cluster<ET>(sh.G, sh.smem, stream);
+            cached_req = sh.G;
+            cached_smem = sh.smem;
+        }
+        if (cached_G != sh.G) {
+            // re-slice the row over fewer CTAs; give up if a slice no longer fits on chip
+            const int es = (int)sizeof(ET);
+            const long long units = ((long long)args.V + kUnit - 1) / kUnit;
+            const long long su = (units + cached_G - 1) / cached_G;
+            if (su * kUnit * es > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
+            sh.G = (int)((units + su - 1) / su);
+            sh.slice_units = (int)su;
+            sh.smem = (int)(su * kUnit * es + su * (kUnit / 32) * 4);
+            args.G = sh.G;
+            args.slice_units = sh.slice_units;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B * (unsigned)sh.G, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)sh.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)sh.G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, specdec_verify_kernel<ET>, args);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SPECDEC_ERR_CUDA;
+    }
+    return SPECDEC_OK;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" specdec_status_t specdec_launch_config(int32_t V, specdec_dtype_t logits_dtype,
+                                                  int32_t* ctas_per_request, int32_t* threads_per_cta,
+                                                  int32_t* smem_bytes, int32_t* slice_ids)
+{
+    LaunchShape s;
+    const specdec_status_t rc = shape_for(V, logits_dtype, &s);
+    if (rc != SPECDEC_OK) return rc;
+    if (ctas_per_request) *ctas_per_request = s.G;
+    if (threads_per_cta) *threads_per_cta = kThreads;
+    if (smem_bytes) *smem_bytes = s.smem;
+    if (slice_ids) *slice_ids = s.slice_units * kUnit;
+    return SPECDEC_OK;
+}
+
+extern "C" specdec_status_t specdec_verify(
+    const void* target_logits, specdec_dtype_t logits_dtype, const int32_t* draft_ids,
+    const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
+    int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
+    const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
+    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* stream)
+{
+    if (logits_dtype != SPECDEC_F32 && logits_dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
+    if (B < 0 || V < 1 || max_k < 0 || max_k > SPECDEC_KMAX) return SPECDEC_ERR_INVALID_ARG;
+    if (!target_logits || !draft_ids || !cu_num_draft || !temperature || !uniforms || !exp_noise ||
+        !out_tokens || !out_num_accepted || !counters)
+        return SPECDEC_ERR_INVALID_ARG;
+    const size_t es = logits_dtype == SPECDEC_F32 ? 4 : 2;
+    if (!aligned(target_logits, es) || !aligned(draft_ids, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
+        !aligned(cu_num_draft, 4) || (bitmask && !aligned(bitmask, 4)) || !aligned(temperature, 4) ||
+        !aligned(uniforms, 4) || !aligned(exp_noise, 4) || !aligned(out_tokens, 4) ||
+        !aligned(out_num_accepted, 4) || !aligned(counters, 8) || (status && !aligned(status, 4)) ||
+        (diag_accept_prob && !aligned(diag_accept_prob, 4)) || (diag_row_stats && !aligned(diag_row_stats, 4)))
+        return SPECDEC_ERR_INVALID_ARG;
+    LaunchShape shape;
+    const specdec_status_t rc = shape_for(V, logits_dtype, &shape);
+    if (rc != SPECDEC_OK) return rc;
+    if (B == 0) return SPECDEC_OK;
+    if ((long long)B * shape.G > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
+
+    Args a;
+    a.logits = target_logits;
+    a.draft_ids = draft_ids;
+    a.q = draft_probs;
+    a.has_q = has_q;
+    a.cu = cu_num_draft;
+    a.bitmask = bitmask;
+    a.temperature = temperature;
+    a.uniforms = uniforms;
+    a.noise = exp_noise;
+    a.out_tokens = out_tokens;
+    a.out_num_accepted = out_num_accepted;
+    a.counters = counters;
+    a.status = status;
+    a.diag_alpha = diag_accept_prob;
+    a.diag_row = diag_row_stats;
+    a.B = B;
+    a.V = V;
+    a.max_k = max_k;
+    a.W = (V + 31) / 32;
+    a.slice_units = shape.slice_units;
+    a.G = shape.G;
+    // bulk async copies need 16-byte aligned rows: row pitch and base of logits and bitmask
+    a.bulk = aligned(target_logits, 16) && ((size_t)V * es) % 16 == 0 &&
+             (!bitmask || (aligned(bitmask, 16) && a.W % 4 == 0));
+    a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
+
+    if (logits_dtype == SPECDEC_F32) return launch<float>(a, shape, B, (cudaStream_t)stream);
+    return launch<uint16_t>(a, shape, B, (cudaStream_t)stream);
+}
+
+extern "C" specdec_status_t specdec_wait(void* stream, int32_t timeout_ms)
+{
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (timeout_ms < 0) return cudaStreamSynchronize(s) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+    // poll with a host-side deadline (steady clock via CUDA events is not needed here)
+    struct timespec t0;
+    clock_gettime(CLOCK_MONOTONIC, &t0);
+    while (true) {
+        const cudaError_t e = cudaStreamQuery(s);
+        if (e == cudaSuccess) return SPECDEC_OK;
+        if (e != cudaErrorNotReady) return SPECDEC_ERR_CUDA;
+        struct timespec t1;
+        clock_gettime(CLOCK_MONOTONIC, &t1);
+        const long long ms = (t1.tv_sec - t0.tv_sec) * 1000LL + (t1.tv_nsec - t0.tv_nsec) / 1000000LL;
+        if (ms >= timeout_ms) return SPECDEC_ERR_TIMEOUT;
+        struct timespec nap = {0, 50000};
+        nanosleep(&nap, nullptr);
+    }
+}
+
+extern "C" const char* specdec_status_string(specdec_status_t s)
+{
+    switch (s) {
+    case SPECDEC_OK: return "SPECDEC_OK";
+    case SPECDEC_ERR_INVALID_ARG: return "SPECDEC_ERR_INVALID_ARG";
+    case SPECDEC_ERR_UNSUPPORTED: return "SPECDEC_ERR_UNSUPPORTED";
+    case SPECDEC_ERR_CUDA: return "SPECDEC_ERR_CUDA";
+    case SPECDEC_ERR_TIMEOUT: return "SPECDEC_ERR_TIMEOUT";
+    }
+    return "SPECDEC_UNKNOWN_STATUS";
+}

@@ -1,0 +1,101 @@
+"""Device-side marshalling: copy a host batch to CUDA tensors, allocate the outputs, call
+the library. No arithmetic of the method happens here."""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import numpy as np
+
+from . import _native
+from .workloads import BF16, Workload
+
+INPUT_FIELDS = ("logits", "draft_ids", "draft_probs", "has_q", "cu_num_draft", "bitmask", "temperature",
+                "uniforms", "exp_noise")
+
+
+def _host_tensor(a: np.ndarray, bf16: bool = False):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if bf16:
+        t = t.view(torch.int16).view(torch.bfloat16)
+    return t
+
+
+def host_tensors(w: Workload, pin: bool = False) -> Dict[str, object]:
+    """The batch's inputs as CPU tensors (optionally page-locked for async copies)."""
+    out = {}
+    for f in INPUT_FIELDS:
+        a = getattr(w, f)
+        if a is None:
+            out[f] = None
+            continue
+        t = _host_tensor(a, bf16=(f == "logits" and w.logits_dtype == BF16))
+        out[f] = t.pin_memory() if pin else t
+    return out
+
+
+def device_tensors(w: Workload, device="cuda", host: Optional[Dict[str, object]] = None) -> Dict[str, object]:
+    host = host or host_tensors(w)
+    return {f: (None if t is None else t.to(device, non_blocking=True)) for f, t in host.items()}
+
+
+@dataclasses.dataclass
+class Outputs:
+    out_tokens: object
+    out_num_accepted: object
+    counters: object
+    status: object
+    diag_accept_prob: Optional[object] = None
+    diag_row_stats: Optional[object] = None
+
+    def numpy(self) -> Dict[str, np.ndarray]:
+        d = {"out_tokens": self.out_tokens, "out_num_accepted": self.out_num_accepted,
+             "counters": self.counters, "status": self.status}
+        if self.diag_accept_prob is not None:
+            d["diag_accept_prob"] = self.diag_accept_prob
+            d["diag_row_stats"] = self.diag_row_stats
+        res = {}
+        for k, t in d.items():
+            t = t.cpu()
+            if k == "counters":
+                res[k] = t.view(dtype=__import__("torch").int64).numpy().view(np.uint64).copy()
+            elif k == "status":
+                res[k] = t.numpy().view(np.uint32).copy()
+            else:
+                res[k] = t.numpy().copy()
+        return res
+
+
+def alloc_outputs(w: Workload, device="cuda", diag: bool = False) -> Outputs:
+    import torch
+
+    return Outputs(
+        out_tokens=torch.full((w.T,), -7, dtype=torch.int32, device=device),
+        out_num_accepted=torch.full((w.B,), -7, dtype=torch.int32, device=device),
+        counters=torch.zeros(4, dtype=torch.int64, device=device),
+        status=torch.zeros(w.B, dtype=torch.int32, device=device),
+        diag_accept_prob=torch.empty(max(w.N, 1), dtype=torch.float32, device=device) if diag else None,
+        diag_row_stats=torch.empty((max(w.T, 1), 2), dtype=torch.float32, device=device) if diag else None,
+    )
+
+
+def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> None:
+    """Queue one verify of batch `w` whose inputs are already in `dev`."""
+    _native.specdec_verify(
+        dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
+        w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
+        out.out_tokens, out.out_num_accepted, out.counters, out.status,
+        out.diag_accept_prob, out.diag_row_stats, stream=stream)
+
+
+def run(w: Workload, device="cuda", diag: bool = True) -> Dict[str, np.ndarray]:
+    """Copy, verify, synchronise, and return the outputs as numpy arrays."""
+    import torch
+
+    dev = device_tensors(w, device)
+    out = alloc_outputs(w, device, diag=diag)
+    verify(w, dev, out)
+    torch.cuda.synchronize()
+    return out.numpy()

@@ -24,7 +24,9 @@ Every tensor has its own substream ``numpy.random.default_rng([seed, tag])``.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from typing import Optional, Sequence
 
 import numpy as np
@@ -50,11 +52,30 @@ _TAGS = {
     "exp_noise": 14,
 }
 
-_ROW_BLOCK = 256  # rows generated per block for the [T, V] tensors
+_ROW_BLOCK = 64  # rows generated per block (one substream each) for the [T, V] tensors
 
 
-def substream(seed: int, tag: str) -> np.random.Generator:
-    return np.random.default_rng([int(seed), _TAGS[tag]])
+def substream(seed: int, tag: str, block: Optional[int] = None) -> np.random.Generator:
+    """Substream of one tensor; tensors generated in row blocks get one substream per block."""
+    if block is None:
+        return np.random.default_rng([int(seed), _TAGS[tag]])
+    return np.random.default_rng([int(seed), _TAGS[tag], int(block)])
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def _for_blocks(n: int, block: int, fn) -> None:
+    """fn(block_index, r0, r1) over [0, n) in blocks, on a thread pool (results do not depend
+    on the thread count: every block draws from its own substream)."""
+    starts = list(range(0, n, block))
+    if len(starts) <= 1 or _threads() == 1:
+        for i, r0 in enumerate(starts):
+            fn(i, r0, min(n, r0 + block))
+        return
+    with concurrent.futures.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        list(ex.map(lambda i: fn(i, starts[i], min(n, starts[i] + block)), range(len(starts))))
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -280,15 +301,17 @@ def make_batch(
         masked_req[substream(seed, "mask_pick").permutation(B)[: B // 2]] = True
 
     # ---- target logits
-    rng_l = substream(seed, "logits")
     if logits_dtype == BF16:
         logits = np.empty((T, V), dtype=np.uint16)
     else:
         logits = np.empty((T, V), dtype=np.float32)
-    for r0 in range(0, T, _ROW_BLOCK):
-        r1 = min(T, r0 + _ROW_BLOCK)
-        blk = rng_l.standard_normal(size=(r1 - r0, V), dtype=np.float32) * np.float32(logit_sigma)
+
+    def _gen_logits(i, r0, r1):
+        blk = substream(seed, "logits", i).standard_normal(size=(r1 - r0, V), dtype=np.float32)
+        blk *= np.float32(logit_sigma)
         logits[r0:r1] = f32_to_bf16_bits(blk) if logits_dtype == BF16 else blk
+
+    _for_blocks(T, _ROW_BLOCK, _gen_logits)
 
     def stored_logits(rows):
         return bf16_bits_to_f32(logits[rows]) if logits_dtype == BF16 else logits[rows]
@@ -299,72 +322,94 @@ def make_batch(
     if mask != "none":
         W = (V + 31) // 32
         bitmask = np.full((T, W), -1, dtype=np.int32)   # all-ones rows (bits >= V set too)
-        rng_m = substream(seed, "mask")
-        for t in range(T):
-            if masked_req[req_of_row[t]]:
-                a = _mask_row(rng_m, V, mask_density, mask_run_len, mask_run_frac)
+        masked_rows = [t for t in range(T) if masked_req[req_of_row[t]]]
+
+        def _gen_masks(i, r0, r1):
+            for t in masked_rows[r0:r1]:
+                a = _mask_row(substream(seed, "mask", t), V, mask_density, mask_run_len, mask_run_frac)
                 allowed_rows[t] = a
                 bitmask[t] = pack_mask_rows(a[None, :])[0]
+
+        _for_blocks(len(masked_rows), _ROW_BLOCK, _gen_masks)
 
     # ---- drafts (and draft probabilities q)
     draft_ids = np.zeros(N, dtype=np.int32)
     q_any = bool(has_q_req.any())
     draft_probs = np.zeros((N, V), dtype=np.float32) if q_any else None
-    rng_dn = substream(seed, "draft_logit_noise")
-    rng_ds = substream(seed, "draft_sample")
-    rng_da = substream(seed, "draft_argmax_pick")
-    rng_du = substream(seed, "draft_uniform_id")
-    rng_fi = substream(seed, "forced_invalid")
     req_of_draft = np.repeat(np.arange(B), kk)
-    for d0 in range(0, N, _ROW_BLOCK):
-        d1 = min(N, d0 + _ROW_BLOCK)
+
+    def _gen_drafts(bi, d0, d1):
+        nb = d1 - d0
+        rng_dn = substream(seed, "draft_logit_noise", bi)
+        rng_ds = substream(seed, "draft_sample", bi)
+        rng_da = substream(seed, "draft_argmax_pick", bi)
+        rng_du = substream(seed, "draft_uniform_id", bi)
+        rng_fi = substream(seed, "forced_invalid", bi)
         rows = row_of_draft[d0:d1]
+        reqs = req_of_draft[d0:d1]
         z = stored_logits(rows).astype(np.float64)
-        noise = rng_dn.standard_normal(size=(d1 - d0, V)) * draft_sigma
-        v_sample = rng_ds.random(size=d1 - d0)
-        pick_arg = rng_da.random(size=d1 - d0) < mf_argmax_frac
-        v_uid = rng_du.random(size=d1 - d0)
-        forced = rng_fi.random(size=d1 - d0) < forced_invalid_frac
-        v_forced = rng_fi.random(size=d1 - d0)
-        for i in range(d1 - d0):
-            d = d0 + i
-            b = req_of_draft[d]
-            t = rows[i]
-            allowed = allowed_rows.get(t)
-            if has_q_req[b]:
-                tq = float(temps[b]) if (draft_temperature == "request" and temps[b] > 0) else 1.0
-                s = (z[i] + noise[i]) / tq
-                if allowed is not None:
-                    s = np.where(allowed, s, -np.inf)
-                q = _softmax_rows_f64(s[None, :])[0]
-                draft_probs[d] = q.astype(np.float32)
-                cdf = np.cumsum(q)
-                x = int(np.searchsorted(cdf, v_sample[i] * cdf[-1], side="right"))
-                x = min(x, V - 1)
-                while q[x] <= 0.0:       # guard against the cdf tail: take the last allowed id
-                    x -= 1
-            else:
-                if pick_arg[i]:
-                    zz = z[i] if allowed is None else np.where(allowed, z[i], -np.inf)
-                    x = int(np.argmax(zz))
-                elif allowed is None:
-                    x = int(v_uid[i] * V)
-                else:
-                    ids = np.flatnonzero(allowed)
-                    x = int(ids[int(v_uid[i] * ids.size)])
-            if allowed is not None and forced[i]:
-                bad = np.flatnonzero(~allowed)
-                if bad.size:
-                    x = int(bad[int(v_forced[i] * bad.size)])
-            draft_ids[d] = min(max(x, 0), V - 1)
+        noise = rng_dn.standard_normal(size=(nb, V), dtype=np.float32) * np.float32(draft_sigma)
+        v_sample = rng_ds.random(size=nb)
+        pick_arg = rng_da.random(size=nb) < mf_argmax_frac
+        v_uid = rng_du.random(size=nb)
+        forced = rng_fi.random(size=nb) < forced_invalid_frac
+        v_forced = rng_fi.random(size=nb)
+        allowed = np.ones((nb, V), dtype=bool)
+        has_mask = np.zeros(nb, dtype=bool)
+        for i, t in enumerate(rows):
+            a = allowed_rows.get(int(t))
+            if a is not None:
+                allowed[i] = a
+                has_mask[i] = True
+        x = np.zeros(nb, dtype=np.int64)
+        qsel = has_q_req[reqs]
+        if qsel.any():
+            tq = np.where((temps[reqs] > 0) & (draft_temperature == "request"), temps[reqs], 1.0)[qsel]
+            s_ = (z[qsel] + noise[qsel]) / tq[:, None]
+            s_ = np.where(allowed[qsel], s_, -np.inf)
+            s_ -= s_.max(axis=1, keepdims=True)
+            q = np.exp(s_)
+            q /= q.sum(axis=1, keepdims=True)
+            draft_probs[d0:d1][qsel] = q.astype(np.float32)
+            cdf = np.cumsum(q, axis=1)
+            thr = v_sample[qsel] * cdf[:, -1]
+            xq = np.minimum((cdf <= thr[:, None]).sum(axis=1), V - 1)
+            # guard against the cdf tail landing on a zero-probability id: take the last positive one
+            zero = q[np.arange(q.shape[0]), xq] <= 0.0
+            if zero.any():
+                for r in np.flatnonzero(zero):
+                    xq[r] = int(np.flatnonzero(q[r] > 0.0)[-1])
+            x[qsel] = xq
+        msel = ~qsel
+        if msel.any():
+            zz = np.where(allowed[msel], z[msel], -np.inf)
+            x_arg = np.argmax(zz, axis=1)
+            cnt = allowed[msel].sum(axis=1)
+            target = np.floor(v_uid[msel] * cnt).astype(np.int64) + 1
+            cs = np.cumsum(allowed[msel], axis=1)
+            x_uni = (cs < target[:, None]).sum(axis=1)
+            x[msel] = np.where(pick_arg[msel], x_arg, x_uni)
+        fsel = forced & has_mask
+        if fsel.any():
+            bad = ~allowed[fsel]
+            cnt = bad.sum(axis=1)
+            target = np.floor(v_forced[fsel] * cnt).astype(np.int64) + 1
+            cs = np.cumsum(bad, axis=1)
+            xf = (cs < target[:, None]).sum(axis=1)
+            x[fsel] = np.where(cnt > 0, xf, x[fsel])
+        draft_ids[d0:d1] = np.clip(x, 0, V - 1)
+
+    _for_blocks(N, _ROW_BLOCK, _gen_drafts)
 
     # ---- random numbers consumed by the verifier
     uniforms = uniforms_from_bits(substream(seed, "uniforms").integers(0, 2 ** 32, size=T, dtype=np.uint32))
     exp_noise = np.empty((T, V), dtype=np.float32)
-    rng_e = substream(seed, "exp_noise")
-    for r0 in range(0, T, _ROW_BLOCK):
-        r1 = min(T, r0 + _ROW_BLOCK)
-        exp_noise[r0:r1] = exp1_from_bits(rng_e.integers(0, 2 ** 32, size=(r1 - r0, V), dtype=np.uint32))
+
+    def _gen_noise(i, r0, r1):
+        bits = substream(seed, "exp_noise", i).integers(0, 2 ** 32, size=(r1 - r0, V), dtype=np.uint32)
+        exp_noise[r0:r1] = exp1_from_bits(bits)
+
+    _for_blocks(T, _ROW_BLOCK, _gen_noise)
 
     has_q = None
     if q_any and not has_q_req.all():

@@ -1,0 +1,113 @@
+"""The C-ABI library loads, exports every symbol include/specdec.h declares, and rejects bad
+arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_specdec_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specdec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if build.needs_rebuild():
+        build.build_library()
+    return _native.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(specdec_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(_native.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "SPECDEC_OK"), (1, "SPECDEC_ERR_INVALID_ARG"), (2, "SPECDEC_ERR_UNSUPPORTED"),
+                       (3, "SPECDEC_ERR_CUDA"), (4, "SPECDEC_ERR_TIMEOUT")]:
+        assert _native.status_string(code) == name
+
+
+@pytest.mark.parametrize("V,dtype", [(1, 0), (8, 0), (37, 1), (1000, 0), (32000, 0), (128256, 0), (151936, 0),
+                                     (151936, 1), (262144, 1), (786432, 0)])
+def test_launch_config_covers_the_row(lib, V, dtype):
+    c = _native.launch_config(V, dtype)
+    G, sl = c["ctas_per_request"], c["slice_ids"]
+    assert 1 <= G <= 16 and sl % 128 == 0
+    assert G * sl >= V and (G - 1) * sl < V          # every CTA owns a non-empty slice
+    es = 4 if dtype == 0 else 2
+    assert c["smem_bytes"] >= sl * es and c["smem_bytes"] <= 200 * 1024
+    assert c["threads_per_cta"] == 256
+
+
+def test_launch_config_rejects(lib):
+    with pytest.raises(_native.SpecdecError) as e:
+        _native.launch_config(0, 0)
+    assert e.value.status == _native.SPECDEC_ERR_INVALID_ARG
+    with pytest.raises(_native.SpecdecError) as e:
+        _native.launch_config(1000, 5)
+    assert e.value.status == _native.SPECDEC_ERR_UNSUPPORTED
+    with pytest.raises(_native.SpecdecError) as e:
+        _native.launch_config(4 * 1024 * 1024, 0)     # a 16 MiB row cannot be staged on chip
+    assert e.value.status == _native.SPECDEC_ERR_UNSUPPORTED
+
+
+def _call(lib, **over):
+    # fake, aligned, non-NULL device addresses: every case below fails (or returns) before any
+    # CUDA call, so nothing is dereferenced
+    a = dict(logits=4096, dtype=0, ids=4096, q=None, has_q=None, cu=4096, B=4, V=1000, max_k=3, mask=None,
+             temp=4096, u=4096, noise=4096, out=4096, acc=4096, ctr=4096, status=None, da=None, dr=None)
+    a.update(over)
+    return lib.specdec_verify(a["logits"], a["dtype"], a["ids"], a["q"], a["has_q"], a["cu"], a["B"], a["V"],
+                              a["max_k"], a["mask"], a["temp"], a["u"], a["noise"], a["out"], a["acc"],
+                              a["ctr"], a["status"], a["da"], a["dr"], None)
+
+
+def test_host_validation(lib):
+    E = _native
+    assert _call(lib, B=0) == E.SPECDEC_OK                        # empty batch: nothing launched
+    assert _call(lib, B=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, V=0) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, max_k=33) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, max_k=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, dtype=2) == E.SPECDEC_ERR_UNSUPPORTED
+    for k in ("logits", "ids", "cu", "temp", "u", "noise", "out", "acc", "ctr"):
+        assert _call(lib, **{k: None}) == E.SPECDEC_ERR_INVALID_ARG, k
+    assert _call(lib, logits=4098) == E.SPECDEC_ERR_INVALID_ARG   # fp32 logits not 4-byte aligned
+    assert _call(lib, dtype=1, logits=4098, B=0) == E.SPECDEC_OK  # bf16 needs 2-byte alignment only
+    assert _call(lib, ctr=4100) == E.SPECDEC_ERR_INVALID_ARG      # counters need 8-byte alignment
+    assert _call(lib, mask=4097) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
+
+
+def test_product_path_has_no_oracle_import():
+    """The package never imports, links or runs the oracle (test infrastructure only)."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_specdec_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "specdec_ref" not in text, f
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        saved = _native._lib
+        _native._lib = None
+        try:
+            _native.load(str(tmp_path / "nope.so"))
+        finally:
+            _native._lib = saved

@@ -1,0 +1,238 @@
+"""GPU library vs CPU oracle, element by element, through the C ABI (needs a GB300)."""
+import dataclasses
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+import oracle
+from oracle import parity
+from speculative_decoding_verification_specdec_gb300 import _native, build, device
+from speculative_decoding_verification_specdec_gb300 import workloads as W
+
+from _hand import batch, rows_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    if build.needs_rebuild():
+        build.build_library()
+    _native.load()
+    torch.cuda.set_device(0)
+    return "cuda:0"
+
+
+def check_parity(w, cuda, label=""):
+    got = device.run(w, device=cuda, diag=True)
+    ref = oracle.verify(w)
+    rep = parity.compare(w, got, ref)
+    assert not (got["status"] & _native.ST_DEVICE_TIMEOUT).any()
+    assert rep.ok, (f"{label or w.name}: {rep.summary()} tokens={rep.token_mismatches[:8]} "
+                    f"acc={rep.accepted_mismatches[:8]} status={rep.status_mismatches[:8]} "
+                    f"alpha={rep.alpha_bad[:5]} rows={rep.row_bad[:5]}")
+    return rep, got, ref
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3])
+def test_config_parity(cuda, cfg):
+    w = W.config(cfg)
+    rep, got, ref = check_parity(w, cuda)
+    print(f"config {cfg} {w.name}: {rep.summary()} counters={list(ref['counters'])}")
+    assert rep.excluded_requests <= max(1, w.B // 50)
+
+
+def test_config4_full_size_parity(cuda):
+    w = W.config(4)
+    rep, got, ref = check_parity(w, cuda)
+    print(f"config 4 {w.name}: {rep.summary()} counters={list(ref['counters'])}")
+    assert rep.excluded_requests <= max(1, w.B // 50)
+
+
+SWEEP = [
+    # V, dtype, B, k range, q_mode, temperature, mask
+    (1, W.F32, 9, (0, 3), "none", "half_greedy(0.5,1.2)", "none"),
+    (7, W.BF16, 11, (0, 4), "half", 0.9, "all"),
+    (37, W.F32, 17, (0, 6), "all", "uniform(0.3,1.5)", "half"),
+    (128, W.F32, 13, (1, 5), "half", "half_greedy(0.5,1.2)", "all"),
+    (129, W.BF16, 13, (1, 5), "none", 1.0, "half"),
+    (1000, W.BF16, 21, (0, 8), "all", "half_greedy(0.5,1.2)", "none"),
+    (1001, W.F32, 21, (0, 8), "half", 0.7, "all"),
+    (5000, W.F32, 33, (2, 6), "all", "uniform(0.5,1.2)", "half"),
+    (12345, W.BF16, 33, (0, 7), "half", "half_greedy(0.5,1.2)", "half"),
+    (40000, W.F32, 29, (1, 8), "none", "uniform(0.5,2.0)", "all"),
+    (70008, W.BF16, 40, (1, 8), "half", "half_greedy(0.5,1.2)", "half"),
+    (131072, W.F32, 24, (3, 6), "all", 0.8, "all"),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SWEEP)))
+def test_sweep_parity(cuda, case):
+    V, dt, B, kr, qm, temp, mask = SWEEP[case]
+    w = W.make_batch(100 + case, name=f"sweep{case}_V{V}", B=B, V=V, k=kr, logits_dtype=dt, logit_sigma=3.0,
+                     temperature=temp, q_mode=qm, draft_sigma=0.5, mask=mask, mask_density=0.1,
+                     mask_run_len=16 if V > 64 else 2, forced_invalid_frac=0.2, max_k=8)
+    check_parity(w, cuda)
+
+
+@pytest.mark.parametrize("ctas", ["1", "3", "16"])
+def test_forced_cluster_shapes(cuda, ctas, monkeypatch):
+    monkeypatch.setenv("SPECDEC_CTAS_PER_REQUEST", ctas)
+    w = W.make_batch(200, name=f"ctas{ctas}", B=20, V=9000, k=(0, 6), logits_dtype=W.F32, logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
+                     mask_density=0.1, mask_run_len=16, forced_invalid_frac=0.2)
+    check_parity(w, cuda)
+
+
+def test_edge_cases_match_oracle(cuda):
+    rng = np.random.default_rng(5)
+    V = 8
+    cases = []
+    z = rng.normal(0, 1, size=(3, V)).astype(np.float32)
+    cases.append(batch(V=V, ks=[0, 0, 0], logits=z, draft_ids=[], temperature=0.0, max_k=0, name="k0_greedy"))
+    cases.append(batch(V=V, ks=[0, 0, 0], logits=z, draft_ids=[], temperature=1.1, max_k=0, name="k0_random"))
+    zz = np.tile(np.arange(V, dtype=np.float32), (4, 1))
+    allowed = np.ones((4, V), dtype=bool)
+    allowed[1] = False
+    for temp in (0.0, 0.8):
+        cases.append(batch(V=V, ks=[3], logits=zz, draft_ids=[V - 1] * 3, temperature=temp, allowed=allowed,
+                           name=f"empty_row_T{temp}"))
+        cases.append(batch(V=V, ks=[2], logits=zz[:3], draft_ids=[V - 1, V], temperature=temp, name=f"bad_id_T{temp}"))
+        cases.append(batch(V=V, ks=[2], logits=zz[:3], draft_ids=[-5, 1], temperature=temp, name=f"neg_id_T{temp}"))
+    for bad in (-1.0, float("nan"), float("inf"), 1e-40):
+        cases.append(batch(V=V, ks=[1, 2], logits=rng.normal(size=(5, V)), draft_ids=[1, 2, 3],
+                           temperature=[bad, 0.9], name=f"bad_T_{bad}"))
+    cases.append(batch(V=V, ks=[1, 3], logits=rng.normal(size=(6, V)), draft_ids=[0, 1, 2, 3], temperature=0.0,
+                       max_k=2, name="k_too_large"))
+    w = batch(V=V, ks=[2, 1], logits=rng.normal(size=(5, V)), draft_ids=[0, 1, 2], temperature=0.7, name="bad_offsets")
+    w.cu_num_draft[:] = [0, 4, 3]
+    cases.append(w)
+    zi = np.full((2, V), -np.inf, dtype=np.float32)
+    zi[:, 5] = 0.0
+    for temp in (0.0, 1.0):
+        cases.append(batch(V=V, ks=[1], logits=zi, draft_ids=[2], temperature=temp, name=f"neg_inf_T{temp}"))
+    # strict u < alpha at alpha = 1/2 exactly (V = 2, equal logits, one-hot draft)
+    w = batch(V=2, ks=[1, 1], logits=np.zeros((4, 2)), draft_ids=[0, 0], temperature=1.0, name="strict")
+    w.uniforms[[0, 2]] = [np.float32(0.5 - 2.0 ** -24), np.float32(0.5)]
+    cases.append(w)
+    # grammar-invalid draft with u = 0
+    al = np.ones((2, 2), dtype=bool)
+    al[0, 1] = False
+    w = batch(V=2, ks=[1], logits=np.zeros((2, 2)), draft_ids=[1], temperature=1.0,
+              q=np.array([[0.5, 0.5]], dtype=np.float32), allowed=al, name="invalid_u0")
+    w.uniforms[:] = 0.0
+    cases.append(w)
+    # p == q exactly (uniform on 4 allowed ids): every draft accepted at the largest draw
+    al = np.zeros((5, 16), dtype=bool)
+    al[:, [1, 4, 9, 15]] = True
+    q = np.zeros((4, 16), dtype=np.float32)
+    q[:, [1, 4, 9, 15]] = 0.25
+    w = batch(V=16, ks=[4], logits=np.full((5, 16), 3.0), draft_ids=[4, 9, 1, 15], temperature=0.6, q=q,
+              allowed=al, name="p_equals_q")
+    w.uniforms[:] = np.float32(1.0 - 2.0 ** -24)
+    cases.append(w)
+    for w in cases:
+        _, got, ref = check_parity(w, cuda, label=w.name)
+        if w.name == "p_equals_q":
+            assert got["out_num_accepted"][0] == 4
+        if w.name == "strict":
+            assert list(got["out_num_accepted"]) == [1, 0]
+
+
+def test_rows_after_stop_are_never_read(cuda):
+    w = W.make_batch(300, B=40, V=3000, k=(2, 6), logits_dtype=W.F32, logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
+                     mask_density=0.2, mask_run_len=16, forced_invalid_frac=0.2)
+    ref = oracle.verify(w)
+    poisoned = dataclasses.replace(w, logits=w.logits.copy(), exp_noise=w.exp_noise.copy(),
+                                   bitmask=w.bitmask.copy())
+    cu = w.cu_num_draft
+    n_poisoned = 0
+    for b in range(w.B):
+        k = int(cu[b + 1] - cu[b])
+        for j in range(int(ref["out_num_accepted"][b]) + 1, k + 1):
+            t = rows_of(cu, b, j)
+            poisoned.logits[t] = np.nan
+            poisoned.exp_noise[t] = np.nan
+            poisoned.bitmask[t] = 0
+            n_poisoned += 1
+    assert n_poisoned > 20
+    got = device.run(poisoned, device=cuda, diag=True)
+    rep = parity.compare(w, got, ref)
+    assert rep.ok, rep.summary()
+    # the library reports which rows it read: exactly rows 0..a_b of each request
+    read = np.isfinite(got["diag_row_stats"][: w.T, 0]) | (got["diag_row_stats"][: w.T, 0] == -np.inf)
+    for b in range(w.B):
+        k = int(cu[b + 1] - cu[b])
+        a = int(ref["out_num_accepted"][b])
+        for j in range(k + 1):
+            assert read[rows_of(cu, b, j)] == (j <= a), (b, j, a)
+
+
+def test_counters_accumulate_and_runs_are_deterministic(cuda):
+    import torch
+
+    w = W.make_batch(400, B=64, V=4096, k=(1, 6), logit_sigma=3.0, temperature="half_greedy(0.5,1.2)",
+                     q_mode="half", draft_sigma=0.5, mask="half", mask_density=0.1, mask_run_len=16,
+                     forced_invalid_frac=0.2)
+    dev = device.device_tensors(w, cuda)
+    out = device.alloc_outputs(w, cuda, diag=True)
+    device.verify(w, dev, out)
+    torch.cuda.synchronize()
+    first = out.numpy()
+    device.verify(w, dev, out)
+    torch.cuda.synchronize()
+    second = out.numpy()
+    assert np.array_equal(second["counters"], 2 * first["counters"])
+    for key in ("out_tokens", "out_num_accepted", "status"):
+        assert np.array_equal(first[key], second[key])
+    assert np.array_equal(first["diag_accept_prob"], second["diag_accept_prob"], equal_nan=True)
+
+
+def test_runs_on_a_side_stream(cuda):
+    import torch
+
+    w = W.make_batch(500, B=16, V=20000, k=(1, 4), logit_sigma=3.0, temperature=0.9, q_mode="all",
+                     draft_sigma=0.5)
+    dev = device.device_tensors(w, cuda)
+    torch.cuda.synchronize()
+    out = device.alloc_outputs(w, cuda, diag=True)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        device.verify(w, dev, out, stream=s)
+    _native.specdec_wait(s, timeout_ms=60000)
+    got = out.numpy()
+    ref = oracle.verify(w)
+    assert parity.compare(w, got, ref).ok
+
+
+def test_chi_square_on_gpu(cuda):
+    """The kernel's first emitted token is distributed as the target p (V = 8, 10^6 requests)."""
+    import _pins
+
+    n, V = 1_000_000, 8
+    z0 = np.array([1.5, -0.5, 0.3, 2.2, -1.0, 0.0, 1.1, -2.0])
+    z1 = np.array([-0.2, 0.9, 1.7, -1.3, 0.4, 2.0, -0.7, 0.1])
+    q0 = np.array([0.05, 0.20, 0.10, 0.05, 0.25, 0.05, 0.10, 0.20])
+    allow = np.ones(V, dtype=bool)
+    allow[[1, 5]] = False
+    variants = {
+        "draft_model": (_pins._chi2_batch(n, np.stack([z0, z1]), 1.0, "q", q_rows=q0[None, :], seed=71), z0, 1.0, None, 2),
+        "draft_model_masked": (_pins._chi2_batch(n, np.stack([z0, z1]), 0.7, "q", q_rows=q0[None, :],
+                                                 allowed_rows=np.stack([allow, allow]), seed=72), z0, 0.7, allow, 2),
+        "model_free": (_pins._chi2_batch(n, np.stack([z0, z1]), 1.0, "mf", x_fixed=[3], seed=73), z0, 1.0, None, 2),
+        "bonus_only": (_pins._chi2_batch(n, z1[None, :], 1.3, "mf", x_fixed=[], seed=74), z1, 1.3, None, 1),
+    }
+    for name, (w, z, T, al, stride) in variants.items():
+        got = device.run(w, device=cuda, diag=False)
+        first = got["out_tokens"][0::stride]
+        p = _pins._target_p(z, T, al)
+        chi2, df = _pins._chi2(np.bincount(first, minlength=V), p)
+        assert chi2 < stats.chi2.ppf(0.999, df), (name, chi2)
+        ref = oracle.verify(w)
+        rep = parity.compare(w, got, ref)
+        assert rep.ok, (name, rep.summary())
