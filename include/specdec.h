@@ -68,7 +68,8 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * library allocates nothing and keeps no state between calls.
  *
  *   target_logits  [T, V] row-major, fp32 or bf16 (logits_dtype); 4- resp. 2-byte aligned.
- *   draft_ids      [N] int32.
+ *   draft_ids      [N] int32; may be NULL when N = 0 (a request that does have drafts then
+ *                  gets SPECDEC_ST_BAD_DRAFT_ID and all its drafts count as invalid).
  *   draft_probs    [N, V] fp32 draft distributions q, or NULL (every request model-free).
  *                  Only q(x) of each tested draft and the q row of a rejected position are read.
  *   has_q          [B] uint8 or NULL (NULL: every request is a draft-model request iff
@@ -97,7 +98,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * Rows after a request's first rejection are never read.
  * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
  * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
- * pointer, B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
+ * pointer (draft_ids may be NULL), B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
  * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype or a row wider than the on-chip
  * staging allows (V * element size > 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
  */

@@ -29,10 +29,12 @@ ST_BAD_OFFSETS = 16
 
 def build(src: str = _SRC, out: str = _LIB, extra_flags=(), quiet: bool = True) -> str:
     """Compile the oracle (gcc, plain C11) into a shared library; returns its path."""
-    cmd = ["gcc", *_CFLAGS, *extra_flags, "-o", out, src, "-lm"]
+    tmp = f"{out}.tmp{os.getpid()}"
+    cmd = ["gcc", *_CFLAGS, *extra_flags, "-o", tmp, src, "-lm"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"oracle build failed: {' '.join(cmd)}\n{res.stderr}")
+    os.replace(tmp, out)
     if not quiet and res.stderr:
         print(res.stderr)
     return out

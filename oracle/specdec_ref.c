@@ -217,7 +217,7 @@ static void verify_request(ref_call* c, int32_t b)
      * outside [0, V) is treated like a forbidden draft and flagged. */
     int32_t g = k;
     for (int32_t j = 0; j < k; ++j) {
-        int32_t x = c->draft_ids[lo + j];
+        int32_t x = c->draft_ids ? c->draft_ids[lo + j] : -1;   /* no id array: every draft invalid */
         int ok = (x >= 0 && x < c->V);
         if (!ok) st |= REF_ST_BAD_DRAFT_ID;
         if (g == k && (!ok || !grammar_allows(c, row0 + j, x))) g = j;
@@ -237,7 +237,7 @@ static void verify_request(ref_call* c, int32_t b)
         const int64_t t = row0 + j;
         const int64_t d = (int64_t)lo + j;
         const int is_bonus = (j == k);
-        const int32_t x = is_bonus ? -1 : c->draft_ids[d];
+        const int32_t x = (is_bonus || !c->draft_ids) ? -1 : c->draft_ids[d];
         const int x_ok = !is_bonus && x >= 0 && x < c->V;
 
         int32_t live = masked_row(c, t);
@@ -309,7 +309,7 @@ int specdec_verify_ref(
     if (B < 0 || V <= 0 || max_k < 0 || max_k > 32) return 1;
     if (logits_dtype != REF_LOGITS_F32 && logits_dtype != REF_LOGITS_BF16) return 1;
     if (B == 0) return 0;
-    if (!target_logits || !draft_ids || !cu_num_draft || !temperature || !uniforms ||
+    if (!target_logits || !cu_num_draft || !temperature || !uniforms ||
         !exp_noise || !out_tokens || !out_num_accepted || !counters)
         return 1;
 

@@ -66,7 +66,7 @@ typedef struct {
  * R, I, D, A are accumulated (added to), never cleared. */
 int specdec_verify_ref(
     const void* target_logits, int32_t logits_dtype,   /* [T, V] */
-    const int32_t* draft_ids,                          /* [N] */
+    const int32_t* draft_ids,                          /* [N]; NULL allowed (then every draft is invalid) */
     const float* draft_probs,                          /* [N, V] or NULL */
     const uint8_t* has_q,                              /* [B] or NULL */
     const int32_t* cu_num_draft,                       /* [B+1] */

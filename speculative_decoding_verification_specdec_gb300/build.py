@@ -26,10 +26,12 @@ def nvcc() -> str:
 
 
 def build_library(out: str = LIB_PATH, extra_flags=(), verbose: bool = False) -> str:
-    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-o", out, *SOURCES]
+    tmp = f"{out}.tmp{os.getpid()}"          # write then rename: concurrent builders never see a partial file
+    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-o", tmp, *SOURCES]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed ({' '.join(cmd)}):\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, out)
     if verbose:
         print(res.stdout, res.stderr)
     return out

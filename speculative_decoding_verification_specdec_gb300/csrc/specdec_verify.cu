@@ -504,7 +504,7 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
         else {
             bool ok = true, allowed = true;
             if (lane < k) {
-                const int32_t x = a.draft_ids[d0 + lane];
+                const int32_t x = a.draft_ids ? a.draft_ids[d0 + lane] : -1;
                 ok = x >= 0 && x < a.V;
                 allowed = ok;
                 if (ok && a.bitmask)
@@ -794,11 +794,11 @@ extern "C" specdec_status_t specdec_verify(
 {
     if (logits_dtype != SPECDEC_F32 && logits_dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     if (B < 0 || V < 1 || max_k < 0 || max_k > SPECDEC_KMAX) return SPECDEC_ERR_INVALID_ARG;
-    if (!target_logits || !draft_ids || !cu_num_draft || !temperature || !uniforms || !exp_noise ||
+    if (!target_logits || !cu_num_draft || !temperature || !uniforms || !exp_noise ||
         !out_tokens || !out_num_accepted || !counters)
         return SPECDEC_ERR_INVALID_ARG;
     const size_t es = logits_dtype == SPECDEC_F32 ? 4 : 2;
-    if (!aligned(target_logits, es) || !aligned(draft_ids, 4) || (draft_probs && !aligned(draft_probs, 4)) ||
+    if (!aligned(target_logits, es) || (draft_ids && !aligned(draft_ids, 4)) || (draft_probs && !aligned(draft_probs, 4)) ||
         !aligned(cu_num_draft, 4) || (bitmask && !aligned(bitmask, 4)) || !aligned(temperature, 4) ||
         !aligned(uniforms, 4) || !aligned(exp_noise, 4) || !aligned(out_tokens, 4) ||
         !aligned(out_num_accepted, 4) || !aligned(counters, 8) || (status && !aligned(status, 4)) ||

@@ -83,7 +83,8 @@ def test_host_validation(lib):
     assert _call(lib, max_k=33) == E.SPECDEC_ERR_INVALID_ARG
     assert _call(lib, max_k=-1) == E.SPECDEC_ERR_INVALID_ARG
     assert _call(lib, dtype=2) == E.SPECDEC_ERR_UNSUPPORTED
-    for k in ("logits", "ids", "cu", "temp", "u", "noise", "out", "acc", "ctr"):
+    assert _call(lib, ids=None, B=0) == E.SPECDEC_OK                # no drafts: the id array may be NULL
+    for k in ("logits", "cu", "temp", "u", "noise", "out", "acc", "ctr"):
         assert _call(lib, **{k: None}) == E.SPECDEC_ERR_INVALID_ARG, k
     assert _call(lib, logits=4098) == E.SPECDEC_ERR_INVALID_ARG   # fp32 logits not 4-byte aligned
     assert _call(lib, dtype=1, logits=4098, B=0) == E.SPECDEC_OK  # bf16 needs 2-byte alignment only
