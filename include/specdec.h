@@ -92,7 +92,8 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *   diag_accept_prob [N] fp32 or NULL: alpha of every draft that was tested, NaN otherwise.
  *   diag_row_stats [T, 2] fp32 or NULL: for every row read, (m, S) with m = max_i z_i / T
  *                  and S = sum_i exp(z_i / T - m) on random requests, (max_i z_i, NaN) on
- *                  greedy ones; (NaN, NaN) for rows not read.
+ *                  greedy ones; (NaN, NaN) for rows not read. Entries of a request skipped
+ *                  for SPECDEC_ST_BAD_OFFSETS are left untouched (its rows are unknown).
  *   stream         a cudaStream_t (NULL = legacy default stream).
  *
  * Rows after a request's first rejection are never read.

@@ -76,8 +76,8 @@ def alloc_outputs(w: Workload, device="cuda", diag: bool = False) -> Outputs:
         out_num_accepted=torch.full((w.B,), -7, dtype=torch.int32, device=device),
         counters=torch.zeros(4, dtype=torch.int64, device=device),
         status=torch.zeros(w.B, dtype=torch.int32, device=device),
-        diag_accept_prob=torch.empty(max(w.N, 1), dtype=torch.float32, device=device) if diag else None,
-        diag_row_stats=torch.empty((max(w.T, 1), 2), dtype=torch.float32, device=device) if diag else None,
+        diag_accept_prob=torch.full((max(w.N, 1),), float("nan"), dtype=torch.float32, device=device) if diag else None,
+        diag_row_stats=torch.full((max(w.T, 1), 2), float("nan"), dtype=torch.float32, device=device) if diag else None,
     )
 
 
