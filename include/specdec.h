@@ -100,8 +100,13 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
  * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
  * pointer (draft_ids may be NULL), B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
- * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype or a row wider than the on-chip
- * staging allows (V * element size > 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
+ * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype (or, with the cluster kernel that
+ * keeps each row slice on chip, a row wider than 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
+ *
+ * Kernels: by default one CTA verifies one request, streaming its rows through a ring of
+ * 32 KB shared-memory stages filled by bulk async copies. Setting the environment variable
+ * SPECDEC_KERNEL=cluster selects the alternative kernel (one thread-block cluster per request,
+ * each CTA holding a slice of every row); both compute identical results.
  */
 specdec_status_t specdec_verify(
     const void* target_logits, specdec_dtype_t logits_dtype,

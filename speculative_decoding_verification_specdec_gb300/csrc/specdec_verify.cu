@@ -35,6 +35,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
 #include <ctime>
 #include <mutex>
 
@@ -650,11 +651,502 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
 }
 
 // ---------------------------------------------------------------------------------------------
+// streaming kernel: one CTA per request, warp-specialised ring of bulk async copies
+// ---------------------------------------------------------------------------------------------
+//
+// Warp 0 is the producer: lane 0 issues cp.async.bulk copies of 32 KB chunks (logits + mask
+// words of a row; or logits + noise + q + mask words of the draw row) into a ring of kStages
+// shared-memory stages, each with a "full" and an "empty" mbarrier. Warps 1..8 consume chunk
+// by chunk, reduce across the CTA at the end of a row, and post the decision (next row / draw
+// / done) through a shared word and a "decision" mbarrier. While a decision is pending the
+// producer has already queued up to kSpec chunks of the next row, so HBM keeps streaming
+// across row boundaries; if the request stops, the consumers drain those chunks unused.
+// No cross-CTA synchronisation exists on this path: every reduction is inside one CTA.
+
+constexpr int kConsumers = 256;
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kStreamThreads = kConsumers + 32;
+constexpr int kStageBytes = 32 * 1024;
+constexpr int kStages = 3;
+constexpr int kSpec = 2;
+
+enum : int { kDecNextRow = 1, kDecDrawP = 2, kDecDrawQ = 3, kDecDrawOneHot = 4, kDecDone = 5 };
+
+template <typename ET> struct Geom {
+    static constexpr int ES = (int)sizeof(ET);
+    // ids per chunk, multiples of kUnit; a row chunk holds logits + mask words, a draw chunk
+    // logits + noise + q + mask words
+    static constexpr int kRowIds = ((kStageBytes * 8) / (ES * 8 + 1)) / kUnit * kUnit;
+    static constexpr int kDrawIds = ((kStageBytes * 8) / ((ES + 8) * 8 + 1)) / kUnit * kUnit;
+    static constexpr int kRowMaskOff = kRowIds * ES;
+    static constexpr int kDrawNoiseOff = kDrawIds * ES;
+    static constexpr int kDrawQOff = kDrawIds * (ES + 4);
+    static constexpr int kDrawMaskOff = kDrawIds * (ES + 8);
+    static_assert(kRowMaskOff + kRowIds / 8 <= kStageBytes, "row chunk overflows a stage");
+    static_assert(kDrawMaskOff + kDrawIds / 8 <= kStageBytes, "draw chunk overflows a stage");
+    static_assert(kRowMaskOff % 16 == 0 && kDrawNoiseOff % 16 == 0 && kDrawQOff % 16 == 0 &&
+                  kDrawMaskOff % 16 == 0, "stage sections must be 16-byte aligned");
+};
+
+struct StreamShared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t dec;
+    Part wpart[2][kConsumerWarps];
+    int32_t xs[SPECDEC_KMAX];
+    float us[SPECDEC_KMAX];
+    float qxs[SPECDEC_KMAX];
+    int32_t k, g, skip, greedy, qmode, timed_out, dec_code;
+    uint32_t st;
+    float c;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory");
+}
+
+// The request's offsets, checked the same way by producer and consumers.
+struct ReqShape {
+    int32_t d0, k, skip;   // skip: 0 ok, 1 bad offsets, 2 k > max_k
+    int64_t row0;
+};
+
+__device__ __forceinline__ ReqShape request_shape(const Args& a, int b)
+{
+    ReqShape r;
+    const int32_t d0 = a.cu[b], d1 = a.cu[b + 1], ntot = a.cu[a.B];
+    r.d0 = d0;
+    r.k = d1 - d0;
+    r.row0 = (int64_t)d0 + b;
+    r.skip = (a.cu[0] != 0 || d0 < 0 || d1 < d0 || d1 > ntot) ? 1 : (r.k > a.max_k ? 2 : 0);
+    return r;
+}
+
+template <typename ET>
+struct Producer {
+    const Args& a;
+    StreamShared& sh;
+    unsigned char* ring;
+    uint32_t it = 0;
+    int lane;
+
+    __device__ Producer(const Args& a_, StreamShared& s_, unsigned char* r_, int lane_)
+        : a(a_), sh(s_), ring(r_), lane(lane_) {}
+
+    __device__ __forceinline__ int acquire()
+    {
+        const int s = (int)(it % kStages);
+        const uint32_t par = ((it / kStages) & 1u) ^ 1u;
+        if (!mbar_wait_bounded(smem_addr(&sh.empty[s]), par)) sh.timed_out = 1;
+        return s;
+    }
+
+    // chunk c of logits row t (+ its mask words)
+    __device__ __forceinline__ void row_chunk(int64_t t, int c)
+    {
+        using G = Geom<ET>;
+        const int s = acquire();
+        unsigned char* st = ring + (size_t)s * kStageBytes;
+        const int64_t i0 = (int64_t)c * G::kRowIds;
+        const int n = (int)min((int64_t)G::kRowIds, (int64_t)a.V - i0);
+        const ET* src = reinterpret_cast<const ET*>(a.logits) + t * (int64_t)a.V + i0;
+        const int32_t* msrc = a.bitmask ? a.bitmask + t * (int64_t)a.W + (i0 >> 5) : nullptr;
+        const int nw = (n + 31) / 32;
+        if (a.bulk) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                const uint32_t bar = smem_addr(&sh.full[s]);
+                const uint32_t lb = (uint32_t)n * G::ES, mb = msrc ? (uint32_t)nw * 4u : 0u;
+                mbar_arrive_expect_tx(bar, lb + mb);
+                bulk_copy_g2s(smem_addr(st), src, lb, bar);
+                if (mb) bulk_copy_g2s(smem_addr(st + G::kRowMaskOff), msrc, mb, bar);
+            }
+        } else {
+            constexpr int VE = Elem<ET>::VE;
+            const int npad = (n + VE - 1) / VE * VE;
+            ET* d = reinterpret_cast<ET*>(st);
+            ET pad;
+            if constexpr (sizeof(ET) == 4) pad = -INFINITY; else pad = (ET)0xFF80u;
+            for (int e = lane; e < npad; e += 32) d[e] = e < n ? src[e] : pad;
+            if (msrc) {
+                uint32_t* dm = reinterpret_cast<uint32_t*>(st + G::kRowMaskOff);
+                for (int w = lane; w < nw; w += 32) dm[w] = (uint32_t)msrc[w];
+            }
+            mbar_arrive(smem_addr(&sh.full[s]));     // every lane arrives after its own stores
+        }
+        ++it;
+    }
+
+    // chunk c of the draw row t (draft slot d): logits, noise, q (with_q), mask words
+    __device__ __forceinline__ void draw_chunk(int64_t t, int64_t d, int c, bool with_q)
+    {
+        using G = Geom<ET>;
+        const int s = acquire();
+        unsigned char* st = ring + (size_t)s * kStageBytes;
+        const int64_t i0 = (int64_t)c * G::kDrawIds;
+        const int n = (int)min((int64_t)G::kDrawIds, (int64_t)a.V - i0);
+        const ET* src = reinterpret_cast<const ET*>(a.logits) + t * (int64_t)a.V + i0;
+        const float* esrc = a.noise + t * (int64_t)a.V + i0;
+        const float* qsrc = with_q ? a.q + d * (int64_t)a.V + i0 : nullptr;
+        const int32_t* msrc = a.bitmask ? a.bitmask + t * (int64_t)a.W + (i0 >> 5) : nullptr;
+        const int nw = (n + 31) / 32;
+        if (a.bulk) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                const uint32_t bar = smem_addr(&sh.full[s]);
+                const uint32_t lb = (uint32_t)n * G::ES, eb = (uint32_t)n * 4u;
+                const uint32_t qb = qsrc ? eb : 0u, mb = msrc ? (uint32_t)nw * 4u : 0u;
+                mbar_arrive_expect_tx(bar, lb + eb + qb + mb);
+                bulk_copy_g2s(smem_addr(st), src, lb, bar);
+                bulk_copy_g2s(smem_addr(st + G::kDrawNoiseOff), esrc, eb, bar);
+                if (qb) bulk_copy_g2s(smem_addr(st + G::kDrawQOff), qsrc, qb, bar);
+                if (mb) bulk_copy_g2s(smem_addr(st + G::kDrawMaskOff), msrc, mb, bar);
+            }
+        } else {
+            constexpr int VE = Elem<ET>::VE;
+            const int npad = (n + VE - 1) / VE * VE;
+            ET* dl = reinterpret_cast<ET*>(st);
+            float* de = reinterpret_cast<float*>(st + G::kDrawNoiseOff);
+            float* dq = reinterpret_cast<float*>(st + G::kDrawQOff);
+            ET pad;
+            if constexpr (sizeof(ET) == 4) pad = -INFINITY; else pad = (ET)0xFF80u;
+            for (int e = lane; e < npad; e += 32) {
+                const bool in = e < n;
+                dl[e] = in ? src[e] : pad;
+                de[e] = in ? esrc[e] : 1.f;
+                dq[e] = (in && qsrc) ? qsrc[e] : 0.f;
+            }
+            if (msrc) {
+                uint32_t* dm = reinterpret_cast<uint32_t*>(st + G::kDrawMaskOff);
+                for (int w = lane; w < nw; w += 32) dm[w] = (uint32_t)msrc[w];
+            }
+            mbar_arrive(smem_addr(&sh.full[s]));
+        }
+        ++it;
+    }
+};
+
+template <typename ET>
+__global__ void __launch_bounds__(kStreamThreads) specdec_verify_stream_kernel(const Args a)
+{
+    using G = Geom<ET>;
+    constexpr int VE = Elem<ET>::VE;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ StreamShared sh;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const int nrow_chunks = (a.V + G::kRowIds - 1) / G::kRowIds;
+    const int ndraw_chunks = (a.V + G::kDrawIds - 1) / G::kDrawIds;
+    // at least one chunk of the next row is issued only after the pending decision was read,
+    // so consumers can never post two decisions ahead of the producer
+    const int spec = min(kSpec, nrow_chunks - 1);
+
+    if (tid == 0) {
+        const uint32_t full_count = a.bulk ? 1u : 32u;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&sh.full[s]), full_count);
+            mbar_init(smem_addr(&sh.empty[s]), kConsumerWarps);
+        }
+        mbar_init(smem_addr(&sh.dec), 1);
+        fence_mbar_init();
+        sh.timed_out = 0;
+    }
+    __syncthreads();
+
+    const ReqShape rs = request_shape(a, b);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (rs.skip == 0) {
+            Producer<ET> pr(a, sh, ring, lane);
+            uint32_t dec_round = 0;
+            int issued_next = 0;
+            for (int j = 0; j <= rs.k; ++j) {
+                const int64_t t = rs.row0 + j;
+                for (int c = issued_next; c < nrow_chunks; ++c) pr.row_chunk(t, c);
+                issued_next = 0;
+                if (j < rs.k) {
+                    for (int c = 0; c < spec; ++c) pr.row_chunk(t + 1, c);
+                    issued_next = spec;
+                }
+                if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
+                ++dec_round;
+                int code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                if (code == kDecNextRow) continue;
+                while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
+                    for (int c = 0; c < ndraw_chunks; ++c) pr.draw_chunk(t, (int64_t)rs.d0 + j, c, code == kDecDrawQ);
+                    if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
+                    ++dec_round;
+                    code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                }
+                break;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int ct = tid - 32, cw = warp - 1;
+        const bool leader = (ct == 0);
+        if (cw == 0) {
+            // a1 ragged decode + a4 grammar-valid prefix (one consumer warp)
+            const float T = a.temperature[b];
+            const bool tvalid = (T == 0.f) || (T >= FLT_MIN && T <= FLT_MAX);
+            const bool greedy = !(T > 0.f) || !tvalid;
+            const bool qmode = a.q != nullptr && (a.has_q == nullptr || a.has_q[b] != 0);
+            int g = rs.skip == 1 ? 0 : rs.k;
+            uint32_t st = rs.skip == 1 ? SPECDEC_ST_BAD_OFFSETS : (rs.skip == 2 ? SPECDEC_ST_K_TOO_LARGE : 0u);
+            if (rs.skip == 0) {
+                bool ok = true, allowed = true;
+                if (lane < rs.k) {
+                    const int32_t x = a.draft_ids ? a.draft_ids[rs.d0 + lane] : -1;
+                    ok = x >= 0 && x < a.V;
+                    allowed = ok;
+                    if (ok && a.bitmask)
+                        allowed = ((uint32_t)a.bitmask[(rs.row0 + lane) * (int64_t)a.W + (x >> 5)] >> (x & 31)) & 1u;
+                    sh.xs[lane] = x;
+                    sh.us[lane] = a.uniforms[rs.row0 + lane];
+                    sh.qxs[lane] = (qmode && ok && !greedy) ? a.q[(int64_t)(rs.d0 + lane) * a.V + x] : 0.f;
+                }
+                const unsigned inval = __ballot_sync(0xffffffffu, lane < rs.k && !allowed);
+                const unsigned badid = __ballot_sync(0xffffffffu, lane < rs.k && !ok);
+                if (inval) g = __ffs(inval) - 1;
+                if (badid) st |= SPECDEC_ST_BAD_DRAFT_ID;
+                if (!tvalid) st |= SPECDEC_ST_BAD_TEMPERATURE;
+            }
+            if (lane == 0) {
+                sh.g = g; sh.greedy = greedy; sh.qmode = qmode; sh.st = st;
+                sh.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);   // log2(e) / T, once
+            }
+        }
+        consumer_sync();
+        const int k = rs.k, g = sh.g;
+        const bool greedy = sh.greedy != 0, qmode = sh.qmode != 0;
+        const float c = sh.c;
+        const float T = a.temperature[b];
+        uint32_t st = sh.st;
+        const bool has_mask = a.bitmask != nullptr;
+
+        if (leader) {
+            if (rs.skip != 1) {
+                if (a.diag_alpha) for (int j = 0; j < k; ++j) a.diag_alpha[rs.d0 + j] = NAN;
+                if (a.diag_row)
+                    for (int j = 0; j <= k; ++j) { a.diag_row[2 * (rs.row0 + j)] = NAN; a.diag_row[2 * (rs.row0 + j) + 1] = NAN; }
+            }
+        }
+
+        uint32_t it = 0;
+        int par = 0;
+        auto wait_full = [&]() -> int {
+            const int s = (int)(it % kStages);
+            if (!mbar_wait_bounded(smem_addr(&sh.full[s]), (it / kStages) & 1u)) sh.timed_out = 1;
+            return s;
+        };
+        auto release = [&](int s) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&sh.empty[s]));
+            ++it;
+        };
+        auto reduce = [&](Part p) -> Part {
+            p = warp_reduce(p, c);
+            if (lane == 0) sh.wpart[par][cw] = p;
+            consumer_sync();
+            Part r = part_identity();
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], c);
+            par ^= 1;
+            return r;
+        };
+        auto post = [&](int code) {
+            if (leader) {
+                *reinterpret_cast<volatile int*>(&sh.dec_code) = code;
+                mbar_arrive(smem_addr(&sh.dec));
+            }
+        };
+
+        int acc_len = 0, emitted = -1;
+        if (rs.skip == 0) {
+            acc_len = k;
+            for (int j = 0; j <= k; ++j) {
+                const int64_t t = rs.row0 + j;
+                const int64_t d = (int64_t)rs.d0 + j;
+                const bool bonus = (j == k);
+                const int x = bonus ? -1 : sh.xs[j];
+
+                // ---- a2/a3/a5/a6: stream the row chunk by chunk
+                Part p = part_identity();
+                for (int ch = 0; ch < nrow_chunks; ++ch) {
+                    const int s = wait_full();
+                    const unsigned char* stg = ring + (size_t)s * kStageBytes;
+                    const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::kRowMaskOff);
+                    const int64_t i0 = (int64_t)ch * G::kRowIds;
+                    const int n = (int)min((int64_t)G::kRowIds, (int64_t)a.V - i0);
+                    const int nvec = (n + VE - 1) / VE;
+                    for (int v = ct; v < nvec; v += kConsumers) {
+                        const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
+                        if (bits == 0u) continue;
+                        float z[VE];
+                        Elem<ET>::load(stg, v, z);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
+                        const int i = (int)(i0 + (int64_t)v * VE);
+                        if (greedy) {
+#pragma unroll
+                            for (int e = 0; e < VE; ++e)
+                                if (z[e] > p.best) { p.best = z[e]; p.idx = i + e; }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < VE; ++e)
+                                if (i + e == x) p.zx = z[e];
+                            float vm = z[0];
+#pragma unroll
+                            for (int e = 1; e < VE; ++e) vm = fmaxf(vm, z[e]);
+                            if (vm == -INFINITY) continue;
+                            if (vm > p.m) {
+                                p.S = (p.m == -INFINITY) ? 0.f : p.S * ex2((p.m - vm) * c);
+                                p.m = vm;
+                            }
+                            float sacc = 0.f;
+#pragma unroll
+                            for (int e = 0; e < VE; ++e) sacc += ex2((z[e] - p.m) * c);
+                            p.S += sacc;
+                        }
+                    }
+                    release(s);
+                }
+                const Part r = reduce(p);
+
+                // ---- decision (identical in every consumer thread)
+                int code = kDecDone;
+                bool stop = true;
+                if (greedy) {
+                    if (r.idx == INT_MAX) {
+                        st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                        if (leader && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
+                        acc_len = j; emitted = -1;
+                    } else {
+                        if (leader && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
+                        if (bonus) {
+                            emitted = r.idx;
+                        } else {
+                            const bool accept = (j < g) && (x == r.idx);
+                            if (leader && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
+                            if (accept) { if (leader) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                            else { acc_len = j; emitted = r.idx; }
+                        }
+                    }
+                } else if (r.m == -INFINITY) {
+                    st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                    if (leader && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
+                    acc_len = j; emitted = -1;
+                } else {
+                    if (leader && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
+                    code = kDecDrawP;
+                    if (!bonus) {
+                        float alpha = 0.f;
+                        if (j < g) {
+                            const float px = (r.zx > -INFINITY) ? ex2((r.zx - r.m) * c) / r.S : 0.f;
+                            if (qmode) {
+                                const float qx = sh.qxs[j];
+                                alpha = (px <= 0.f) ? 0.f : (qx <= px ? 1.f : px / qx);
+                            } else {
+                                alpha = px;
+                            }
+                        }
+                        if (leader && a.diag_alpha) a.diag_alpha[d] = alpha;
+                        if (sh.us[j] < alpha) { if (leader) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                        else code = qmode ? kDecDrawQ : kDecDrawOneHot;
+                    }
+                }
+                post(code);
+                if (!stop) continue;
+
+                // drain the chunks of row j+1 the producer queued before this decision
+                if (j < k)
+                    for (int ch = 0; ch < spec; ++ch) release(wait_full());
+
+                // ---- a9/a10: draw pass(es) over the stop / bonus row
+                while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
+                    const float invS = 1.f / r.S;
+                    Part dp = part_identity();
+                    for (int ch = 0; ch < ndraw_chunks; ++ch) {
+                        const int s = wait_full();
+                        const unsigned char* stg = ring + (size_t)s * kStageBytes;
+                        const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::kDrawMaskOff);
+                        const float* se = reinterpret_cast<const float*>(stg + G::kDrawNoiseOff);
+                        const float* sq = reinterpret_cast<const float*>(stg + G::kDrawQOff);
+                        const int64_t i0 = (int64_t)ch * G::kDrawIds;
+                        const int n = (int)min((int64_t)G::kDrawIds, (int64_t)a.V - i0);
+                        const int nvec = (n + VE - 1) / VE;
+                        for (int v = ct; v < nvec; v += kConsumers) {
+                            const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
+                            if (bits == 0u) continue;
+                            float z[VE];
+                            Elem<ET>::load(stg, v, z);
+                            const int e0 = v * VE;
+#pragma unroll
+                            for (int e = 0; e < VE; ++e) {
+                                if (!((bits >> e) & 1u) || !(z[e] > -INFINITY)) continue;
+                                const int i = (int)(i0 + e0 + e);
+                                const float pe = ex2((z[e] - r.m) * c) * invS;
+                                float w = pe;
+                                if (code == kDecDrawQ) w = fmaxf(pe - sq[e0 + e], 0.f);
+                                else if (code == kDecDrawOneHot && i == x) w = 0.f;
+                                if (w > 0.f) {
+                                    dp.flag = 1;
+                                    const float sc = w / se[e0 + e];
+                                    if (sc > dp.best) { dp.best = sc; dp.idx = i; }
+                                }
+                            }
+                        }
+                        release(s);
+                    }
+                    const Part dr = reduce(dp);
+                    if (code == kDecDrawQ && !dr.flag) { code = kDecDrawP; post(code); continue; }   // empty residual
+                    emitted = dr.idx == INT_MAX ? -1 : dr.idx;
+                    post(kDecDone);
+                    break;
+                }
+                acc_len = j;
+                break;
+            }
+        }
+
+        // ---- a11: emit, count
+        if (leader) {
+            if (rs.skip == 0) {
+                a.out_tokens[rs.row0 + acc_len] = emitted;
+                for (int j = acc_len + 1; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
+                atomicAdd(&a.counters[0], (unsigned long long)k);
+                atomicAdd(&a.counters[1], (unsigned long long)(k - g));
+                atomicAdd(&a.counters[2], (unsigned long long)g);
+                atomicAdd(&a.counters[3], (unsigned long long)acc_len);
+            } else if (rs.skip == 2) {
+                for (int j = 0; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
+            }
+            a.out_num_accepted[b] = rs.skip == 0 ? acc_len : 0;
+        }
+        if (leader && a.status) {
+            // status word written at the top of this block; all this CTA's bits land here
+            a.status[b] = st;
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && sh.timed_out && a.status) atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
 
 struct LaunchShape {
-    int G, slice_units, smem;
+    int stream;             // 1: one CTA per request (streaming ring); 0: one cluster per request
+    int G, slice_units, smem, threads;
 };
 
 specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, LaunchShape* out)
@@ -675,10 +1167,22 @@ specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, LaunchShape* out)
     const long long su = (units + G - 1) / G;
     G = (units + su - 1) / su;                      // no CTA with an empty slice
     const long long slice_bytes = su * kUnit * es;
+    const char* kind = std::getenv("SPECDEC_KERNEL");                // comparison runs
+    const bool cluster = kind && std::strcmp(kind, "cluster") == 0;
+    if (!cluster) {
+        out->stream = 1;
+        out->G = 1;
+        out->slice_units = (int)units;
+        out->smem = kStages * kStageBytes;
+        out->threads = kStreamThreads;
+        return SPECDEC_OK;
+    }
     if (slice_bytes > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
+    out->stream = 0;
     out->G = (int)G;
     out->slice_units = (int)su;
     out->smem = (int)(slice_bytes + su * (kUnit / 32) * 4);
+    out->threads = kThreads;
     return SPECDEC_OK;
 }
 
@@ -692,6 +1196,9 @@ cudaError_t configure_kernel_once()
                                    kMaxSliceBytes + kMaxSliceBytes / 32 + 1024);
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(specdec_verify_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStages * kStageBytes);
     });
     return err;
 }
@@ -724,6 +1231,11 @@ template <typename ET>
 specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream)
 {
     if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
+    if (sh.stream) {
+        specdec_verify_stream_kernel<ET><<<(unsigned)B, kStreamThreads, (size_t)sh.smem, stream>>>(args);
+        const cudaError_t err = cudaGetLastError();
+        return err == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+    }
     {
         // the cluster size actually used, cached per (G, smem) request
         static std::mutex mu;
@@ -779,7 +1291,7 @@ extern "C" specdec_status_t specdec_launch_config(int32_t V, specdec_dtype_t log
     const specdec_status_t rc = shape_for(V, logits_dtype, &s);
     if (rc != SPECDEC_OK) return rc;
     if (ctas_per_request) *ctas_per_request = s.G;
-    if (threads_per_cta) *threads_per_cta = kThreads;
+    if (threads_per_cta) *threads_per_cta = s.threads;
     if (smem_bytes) *smem_bytes = s.smem;
     if (slice_ids) *slice_ids = s.slice_units * kUnit;
     return SPECDEC_OK;
@@ -833,8 +1345,10 @@ extern "C" specdec_status_t specdec_verify(
     a.slice_units = shape.slice_units;
     a.G = shape.G;
     // bulk async copies need 16-byte aligned rows: row pitch and base of logits and bitmask
+    // (the streaming kernel also bulk-copies noise and q rows: their bases must be aligned too)
     a.bulk = aligned(target_logits, 16) && ((size_t)V * es) % 16 == 0 &&
-             (!bitmask || (aligned(bitmask, 16) && a.W % 4 == 0));
+             (!bitmask || (aligned(bitmask, 16) && a.W % 4 == 0)) && aligned(exp_noise, 16) &&
+             (!draft_probs || aligned(draft_probs, 16));
     a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
 
     if (logits_dtype == SPECDEC_F32) return launch<float>(a, shape, B, (cudaStream_t)stream);

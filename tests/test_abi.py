@@ -42,17 +42,23 @@ def test_status_strings(lib):
 
 @pytest.mark.parametrize("V,dtype", [(1, 0), (8, 0), (37, 1), (1000, 0), (32000, 0), (128256, 0), (151936, 0),
                                      (151936, 1), (262144, 1), (786432, 0)])
-def test_launch_config_covers_the_row(lib, V, dtype):
+@pytest.mark.parametrize("kernel", ["stream", "cluster"])
+def test_launch_config_covers_the_row(lib, V, dtype, kernel, monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", kernel)
     c = _native.launch_config(V, dtype)
     G, sl = c["ctas_per_request"], c["slice_ids"]
     assert 1 <= G <= 16 and sl % 128 == 0
     assert G * sl >= V and (G - 1) * sl < V          # every CTA owns a non-empty slice
     es = 4 if dtype == 0 else 2
-    assert c["smem_bytes"] >= sl * es and c["smem_bytes"] <= 200 * 1024
-    assert c["threads_per_cta"] == 256
+    if kernel == "cluster":
+        assert c["smem_bytes"] >= sl * es and c["smem_bytes"] <= 200 * 1024
+        assert c["threads_per_cta"] == 256
+    else:
+        assert G == 1 and c["smem_bytes"] == 3 * 32 * 1024 and c["threads_per_cta"] == 288
 
 
-def test_launch_config_rejects(lib):
+def test_launch_config_rejects(lib, monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
     with pytest.raises(_native.SpecdecError) as e:
         _native.launch_config(0, 0)
     assert e.value.status == _native.SPECDEC_ERR_INVALID_ARG
@@ -62,6 +68,8 @@ def test_launch_config_rejects(lib):
     with pytest.raises(_native.SpecdecError) as e:
         _native.launch_config(4 * 1024 * 1024, 0)     # a 16 MiB row cannot be staged on chip
     assert e.value.status == _native.SPECDEC_ERR_UNSUPPORTED
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")   # the streaming kernel has no row-size limit
+    assert _native.launch_config(4 * 1024 * 1024, 0)["ctas_per_request"] == 1
 
 
 def _call(lib, **over):
@@ -75,7 +83,8 @@ def _call(lib, **over):
                               a["ctr"], a["status"], a["da"], a["dr"], None)
 
 
-def test_host_validation(lib):
+def test_host_validation(lib, monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
     E = _native
     assert _call(lib, B=0) == E.SPECDEC_OK                        # empty batch: nothing launched
     assert _call(lib, B=-1) == E.SPECDEC_ERR_INVALID_ARG

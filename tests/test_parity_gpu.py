@@ -38,15 +38,24 @@ def check_parity(w, cuda, label=""):
     return rep, got, ref
 
 
+KERNELS = ["stream", "cluster"]
+
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3])
-def test_config_parity(cuda, cfg):
+def test_config_parity(cuda, cfg, kernel):
     w = W.config(cfg)
     rep, got, ref = check_parity(w, cuda)
     print(f"config {cfg} {w.name}: {rep.summary()} counters={list(ref['counters'])}")
     assert rep.excluded_requests <= max(1, w.B // 50)
 
 
-def test_config4_full_size_parity(cuda):
+def test_config4_full_size_parity(cuda, kernel):
     w = W.config(4)
     rep, got, ref = check_parity(w, cuda)
     print(f"config 4 {w.name}: {rep.summary()} counters={list(ref['counters'])}")
@@ -71,7 +80,7 @@ SWEEP = [
 
 
 @pytest.mark.parametrize("case", range(len(SWEEP)))
-def test_sweep_parity(cuda, case):
+def test_sweep_parity(cuda, case, kernel):
     V, dt, B, kr, qm, temp, mask = SWEEP[case]
     w = W.make_batch(100 + case, name=f"sweep{case}_V{V}", B=B, V=V, k=kr, logits_dtype=dt, logit_sigma=3.0,
                      temperature=temp, q_mode=qm, draft_sigma=0.5, mask=mask, mask_density=0.1,
@@ -81,6 +90,7 @@ def test_sweep_parity(cuda, case):
 
 @pytest.mark.parametrize("ctas", ["1", "3", "16"])
 def test_forced_cluster_shapes(cuda, ctas, monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
     monkeypatch.setenv("SPECDEC_CTAS_PER_REQUEST", ctas)
     w = W.make_batch(200, name=f"ctas{ctas}", B=20, V=9000, k=(0, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
@@ -88,7 +98,7 @@ def test_forced_cluster_shapes(cuda, ctas, monkeypatch):
     check_parity(w, cuda)
 
 
-def test_edge_cases_match_oracle(cuda):
+def test_edge_cases_match_oracle(cuda, kernel):
     rng = np.random.default_rng(5)
     V = 8
     cases = []
@@ -143,7 +153,7 @@ def test_edge_cases_match_oracle(cuda):
             assert list(got["out_num_accepted"]) == [1, 0]
 
 
-def test_rows_after_stop_are_never_read(cuda):
+def test_rows_after_stop_are_never_read(cuda, kernel):
     w = W.make_batch(300, B=40, V=3000, k=(2, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
                      mask_density=0.2, mask_run_len=16, forced_invalid_frac=0.2)
@@ -173,7 +183,7 @@ def test_rows_after_stop_are_never_read(cuda):
             assert read[rows_of(cu, b, j)] == (j <= a), (b, j, a)
 
 
-def test_counters_accumulate_and_runs_are_deterministic(cuda):
+def test_counters_accumulate_and_runs_are_deterministic(cuda, kernel):
     import torch
 
     w = W.make_batch(400, B=64, V=4096, k=(1, 6), logit_sigma=3.0, temperature="half_greedy(0.5,1.2)",
@@ -210,7 +220,7 @@ def test_runs_on_a_side_stream(cuda):
     assert parity.compare(w, got, ref).ok
 
 
-def test_chi_square_on_gpu(cuda):
+def test_chi_square_on_gpu(cuda, kernel):
     """The kernel's first emitted token is distributed as the target p (V = 8, 10^6 requests)."""
     import _pins
 
