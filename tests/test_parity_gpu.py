@@ -153,6 +153,37 @@ def test_edge_cases_match_oracle(cuda, kernel):
             assert list(got["out_num_accepted"]) == [1, 0]
 
 
+def test_mixed_density_rows(cuda, kernel):
+    """Rows of one request with different mask densities (all-ones, 5 %, one id, none) on an aligned
+    layout, so that requests run the sparse or dense path and meet rows of the other kind."""
+    rng = np.random.default_rng(77)
+    V, B = 131072, 12
+    ks = [5] * B
+    T = 6 * B
+    allowed = np.zeros((T, V), dtype=bool)
+    kinds = rng.integers(0, 4, size=T)
+    for t in range(T):
+        if kinds[t] == 0:
+            allowed[t] = True
+        elif kinds[t] == 1:
+            allowed[t, rng.choice(V, size=V // 20, replace=False)] = True
+        elif kinds[t] == 2:
+            allowed[t, rng.integers(0, V)] = True
+    logits = rng.normal(0, 3, size=(T, V)).astype(np.float32)
+    drafts = []
+    for b in range(B):
+        for j in range(5):
+            t = 6 * b + j
+            ids = np.flatnonzero(allowed[t])
+            z = np.where(allowed[t], logits[t], -np.inf)
+            drafts.append(int(np.argmax(z)) if ids.size and rng.random() < 0.7 else int(rng.integers(0, V)))
+    for dt in (W.F32, W.BF16):
+        for temp in (0.0, 0.9):
+            w = batch(V=V, ks=ks, logits=logits, draft_ids=drafts, temperature=temp, allowed=allowed, seed=3, dtype=dt,
+                      name=f"mixed_{dt}_{temp}")
+            check_parity(w, cuda)
+
+
 def test_rows_after_stop_are_never_read(cuda, kernel):
     w = W.make_batch(300, B=40, V=3000, k=(2, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
