@@ -415,7 +415,7 @@ def main():
                "sample": f"first {sub.B} of {w.B} requests ({sub.N} drafts), one pass, {dt:.1f} s"}
 
     if rank == 0:
-        shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0)
+        shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0, B=w.B)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True,

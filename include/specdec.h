@@ -103,10 +103,12 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype (or, with the cluster kernel that
  * keeps each row slice on chip, a row wider than 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
  *
- * Kernels: by default one CTA verifies one request, streaming its rows through a ring of
- * 32 KB shared-memory stages filled by bulk async copies. Setting the environment variable
- * SPECDEC_KERNEL=cluster selects the alternative kernel (one thread-block cluster per request,
- * each CTA holding a slice of every row); both compute identical results.
+ * Kernels: by default each request is verified by a cluster of G CTAs (G = 1 for large
+ * batches, up to 8 for small ones), each streaming its slice of every row through a ring of
+ * 32 KB shared-memory stages filled by bulk async copies; requests whose bitmask allows few ids
+ * gather only the allowed 16-byte groups instead. Setting the environment variable
+ * SPECDEC_KERNEL=cluster selects the alternative kernel that keeps a slice of every row resident
+ * in shared memory; SPECDEC_CTAS_PER_REQUEST=G forces G. All shapes compute identical results.
  */
 specdec_status_t specdec_verify(
     const void* target_logits, specdec_dtype_t logits_dtype,
@@ -139,13 +141,14 @@ specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
 const char* specdec_status_string(specdec_status_t status);
 
 /*
- * specdec_launch_config -- the launch shape specdec_verify uses for a vocabulary size and
- * dtype (host arithmetic only; no GPU needed): CTAs per request (a thread-block cluster that
- * splits each vocabulary row into contiguous slices), threads per CTA, dynamic shared memory
- * per CTA in bytes, and vocabulary ids per slice. Any output pointer may be NULL.
- * Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED like specdec_verify.
+ * specdec_launch_config -- the launch shape specdec_verify uses for a batch of B requests of
+ * vocabulary size V (host arithmetic; the SM count comes from the current device, 152 when none
+ * is visible): CTAs per request (a thread-block cluster that splits every vocabulary row into
+ * contiguous slices), threads per CTA, dynamic shared memory per CTA in bytes, and vocabulary ids
+ * per slice. Any output pointer may be NULL. Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED
+ * like specdec_verify.
  */
-specdec_status_t specdec_launch_config(int32_t V, specdec_dtype_t logits_dtype,
+specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                        int32_t* ctas_per_request, int32_t* threads_per_cta,
                                        int32_t* smem_bytes, int32_t* slice_ids);
 

@@ -55,7 +55,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specdec_status_string.restype = ctypes.c_char_p
     lib.specdec_status_string.argtypes = [ctypes.c_int]
     lib.specdec_launch_config.restype = ctypes.c_int
-    lib.specdec_launch_config.argtypes = [i32, ctypes.c_int, vp, vp, vp, vp]
+    lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -64,9 +64,9 @@ def status_string(status: int) -> str:
     return load().specdec_status_string(int(status)).decode()
 
 
-def launch_config(V: int, dtype: int) -> dict:
+def launch_config(V: int, dtype: int, B: int = 1024) -> dict:
     c, t, s, w = (ctypes.c_int32() for _ in range(4))
-    rc = load().specdec_launch_config(int(V), int(dtype), ctypes.byref(c), ctypes.byref(t),
+    rc = load().specdec_launch_config(int(B), int(V), int(dtype), ctypes.byref(c), ctypes.byref(t),
                                       ctypes.byref(s), ctypes.byref(w))
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_launch_config")

@@ -41,6 +41,35 @@
 
 #include "specdec.h"
 
+// Phase tracing (diagnostic builds only: compile with -DSPECDEC_TRACE). The first consumer
+// thread of each request writes (%globaltimer << 4 | tag) into trace[request * 64 + i] and the
+// number of stamps into slot 63. The default build compiles every stamp away.
+#ifdef SPECDEC_TRACE
+__device__ unsigned long long* g_specdec_trace = nullptr;
+extern "C" int specdec_trace_set(void* buffer)
+{
+    return (int)cudaMemcpyToSymbol(g_specdec_trace, &buffer, sizeof(buffer));
+}
+#define SPECDEC_TRACE_BEGIN(req, on)                                                               \
+    int trace_n_ = 0;                                                                              \
+    const bool trace_on_ = (on);                                                                   \
+    unsigned long long* trace_ = g_specdec_trace ? g_specdec_trace + (size_t)(req) * 64 : nullptr;
+#define SPECDEC_STAMP(tag)                                                                         \
+    do {                                                                                           \
+        if (trace_on_ && trace_ && trace_n_ < 62) {                                               \
+            unsigned long long t_;                                                                 \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                 \
+            trace_[trace_n_++] = (t_ << 4) | (unsigned long long)(tag);                            \
+        }                                                                                          \
+    } while (0)
+#define SPECDEC_TRACE_END()                                                                        \
+    do { if (trace_on_ && trace_) trace_[63] = (unsigned long long)trace_n_; } while (0)
+#else
+#define SPECDEC_TRACE_BEGIN(req, on)
+#define SPECDEC_STAMP(tag) do { } while (0)
+#define SPECDEC_TRACE_END() do { } while (0)
+#endif
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -712,7 +741,9 @@ struct StreamShared {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t dec;
+    uint64_t pbar[2];                      // cluster exchange: partials of the G CTAs landed
     Part wpart[2][kConsumerWarps];
+    Part parts[2][kMaxCluster];            // cluster exchange: one partial per CTA of the request
     int32_t scan[kConsumerWarps];
     int32_t xs[SPECDEC_KMAX];
     float us[SPECDEC_KMAX];
@@ -730,6 +761,36 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 __device__ __forceinline__ void consumer_sync()
 {
     asm volatile("bar.sync 1, %0;" :: "n"(kConsumers) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 __device__ __forceinline__ float fast_rcp(float x)
@@ -825,10 +886,10 @@ struct Producer {
     StreamShared& sh;
     unsigned char* ring;
     uint32_t it = 0;
-    int lane;
+    int lane, lo, hi;        // this CTA's slice [lo, hi) of every row
 
-    __device__ Producer(const Args& a_, StreamShared& s_, unsigned char* r_, int lane_)
-        : a(a_), sh(s_), ring(r_), lane(lane_) {}
+    __device__ Producer(const Args& a_, StreamShared& s_, unsigned char* r_, int lane_, int lo_, int hi_)
+        : a(a_), sh(s_), ring(r_), lane(lane_), lo(lo_), hi(hi_) {}
 
     __device__ __forceinline__ int acquire()
     {
@@ -838,14 +899,14 @@ struct Producer {
         return s;
     }
 
-    // chunk c of logits row t (+ its mask words)
+    // chunk c of the slice of logits row t (+ its mask words)
     __device__ __forceinline__ void row_chunk(int64_t t, int c)
     {
         using G = Geom<ET>;
         const int s = acquire();
         unsigned char* st = ring + (size_t)s * kStageBytes;
-        const int64_t i0 = (int64_t)c * G::kRowIds;
-        const int n = (int)min((int64_t)G::kRowIds, (int64_t)a.V - i0);
+        const int i0 = lo + c * G::kRowIds;
+        const int n = min(G::kRowIds, hi - i0);
         const ET* src = reinterpret_cast<const ET*>(a.logits) + t * (int64_t)a.V + i0;
         const int32_t* msrc = a.bitmask ? a.bitmask + t * (int64_t)a.W + (i0 >> 5) : nullptr;
         const int nw = (n + 31) / 32;
@@ -874,15 +935,15 @@ struct Producer {
         ++it;
     }
 
-    // chunk c of the draw row t (draft slot d): logits, noise, q (with_q), mask words
+    // chunk c of the slice of draw row t (draft slot d): logits, noise, q (with_q), mask words
     __device__ __forceinline__ void draw_chunk(int64_t t, int64_t d, int c, bool with_q)
     {
         using G = Geom<ET>;
         const int s = acquire();
         unsigned char* st = ring + (size_t)s * kStageBytes;
         const int ids = G::draw_ids(with_q);
-        const int64_t i0 = (int64_t)c * ids;
-        const int n = (int)min((int64_t)ids, (int64_t)a.V - i0);
+        const int i0 = lo + c * ids;
+        const int n = min(ids, hi - i0);
         const ET* src = reinterpret_cast<const ET*>(a.logits) + t * (int64_t)a.V + i0;
         const float* esrc = a.noise + t * (int64_t)a.V + i0;
         const float* qsrc = with_q ? a.q + d * (int64_t)a.V + i0 : nullptr;
@@ -924,30 +985,23 @@ struct Producer {
     }
 };
 
-// Load the 16-byte group g (VE ids) of row `row` of a [*, V] array whose rows are 16-byte aligned.
+// Load the 16-byte group g (VE ids) of row `row` of the logits (rows 16-byte aligned).
 template <typename ET>
-__device__ __forceinline__ void gather_logits(const Args& a, int64_t row, int g, float z[Elem<ET>::VE])
+__device__ __forceinline__ uint4 gather_group(const Args& a, int64_t row, int g)
 {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const ET*>(a.logits) + row * (int64_t)a.V) + g);
+    return __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const ET*>(a.logits) + row * (int64_t)a.V) + g);
+}
+
+template <typename ET>
+__device__ __forceinline__ void unpack_group(const uint4 u, float z[Elem<ET>::VE])
+{
     if constexpr (sizeof(ET) == 4) {
         z[0] = __uint_as_float(u.x); z[1] = __uint_as_float(u.y); z[2] = __uint_as_float(u.z); z[3] = __uint_as_float(u.w);
     } else {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            z[2 * i] = __uint_as_float(w[i] << 16);
-            z[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-}
-
-template <int VE>
-__device__ __forceinline__ void gather_f32(const float* rowp, int g, float v[VE])
-{
-#pragma unroll
-    for (int h = 0; h < VE / 4; ++h) {
-        const float4 f = __ldcs(reinterpret_cast<const float4*>(rowp + (int64_t)g * VE) + h);
-        v[4 * h] = f.x; v[4 * h + 1] = f.y; v[4 * h + 2] = f.z; v[4 * h + 3] = f.w;
+        z[0] = __uint_as_float(u.x << 16); z[1] = __uint_as_float(u.x & 0xffff0000u);
+        z[2] = __uint_as_float(u.y << 16); z[3] = __uint_as_float(u.y & 0xffff0000u);
+        z[4] = __uint_as_float(u.z << 16); z[5] = __uint_as_float(u.z & 0xffff0000u);
+        z[6] = __uint_as_float(u.w << 16); z[7] = __uint_as_float(u.w & 0xffff0000u);
     }
 }
 
@@ -961,8 +1015,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
     __shared__ StreamShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = blockIdx.x;
-    const int nrow_chunks = (a.V + G::kRowIds - 1) / G::kRowIds;
+    const int NC = a.G;                                           // CTAs per request (cluster)
+    const int rank = (int)cluster_ctarank();
+    const int b = (int)cluster_id_x();
+    const int lo = rank * a.slice_units * kUnit;
+    const int hi = min(a.V, lo + a.slice_units * kUnit);
+    const int nrow_chunks = (hi - lo + G::kRowIds - 1) / G::kRowIds;
     // at least one chunk of the next row is issued only after the pending decision was read,
     // so consumers can never post two decisions ahead of the producer
     const int spec = min(kSpec, nrow_chunks - 1);
@@ -974,17 +1032,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             mbar_init(smem_addr(&sh.empty[s]), kConsumerWarps);
         }
         mbar_init(smem_addr(&sh.dec), 1);
+        mbar_init(smem_addr(&sh.pbar[0]), (uint32_t)NC);
+        mbar_init(smem_addr(&sh.pbar[1]), (uint32_t)NC);
         fence_mbar_init();
         sh.timed_out = 0;
     }
-    __syncthreads();
+    // every CTA of the request has initialised its barriers before any partial is sent
+    if (NC > 1) cluster_sync_all(); else __syncthreads();
 
     const ReqShape rs = request_shape(a, b);
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
         if (rs.skip == 0 && !request_is_sparse(a, rs.row0, lane)) {
-            Producer<ET> pr(a, sh, ring, lane);
+            Producer<ET> pr(a, sh, ring, lane, lo, hi);
             uint32_t dec_round = 0;
             int issued_next = 0;
             for (int j = 0; j <= rs.k; ++j) {
@@ -1001,7 +1062,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (code == kDecNextRow) continue;
                 while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
                     const bool wq = (code == kDecDrawQ);
-                    const int nd = (a.V + G::draw_ids(wq) - 1) / G::draw_ids(wq);
+                    const int nd = (hi - lo + G::draw_ids(wq) - 1) / G::draw_ids(wq);
                     for (int c = 0; c < nd; ++c) pr.draw_chunk(t, (int64_t)rs.d0 + j, c, wq);
                     if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
                     ++dec_round;
@@ -1014,6 +1075,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // ------------------------------------------------------------------ consumers
         const int ct = tid - 32, cw = warp - 1;
         const bool leader = (ct == 0);
+        const bool writer = leader && rank == 0;
+        SPECDEC_TRACE_BEGIN(b, writer);
+        SPECDEC_STAMP(0);
         if (cw == 0) {
             // a1 ragged decode + a4 grammar-valid prefix (one consumer warp)
             const float T = a.temperature[b];
@@ -1048,6 +1112,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             }
         }
         consumer_sync();
+        SPECDEC_STAMP(1);
         const int k = rs.k, g = sh.g;
         const bool greedy = sh.greedy != 0, qmode = sh.qmode != 0, sparse = sh.sparse != 0;
         const float c = sh.c;
@@ -1055,14 +1120,15 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         uint32_t st = sh.st;
         const bool has_mask = a.bitmask != nullptr;
         uint32_t* list = reinterpret_cast<uint32_t*>(ring);
+        const int wlo = lo >> 5, whi = (hi + 31) >> 5;             // this slice's mask words
 
-        if (leader && rs.skip != 1) {
+        if (writer && rs.skip != 1) {
             if (a.diag_alpha) for (int j = 0; j < k; ++j) a.diag_alpha[rs.d0 + j] = NAN;
             if (a.diag_row)
                 for (int j = 0; j <= k; ++j) { a.diag_row[2 * (rs.row0 + j)] = NAN; a.diag_row[2 * (rs.row0 + j) + 1] = NAN; }
         }
 
-        uint32_t it = 0;
+        uint32_t it = 0, xround = 0;
         int par = 0;
         auto wait_full = [&]() -> int {
             const int s = (int)(it % kStages);
@@ -1074,6 +1140,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             if (lane == 0) mbar_arrive(smem_addr(&sh.empty[s]));
             ++it;
         };
+        // CTA-wide reduction of the consumers' partials, then (NC > 1) a point-to-point exchange
+        // with the other CTAs of the request: consumer thread i stores this CTA's partial into
+        // CTA i's slot and arrives on CTA i's barrier; every CTA folds the NC partials in rank
+        // order, so all of them hold bit-identical results.
         auto reduce = [&](Part p) -> Part {
             p = warp_reduce(p, c);
             if (lane == 0) sh.wpart[par][cw] = p;
@@ -1082,7 +1152,23 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], c);
             par ^= 1;
-            return r;
+            if (NC == 1) return r;
+            const int slot = (int)(xround & 1u);
+            if (ct < NC) {
+                const uint32_t base = map_to_rank(smem_addr(&sh.parts[slot][rank]), (uint32_t)ct);
+                st_cluster_u32(base + 0, __float_as_uint(r.m));
+                st_cluster_u32(base + 4, __float_as_uint(r.S));
+                st_cluster_u32(base + 8, __float_as_uint(r.zx));
+                st_cluster_u32(base + 12, __float_as_uint(r.best));
+                st_cluster_u32(base + 16, (uint32_t)r.idx);
+                st_cluster_u32(base + 20, (uint32_t)r.flag);
+                mbar_arrive_remote(map_to_rank(smem_addr(&sh.pbar[slot]), (uint32_t)ct));
+            }
+            if (!mbar_wait_cluster_bounded(smem_addr(&sh.pbar[slot]), (xround >> 1) & 1u)) sh.timed_out = 1;
+            ++xround;
+            Part q = part_identity();
+            for (int i = 0; i < NC; ++i) combine(q, sh.parts[slot][i], c);
+            return q;
         };
         auto post = [&](int code) {
             if (leader && !sparse) {
@@ -1101,7 +1187,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             uint32_t words[kPer];
 #pragma unroll
             for (int q4 = 0; q4 < kPer / 4; ++q4) {
-                const int w = my0 + 4 * q4;               // W is a multiple of 4 here
+                const int w = my0 + 4 * q4;               // W and the slice bounds are multiples of 4 words
                 const uint4 u = (w < w1) ? __ldg(mrow + (w >> 2)) : make_uint4(0u, 0u, 0u, 0u);
                 words[4 * q4] = u.x; words[4 * q4 + 1] = u.y; words[4 * q4 + 2] = u.z; words[4 * q4 + 3] = u.w;
             }
@@ -1151,7 +1237,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         int acc_len = 0, emitted = -1;
         if (rs.skip == 0) {
             acc_len = k;
-            int listed_row = -1, listed_n = 0;            // row whose whole list is in `list`
+            int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
             for (int j = 0; j <= k; ++j) {
                 const int64_t t = rs.row0 + j;
                 const int64_t d = (int64_t)rs.d0 + j;
@@ -1161,13 +1247,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 float mc = 0.f;                            // running round(m * c)
 
                 if (!sparse) {
-                    // ---- a2/a3/a5/a6 dense: stream the row chunk by chunk
+                    // ---- a2/a3/a5/a6 dense: stream the slice chunk by chunk
                     for (int ch = 0; ch < nrow_chunks; ++ch) {
                         const int s = wait_full();
+                        if (ch == 0) SPECDEC_STAMP(2);
                         const unsigned char* stg = ring + (size_t)s * kStageBytes;
                         const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::kRowMaskOff);
-                        const int i0 = ch * G::kRowIds;
-                        const int n = min(G::kRowIds, a.V - i0);
+                        const int i0 = lo + ch * G::kRowIds;
+                        const int n = min(G::kRowIds, hi - i0);
                         const int nvec = (n + VE - 1) / VE;
                         const int vx = (!greedy && x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
                         for (int v = ct; v < nvec; v += kConsumers) {
@@ -1193,33 +1280,49 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         release(s);
                     }
                 } else {
-                    // ---- sparse: gather only the allowed 16-byte groups
-                    for (int w0 = 0; w0 < a.W; w0 += kSegWords) {
-                        const int n = build_list(t, w0, min(a.W, w0 + kSegWords));
-                        listed_row = (w0 == 0 && a.W <= kSegWords) ? j : -1;
+                    // ---- sparse: gather only the allowed 16-byte groups of the slice
+                    constexpr int U = 4;
+                    for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
+                        const int n = build_list(t, w0, min(whi, w0 + kSegWords));
+                        if (w0 == wlo) SPECDEC_STAMP(2);
+                        listed_row = (whi - wlo <= kSegWords) ? j : -1;
                         listed_n = n;
                         const int gx = (!greedy && x >= 0) ? x / VE : -1;
-                        for (int e = ct; e < n; e += kConsumers) {
-                            const uint32_t ent = list[e];
-                            const int grp = (int)(ent >> 8);
-                            const uint32_t bits = ent & 0xffu;
-                            float z[VE];
-                            gather_logits<ET>(a, t, grp, z);
+                        for (int e0 = ct; e0 < n; e0 += kConsumers * U) {
+                            uint32_t ent[U];
+                            uint4 raw[U];
 #pragma unroll
-                            for (int q = 0; q < VE; ++q) z[q] = ((bits >> q) & 1u) ? z[q] : -INFINITY;
-                            if (greedy) {
-                                argmax_fold<VE>(p, z, grp * VE);
-                            } else {
-                                if (grp == gx) {
+                            for (int u = 0; u < U; ++u) {
+                                const int e = e0 + u * kConsumers;
+                                ent[u] = e < n ? list[e] : 0u;
+                            }
 #pragma unroll
-                                    for (int q = 0; q < VE; ++q)
-                                        if (q == x - grp * VE) p.zx = z[q];
+                            for (int u = 0; u < U; ++u)
+                                raw[u] = (ent[u] & 0xffu) ? gather_group<ET>(a, t, (int)(ent[u] >> 8)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                            for (int u = 0; u < U; ++u) {
+                                const uint32_t bits = ent[u] & 0xffu;
+                                if (!bits) continue;
+                                const int grp = (int)(ent[u] >> 8);
+                                float z[VE];
+                                unpack_group<ET>(raw[u], z);
+#pragma unroll
+                                for (int q = 0; q < VE; ++q) z[q] = ((bits >> q) & 1u) ? z[q] : -INFINITY;
+                                if (greedy) {
+                                    argmax_fold<VE>(p, z, grp * VE);
+                                } else {
+                                    if (grp == gx) {
+#pragma unroll
+                                        for (int q = 0; q < VE; ++q)
+                                            if (q == x - grp * VE) p.zx = z[q];
+                                    }
+                                    softmax_fold<VE>(p, mc, z, c);
                                 }
-                                softmax_fold<VE>(p, mc, z, c);
                             }
                         }
                     }
                 }
+                SPECDEC_STAMP(3);
                 // each thread's terms were taken against mc = round(m*c); rebase its sum on the
                 // exact m*c (combine() rescales partials by exp2((m_a - m_b) * c))
                 if (!greedy && p.m > -INFINITY) {
@@ -1227,36 +1330,37 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     p.S = fmaf(p.S, -dlt * 0.69314718f, p.S);     // * 2^-dlt, |dlt| tiny
                 }
                 const Part r = reduce(p);
+                SPECDEC_STAMP(4);
 
-                // ---- decision (identical in every consumer thread)
+                // ---- decision (identical in every consumer thread of every CTA of the request)
                 int code = kDecDone;
                 bool stop = true;
                 float MC = 0.f, S_mc = 1.f;
                 if (greedy) {
                     if (r.idx == INT_MAX) {
                         st |= SPECDEC_ST_EMPTY_MASK_ROW;
-                        if (leader && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
+                        if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
                         acc_len = j; emitted = -1;
                     } else {
-                        if (leader && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
+                        if (writer && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
                         if (bonus) {
                             emitted = r.idx;
                         } else {
                             const bool accept = (j < g) && (x == r.idx);
-                            if (leader && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
-                            if (accept) { if (leader) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                            if (writer && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
+                            if (accept) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
                             else { acc_len = j; emitted = r.idx; }
                         }
                     }
                 } else if (r.m == -INFINITY) {
                     st |= SPECDEC_ST_EMPTY_MASK_ROW;
-                    if (leader && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
                     acc_len = j; emitted = -1;
                 } else {
                     MC = r.m * c;
                     // S against MC = round(M*c), the reference the draw terms use
                     S_mc = fmaf(r.S, fmaf(r.m, c, -MC) * 0.69314718f, r.S);
-                    if (leader && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
                     code = kDecDrawP;
                     if (!bonus) {
                         float alpha = 0.f;
@@ -1269,8 +1373,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                                 alpha = px;
                             }
                         }
-                        if (leader && a.diag_alpha) a.diag_alpha[d] = alpha;
-                        if (sh.us[j] < alpha) { if (leader) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                        if (writer && a.diag_alpha) a.diag_alpha[d] = alpha;
+                        if (sh.us[j] < alpha) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
                         else code = qmode ? kDecDrawQ : kDecDrawOneHot;
                     }
                 }
@@ -1283,20 +1387,21 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 
                 // ---- a9/a10: draw pass(es) over the stop / bonus row
                 while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
+                    SPECDEC_STAMP(5);
                     const float invS = 1.f / S_mc;
                     Part dp = part_identity();
                     if (!sparse) {
                         const bool wq = (code == kDecDrawQ);
                         const int ids = G::draw_ids(wq);
-                        const int nd = (a.V + ids - 1) / ids;
+                        const int nd = (hi - lo + ids - 1) / ids;
                         for (int ch = 0; ch < nd; ++ch) {
                             const int s = wait_full();
                             const unsigned char* stg = ring + (size_t)s * kStageBytes;
                             const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::dmask_off(wq));
                             const float* se = reinterpret_cast<const float*>(stg + G::noise_off(wq));
                             const float* sq = reinterpret_cast<const float*>(stg + G::q_off(wq));
-                            const int i0 = ch * ids;
-                            const int n = min(ids, a.V - i0);
+                            const int i0 = lo + ch * ids;
+                            const int n = min(ids, hi - i0);
                             const int nvec = (n + VE - 1) / VE;
                             for (int v = ct; v < nvec; v += kConsumers) {
                                 const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
@@ -1312,25 +1417,51 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             release(s);
                         }
                     } else {
+                        constexpr int U = 2;
                         const float* Erow = a.noise + t * (int64_t)a.V;
                         const float* Qrow = (code == kDecDrawQ) ? a.q + d * (int64_t)a.V : nullptr;
-                        for (int w0 = 0; w0 < a.W; w0 += kSegWords) {
-                            const int n = (listed_row == j) ? listed_n : build_list(t, w0, min(a.W, w0 + kSegWords));
-                            for (int e = ct; e < n; e += kConsumers) {
-                                const uint32_t ent = list[e];
-                                const int grp = (int)(ent >> 8);
-                                const uint32_t bits = ent & 0xffu;
-                                float z[VE], ev[VE], qv[VE];
-                                gather_logits<ET>(a, t, grp, z);
-                                gather_f32<VE>(Erow, grp, ev);
-                                if (Qrow) gather_f32<VE>(Qrow, grp, qv);
+                        for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
+                            const int n = (listed_row == j) ? listed_n : build_list(t, w0, min(whi, w0 + kSegWords));
+                            for (int e0 = ct; e0 < n; e0 += kConsumers * U) {
+                                uint32_t ent[U];
+                                uint4 raw[U];
+                                float4 ev[U][VE / 4], qv[U][VE / 4];
 #pragma unroll
-                                for (int q = 0; q < VE; ++q)
-                                    if ((bits >> q) & 1u)
-                                        draw_fold(dp, z[q], ev[q], Qrow ? qv[q] : 0.f, grp * VE + q, code, x, c, MC, invS);
+                                for (int u = 0; u < U; ++u) {
+                                    const int e = e0 + u * kConsumers;
+                                    ent[u] = e < n ? list[e] : 0u;
+                                }
+#pragma unroll
+                                for (int u = 0; u < U; ++u) {
+                                    const bool live = (ent[u] & 0xffu) != 0u;
+                                    const int grp = (int)(ent[u] >> 8);
+                                    raw[u] = live ? gather_group<ET>(a, t, grp) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                                    for (int h = 0; h < VE / 4; ++h) {
+                                        ev[u][h] = live ? __ldcs(reinterpret_cast<const float4*>(Erow + (int64_t)grp * VE) + h)
+                                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+                                        qv[u][h] = (live && Qrow) ? __ldcs(reinterpret_cast<const float4*>(Qrow + (int64_t)grp * VE) + h)
+                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                                    }
+                                }
+#pragma unroll
+                                for (int u = 0; u < U; ++u) {
+                                    const uint32_t bits = ent[u] & 0xffu;
+                                    if (!bits) continue;
+                                    const int grp = (int)(ent[u] >> 8);
+                                    float z[VE];
+                                    unpack_group<ET>(raw[u], z);
+                                    const float* evf = reinterpret_cast<const float*>(ev[u]);
+                                    const float* qvf = reinterpret_cast<const float*>(qv[u]);
+#pragma unroll
+                                    for (int q = 0; q < VE; ++q)
+                                        if ((bits >> q) & 1u)
+                                            draw_fold(dp, z[q], evf[q], qvf[q], grp * VE + q, code, x, c, MC, invS);
+                                }
                             }
                         }
                     }
+                    SPECDEC_STAMP(6);
                     const Part dr = reduce(dp);
                     if (code == kDecDrawQ && !dr.flag) { code = kDecDrawP; post(code); continue; }   // empty residual
                     emitted = dr.idx == INT_MAX ? -1 : dr.idx;
@@ -1342,8 +1473,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             }
         }
 
+        SPECDEC_STAMP(7);
+        SPECDEC_TRACE_END();
         // ---- a11: emit, count
-        if (leader) {
+        if (writer) {
             if (rs.skip == 0) {
                 a.out_tokens[rs.row0 + acc_len] = emitted;
                 for (int j = acc_len + 1; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
@@ -1359,6 +1492,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         }
     }
     __syncthreads();
+    // a copy that missed its deadline marks the request (any CTA of it) after rank 0 wrote status
+    if (NC > 1) cluster_sync_all();
     if (tid == 0 && sh.timed_out && a.status) atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
 }
 
@@ -1367,18 +1502,51 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 // ---------------------------------------------------------------------------------------------
 
 struct LaunchShape {
-    int stream;             // 1: one CTA per request (streaming ring); 0: one cluster per request
+    int stream;             // 1: streaming kernel (ring per CTA); 0: slice-resident cluster kernel
     int G, slice_units, smem, threads;
 };
 
-specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, LaunchShape* out)
+int device_sms()
 {
-    if (V <= 0) return SPECDEC_ERR_INVALID_ARG;
+    static int sms = -1;
+    if (sms < 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            sms = n;
+        else {
+            (void)cudaGetLastError();
+            sms = 152;      // no device visible: assume a GB300
+        }
+    }
+    return sms;
+}
+
+// CTAs per request for the streaming kernel: enough requests-in-flight for every SM to hold two
+// CTAs, and no more CTAs per request than that (a request is a serial chain of row passes; more
+// CTAs per request shorten the chain, fewer keep the per-row exchange cheap).
+int stream_ctas_per_request(int32_t B, int sms)
+{
+    long long G = (2LL * sms + (B > 0 ? B : 1) - 1) / (B > 0 ? B : 1);
+    if (G < 1) G = 1;
+    if (G > 8) G = 8;
+    return (int)G;
+}
+
+specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, int32_t B, LaunchShape* out)
+{
+    if (V <= 0 || B < 0) return SPECDEC_ERR_INVALID_ARG;
     if (dt != SPECDEC_F32 && dt != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     const int es = dt == SPECDEC_F32 ? 4 : 2;
     const long long units = ((long long)V + kUnit - 1) / kUnit;
-    const long long row_bytes = (long long)V * es;
-    long long G = (row_bytes + kTargetSliceBytes - 1) / kTargetSliceBytes;
+    const char* kind = std::getenv("SPECDEC_KERNEL");                // comparison runs
+    const bool cluster = kind && std::strcmp(kind, "cluster") == 0;
+    long long G;
+    if (cluster) {
+        const long long row_bytes = (long long)V * es;
+        G = (row_bytes + kTargetSliceBytes - 1) / kTargetSliceBytes;
+    } else {
+        G = stream_ctas_per_request(B, device_sms());
+    }
     if (const char* env = std::getenv("SPECDEC_CTAS_PER_REQUEST")) {     // tuning sweeps
         const long long forced = std::atoll(env);
         if (forced >= 1) G = forced;
@@ -1388,21 +1556,17 @@ specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, LaunchShape* out)
     if (G > units) G = units;
     const long long su = (units + G - 1) / G;
     G = (units + su - 1) / su;                      // no CTA with an empty slice
-    const long long slice_bytes = su * kUnit * es;
-    const char* kind = std::getenv("SPECDEC_KERNEL");                // comparison runs
-    const bool cluster = kind && std::strcmp(kind, "cluster") == 0;
+    out->G = (int)G;
+    out->slice_units = (int)su;
     if (!cluster) {
         out->stream = 1;
-        out->G = 1;
-        out->slice_units = (int)units;
-        out->smem = kStages * kStageBytes;
+        out->smem = kRingBytes;
         out->threads = kStreamThreads;
         return SPECDEC_OK;
     }
+    const long long slice_bytes = su * kUnit * es;
     if (slice_bytes > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
     out->stream = 0;
-    out->G = (int)G;
-    out->slice_units = (int)su;
     out->smem = (int)(slice_bytes + su * (kUnit / 32) * 4);
     out->threads = kThreads;
     return SPECDEC_OK;
@@ -1420,19 +1584,20 @@ cudaError_t configure_kernel_once()
             err = cudaFuncSetAttribute(specdec_verify_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStages * kStageBytes);
+                                       kRingBytes);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     return err;
 }
 
-// Largest cluster size <= G that the device can co-schedule with this shared memory.
-template <typename ET>
-int schedulable_cluster(int G, int smem, cudaStream_t stream)
+// Largest cluster size <= G that the device can co-schedule for this kernel and shared memory.
+int schedulable_cluster(void (*kernel)(Args), int G, int smem, int threads, cudaStream_t stream)
 {
     for (; G > 1; --G) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)G, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = (size_t)smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -1443,7 +1608,7 @@ int schedulable_cluster(int G, int smem, cudaStream_t stream)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, specdec_verify_kernel<ET>, &cfg) == cudaSuccess && n > 0) return G;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n > 0) return G;
         (void)cudaGetLastError();
     }
     return 1;
@@ -1453,37 +1618,35 @@ template <typename ET>
 specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream)
 {
     if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
-    if (sh.stream) {
-        specdec_verify_stream_kernel<ET><<<(unsigned)B, kStreamThreads, (size_t)sh.smem, stream>>>(args);
-        const cudaError_t err = cudaGetLastError();
-        return err == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
-    }
-    {
-        // the cluster size actually used, cached per (G, smem) request
+    void (*kernel)(Args) = sh.stream ? specdec_verify_stream_kernel<ET> : specdec_verify_kernel<ET>;
+    if (sh.G > 1) {
+        // the cluster size actually used, cached per (kernel, G, smem) request
         static std::mutex mu;
+        static void (*cached_kernel)(Args) = nullptr;
         static int cached_req = -1, cached_smem = -1, cached_G = -1;
         std::lock_guard<std::mutex> lock(mu);
-        if (cached_req != sh.G || cached_smem != sh.smem) {
-            cached_G = schedulable_cluster<ET>(sh.G, sh.smem, stream);
+        if (cached_kernel != kernel || cached_req != sh.G || cached_smem != sh.smem) {
+            cached_G = schedulable_cluster(kernel, sh.G, sh.smem, sh.threads, stream);
+            cached_kernel = kernel;
             cached_req = sh.G;
             cached_smem = sh.smem;
         }
         if (cached_G != sh.G) {
-            // re-slice the row over fewer CTAs; give up if a slice no longer fits on chip
+            // re-slice the row over fewer CTAs; the cluster kernel gives up if a slice no longer fits
             const int es = (int)sizeof(ET);
             const long long units = ((long long)args.V + kUnit - 1) / kUnit;
             const long long su = (units + cached_G - 1) / cached_G;
-            if (su * kUnit * es > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
+            if (!sh.stream && su * kUnit * es > kMaxSliceBytes) return SPECDEC_ERR_UNSUPPORTED;
             sh.G = (int)((units + su - 1) / su);
             sh.slice_units = (int)su;
-            sh.smem = (int)(su * kUnit * es + su * (kUnit / 32) * 4);
+            if (!sh.stream) sh.smem = (int)(su * kUnit * es + su * (kUnit / 32) * 4);
             args.G = sh.G;
             args.slice_units = sh.slice_units;
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)B * (unsigned)sh.G, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)sh.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1493,7 +1656,7 @@ specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t strea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, specdec_verify_kernel<ET>, args);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args);
     if (err != cudaSuccess) {
         (void)cudaGetLastError();
         return SPECDEC_ERR_CUDA;
@@ -1505,12 +1668,12 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 }  // namespace
 
-extern "C" specdec_status_t specdec_launch_config(int32_t V, specdec_dtype_t logits_dtype,
+extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                                   int32_t* ctas_per_request, int32_t* threads_per_cta,
                                                   int32_t* smem_bytes, int32_t* slice_ids)
 {
     LaunchShape s;
-    const specdec_status_t rc = shape_for(V, logits_dtype, &s);
+    const specdec_status_t rc = shape_for(V, logits_dtype, B, &s);
     if (rc != SPECDEC_OK) return rc;
     if (ctas_per_request) *ctas_per_request = s.G;
     if (threads_per_cta) *threads_per_cta = s.threads;
@@ -1539,7 +1702,7 @@ extern "C" specdec_status_t specdec_verify(
         (diag_accept_prob && !aligned(diag_accept_prob, 4)) || (diag_row_stats && !aligned(diag_row_stats, 4)))
         return SPECDEC_ERR_INVALID_ARG;
     LaunchShape shape;
-    const specdec_status_t rc = shape_for(V, logits_dtype, &shape);
+    const specdec_status_t rc = shape_for(V, logits_dtype, B, &shape);
     if (rc != SPECDEC_OK) return rc;
     if (B == 0) return SPECDEC_OK;
     if ((long long)B * shape.G > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;

@@ -43,9 +43,10 @@ def test_status_strings(lib):
 @pytest.mark.parametrize("V,dtype", [(1, 0), (8, 0), (37, 1), (1000, 0), (32000, 0), (128256, 0), (151936, 0),
                                      (151936, 1), (262144, 1), (786432, 0)])
 @pytest.mark.parametrize("kernel", ["stream", "cluster"])
-def test_launch_config_covers_the_row(lib, V, dtype, kernel, monkeypatch):
+@pytest.mark.parametrize("B", [1, 64, 128, 1024])
+def test_launch_config_covers_the_row(lib, V, dtype, kernel, B, monkeypatch):
     monkeypatch.setenv("SPECDEC_KERNEL", kernel)
-    c = _native.launch_config(V, dtype)
+    c = _native.launch_config(V, dtype, B=B)
     G, sl = c["ctas_per_request"], c["slice_ids"]
     assert 1 <= G <= 16 and sl % 128 == 0
     assert G * sl >= V and (G - 1) * sl < V          # every CTA owns a non-empty slice
@@ -54,7 +55,10 @@ def test_launch_config_covers_the_row(lib, V, dtype, kernel, monkeypatch):
         assert c["smem_bytes"] >= sl * es and c["smem_bytes"] <= 200 * 1024
         assert c["threads_per_cta"] == 256
     else:
-        assert G == 1 and c["smem_bytes"] == 3 * 32 * 1024 and c["threads_per_cta"] == 288
+        assert c["smem_bytes"] == 3 * 32 * 1024 and c["threads_per_cta"] == 288
+        assert G <= 8
+        if B >= 2 * 152:
+            assert G == 1                            # enough requests to fill the GPU
 
 
 def test_launch_config_rejects(lib, monkeypatch):
@@ -69,7 +73,7 @@ def test_launch_config_rejects(lib, monkeypatch):
         _native.launch_config(4 * 1024 * 1024, 0)     # a 16 MiB row cannot be staged on chip
     assert e.value.status == _native.SPECDEC_ERR_UNSUPPORTED
     monkeypatch.setenv("SPECDEC_KERNEL", "stream")   # the streaming kernel has no row-size limit
-    assert _native.launch_config(4 * 1024 * 1024, 0)["ctas_per_request"] == 1
+    assert _native.launch_config(4 * 1024 * 1024, 0, B=1024)["ctas_per_request"] == 1
 
 
 def _call(lib, **over):
