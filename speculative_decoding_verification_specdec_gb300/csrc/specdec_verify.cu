@@ -836,47 +836,92 @@ __device__ __forceinline__ float ex2_scaled(float z, float c, float mc)
     return ex2(fmaf(z, c, -mc));
 }
 
-// Fold one vector's masked logits into a running (m, S, mc) of the online softmax.
-template <int VE>
-__device__ __forceinline__ void softmax_fold(Part& p, float& mc, const float z[VE], float c)
+// ---- batched per-thread processing: NB 16-byte groups at once, so that loads, exponentials and
+// the max / sum trees of different groups are independent (ILP instead of one long chain)
+
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v)
 {
-    float vm = z[0];
+    float t[N];
 #pragma unroll
-    for (int e = 1; e < VE; ++e) vm = fmaxf(vm, z[e]);
-    if (vm == -INFINITY) return;
-    if (vm > p.m) {
-        const float nmc = vm * c;
+    for (int i = 0; i < N; ++i) t[i] = v[i];
+#pragma unroll
+    for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    return t[0];
+}
+
+template <int N>
+__device__ __forceinline__ float tree_sum(const float* v)
+{
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = v[i];
+#pragma unroll
+    for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] += t[i + w];
+    return t[0];
+}
+
+// Greedy fold of N values whose ids are ids[i] (increasing in i): max, lowest id on ties.
+template <int N>
+__device__ __forceinline__ void argmax_batch(Part& p, const float* z, const int* ids)
+{
+    const float bm = tree_max<N>(z);
+    if (bm > p.best) {                         // strict: an equal earlier best keeps its lower id
+        int id = INT_MAX;
+#pragma unroll
+        for (int i = N - 1; i >= 0; --i) id = (z[i] == bm) ? ids[i] : id;
+        p.best = bm;
+        p.idx = id;
+    }
+}
+
+// Online-softmax fold of N masked logits against the running reference mc = round(m * c).
+template <int N>
+__device__ __forceinline__ void softmax_batch(Part& p, float& mc, const float* z, float c)
+{
+    const float bm = tree_max<N>(z);
+    if (!(bm > -INFINITY)) return;
+    if (bm > p.m) {
+        const float nmc = bm * c;
         p.S = (p.m == -INFINITY) ? 0.f : p.S * ex2(mc - nmc);
-        p.m = vm;
+        p.m = bm;
         mc = nmc;
     }
-    float s = 0.f;
+    float e[N];
 #pragma unroll
-    for (int e = 0; e < VE; ++e) s += ex2_scaled(z[e], c, mc);
-    p.S += s;
+    for (int i = 0; i < N; ++i) e[i] = ex2_scaled(z[i], c, mc);
+    p.S += tree_sum<N>(e);
 }
 
-template <int VE>
-__device__ __forceinline__ void argmax_fold(Part& p, const float z[VE], int i0)
+// Draw fold of N candidates: w from p (and q), score w / E; -1 marks "no candidate".
+template <int N>
+__device__ __forceinline__ void draw_batch(Part& p, const float* z, const float* E, const float* qv, const int* ids,
+                                           int code, int x, float c, float MC, float invS)
 {
+    float sc[N];
+    int any = 0;
 #pragma unroll
-    for (int e = 0; e < VE; ++e)
-        if (z[e] > p.best) { p.best = z[e]; p.idx = i0 + e; }
-}
-
-// One draw candidate: w from p (and q), score w / E (rcp.approx; ties on exact equality).
-__device__ __forceinline__ void draw_fold(Part& p, float z, float E, float qv, int i, int code, int x,
-                                          float c, float MC, float invS)
-{
-    if (!(z > -INFINITY)) return;
-    const float pe = ex2_scaled(z, c, MC) * invS;
-    float w = pe;
-    if (code == kDecDrawQ) w = fmaxf(pe - qv, 0.f);
-    else if (code == kDecDrawOneHot && i == x) w = 0.f;
-    if (w > 0.f) {
-        p.flag = 1;
-        const float sc = w * fast_rcp(E);
-        if (sc > p.best) { p.best = sc; p.idx = i; }
+    for (int i = 0; i < N; ++i) {
+        const float pe = ex2_scaled(z[i], c, MC) * invS;        // z = -inf gives 0
+        float w = pe;
+        if (code == kDecDrawQ) w = fmaxf(pe - qv[i], 0.f);
+        else if (code == kDecDrawOneHot) w = (ids[i] == x) ? 0.f : pe;
+        const bool cand = w > 0.f;
+        any |= cand ? 1 : 0;
+        sc[i] = cand ? w * fast_rcp(E[i]) : -1.f;
+    }
+    p.flag |= any;
+    const float bm = tree_max<N>(sc);
+    if (bm > 0.f && bm > p.best) {
+        int id = INT_MAX;
+#pragma unroll
+        for (int i = N - 1; i >= 0; --i) id = (sc[i] == bm) ? ids[i] : id;
+        p.best = bm;
+        p.idx = id;
     }
 }
 
@@ -1251,32 +1296,45 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     for (int ch = 0; ch < nrow_chunks; ++ch) {
                         const int s = wait_full();
                         if (ch == 0) SPECDEC_STAMP(2);
+                        if (j == 0 && ch > 0) SPECDEC_STAMP(8);
                         const unsigned char* stg = ring + (size_t)s * kStageBytes;
                         const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::kRowMaskOff);
                         const int i0 = lo + ch * G::kRowIds;
                         const int n = min(G::kRowIds, hi - i0);
                         const int nvec = (n + VE - 1) / VE;
-                        const int vx = (!greedy && x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
-                        for (int v = ct; v < nvec; v += kConsumers) {
-                            const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
-                            if (bits == 0u) continue;
-                            float z[VE];
-                            Elem<ET>::load(stg, v, z);
-                            if (has_mask) {
+                        constexpr int NB = 4;
+                        for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
+                            float z[NB * VE];
+                            int ids[NB * VE];
 #pragma unroll
-                                for (int e = 0; e < VE; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
+                            for (int u = 0; u < NB; ++u) {
+                                const int v = vb + u * kConsumers;
+                                if (v < nvec) {
+                                    Elem<ET>::load(stg, v, z + u * VE);
+                                    if (has_mask) {
+                                        const uint32_t bits = vec_bits<VE>(sm, true, v);
+#pragma unroll
+                                        for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < VE; ++e) z[u * VE + e] = -INFINITY;
+                                }
+#pragma unroll
+                                for (int e = 0; e < VE; ++e) ids[u * VE + e] = i0 + v * VE + e;
                             }
                             if (greedy) {
-                                argmax_fold<VE>(p, z, i0 + v * VE);
+                                argmax_batch<NB * VE>(p, z, ids);
                             } else {
-                                if (v == vx) {
+                                if (x >= i0 && x < i0 + n) {
 #pragma unroll
-                                    for (int e = 0; e < VE; ++e)
-                                        if (e == (x - i0) % VE) p.zx = z[e];
+                                    for (int q = 0; q < NB * VE; ++q)
+                                        if (ids[q] == x) p.zx = z[q];
                                 }
-                                softmax_fold<VE>(p, mc, z, c);
+                                softmax_batch<NB * VE>(p, mc, z, c);
                             }
                         }
+                        if (j == 0) SPECDEC_STAMP(9);
                         release(s);
                     }
                 } else {
@@ -1299,25 +1357,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
                             for (int u = 0; u < U; ++u)
                                 raw[u] = (ent[u] & 0xffu) ? gather_group<ET>(a, t, (int)(ent[u] >> 8)) : make_uint4(0u, 0u, 0u, 0u);
+                            float z[U * VE];
+                            int ids[U * VE];
 #pragma unroll
                             for (int u = 0; u < U; ++u) {
                                 const uint32_t bits = ent[u] & 0xffu;
-                                if (!bits) continue;
                                 const int grp = (int)(ent[u] >> 8);
-                                float z[VE];
-                                unpack_group<ET>(raw[u], z);
+                                unpack_group<ET>(raw[u], z + u * VE);
 #pragma unroll
-                                for (int q = 0; q < VE; ++q) z[q] = ((bits >> q) & 1u) ? z[q] : -INFINITY;
-                                if (greedy) {
-                                    argmax_fold<VE>(p, z, grp * VE);
-                                } else {
-                                    if (grp == gx) {
-#pragma unroll
-                                        for (int q = 0; q < VE; ++q)
-                                            if (q == x - grp * VE) p.zx = z[q];
-                                    }
-                                    softmax_fold<VE>(p, mc, z, c);
+                                for (int q = 0; q < VE; ++q) {
+                                    z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                                    ids[u * VE + q] = grp * VE + q;
                                 }
+                            }
+                            if (greedy) {
+                                argmax_batch<U * VE>(p, z, ids);
+                            } else {
+                                if (gx >= 0) {
+#pragma unroll
+                                    for (int q = 0; q < U * VE; ++q)
+                                        if (ids[q] == x) p.zx = z[q];
+                                }
+                                softmax_batch<U * VE>(p, mc, z, c);
                             }
                         }
                     }
@@ -1403,16 +1464,31 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             const int i0 = lo + ch * ids;
                             const int n = min(ids, hi - i0);
                             const int nvec = (n + VE - 1) / VE;
-                            for (int v = ct; v < nvec; v += kConsumers) {
-                                const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
-                                if (bits == 0u) continue;
-                                float z[VE];
-                                Elem<ET>::load(stg, v, z);
-                                const int e0 = v * VE;
+                            constexpr int NB = (VE == 4) ? 2 : 1;
+                            for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
+                                float z[NB * VE], ev[NB * VE], qv[NB * VE];
+                                int ids[NB * VE];
 #pragma unroll
-                                for (int e = 0; e < VE; ++e)
-                                    if ((bits >> e) & 1u)
-                                        draw_fold(dp, z[e], se[e0 + e], wq ? sq[e0 + e] : 0.f, i0 + e0 + e, code, x, c, MC, invS);
+                                for (int u = 0; u < NB; ++u) {
+                                    const int v = vb + u * kConsumers;
+                                    const int e0 = v * VE;
+                                    if (v < nvec) {
+                                        Elem<ET>::load(stg, v, z + u * VE);
+                                        const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
+#pragma unroll
+                                        for (int e = 0; e < VE; ++e) {
+                                            z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
+                                            ev[u * VE + e] = se[e0 + e];
+                                            qv[u * VE + e] = wq ? sq[e0 + e] : 0.f;
+                                        }
+                                    } else {
+#pragma unroll
+                                        for (int e = 0; e < VE; ++e) { z[u * VE + e] = -INFINITY; ev[u * VE + e] = 1.f; qv[u * VE + e] = 0.f; }
+                                    }
+#pragma unroll
+                                    for (int e = 0; e < VE; ++e) ids[u * VE + e] = i0 + e0 + e;
+                                }
+                                draw_batch<NB * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
                             }
                             release(s);
                         }
@@ -1444,20 +1520,24 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                                     }
                                 }
+                                float z[U * VE], evf[U * VE], qvf[U * VE];
+                                int ids[U * VE];
 #pragma unroll
                                 for (int u = 0; u < U; ++u) {
                                     const uint32_t bits = ent[u] & 0xffu;
-                                    if (!bits) continue;
                                     const int grp = (int)(ent[u] >> 8);
-                                    float z[VE];
-                                    unpack_group<ET>(raw[u], z);
-                                    const float* evf = reinterpret_cast<const float*>(ev[u]);
-                                    const float* qvf = reinterpret_cast<const float*>(qv[u]);
+                                    unpack_group<ET>(raw[u], z + u * VE);
+                                    const float* e4 = reinterpret_cast<const float*>(ev[u]);
+                                    const float* q4 = reinterpret_cast<const float*>(qv[u]);
 #pragma unroll
-                                    for (int q = 0; q < VE; ++q)
-                                        if ((bits >> q) & 1u)
-                                            draw_fold(dp, z[q], evf[q], qvf[q], grp * VE + q, code, x, c, MC, invS);
+                                    for (int q = 0; q < VE; ++q) {
+                                        z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                                        evf[u * VE + q] = e4[q];
+                                        qvf[u * VE + q] = q4[q];
+                                        ids[u * VE + q] = grp * VE + q;
+                                    }
                                 }
+                                draw_batch<U * VE>(dp, z, evf, qvf, ids, code, x, c, MC, invS);
                             }
                         }
                     }
