@@ -925,6 +925,118 @@ __device__ __forceinline__ void draw_batch(Part& p, const float* z, const float*
     }
 }
 
+
+// ---- raw 16-byte groups and their max
+
+template <typename ET> struct Raw;
+template <> struct Raw<float> {
+    static constexpr uint32_t kNegInf = 0xff800000u;                  // fp32 -inf
+};
+template <> struct Raw<uint16_t> {
+    static constexpr uint32_t kNegInf = 0xff80ff80u;                  // two bf16 -inf
+};
+
+template <typename ET>
+__device__ __forceinline__ void unpack_raw(const uint4 u, float* z)
+{
+    if constexpr (sizeof(ET) == 4) {
+        z[0] = __uint_as_float(u.x); z[1] = __uint_as_float(u.y); z[2] = __uint_as_float(u.z); z[3] = __uint_as_float(u.w);
+    } else {
+        z[0] = __uint_as_float(u.x << 16); z[1] = __uint_as_float(u.x & 0xffff0000u);
+        z[2] = __uint_as_float(u.y << 16); z[3] = __uint_as_float(u.y & 0xffff0000u);
+        z[4] = __uint_as_float(u.z << 16); z[5] = __uint_as_float(u.z & 0xffff0000u);
+        z[6] = __uint_as_float(u.w << 16); z[7] = __uint_as_float(u.w & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Max of NB raw groups: exact either way (bf16 values compare exactly in bf16x2).
+template <typename ET, int NB>
+__device__ __forceinline__ float raw_max(const uint4* raw, const float* z)
+{
+    if constexpr (sizeof(ET) == 2) {
+        uint32_t t[NB * 4];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) { t[4 * u] = raw[u].x; t[4 * u + 1] = raw[u].y; t[4 * u + 2] = raw[u].z; t[4 * u + 3] = raw[u].w; }
+#pragma unroll
+        for (int w = NB * 2; w >= 1; w /= 2)
+#pragma unroll
+            for (int i = 0; i < w; ++i) t[i] = bf16x2_max(t[i], t[i + w]);
+        return fmaxf(__uint_as_float(t[0] << 16), __uint_as_float(t[0] & 0xffff0000u));
+    } else {
+        return tree_max<NB * 4>(z);
+    }
+}
+
+// Greedy fold with ids base + u * stride + e (increasing): max, lowest id on ties.
+template <int NB, int VE>
+__device__ __forceinline__ void argmax_lazy(Part& p, const float* z, float bm, int base, int stride)
+{
+    if (bm > p.best) {                         // strict: an equal earlier best keeps its lower id
+        int id = INT_MAX;
+#pragma unroll
+        for (int u = NB - 1; u >= 0; --u)
+#pragma unroll
+            for (int e = VE - 1; e >= 0; --e) id = (z[u * VE + e] == bm) ? base + u * stride + e : id;
+        p.best = bm;
+        p.idx = id;
+    }
+}
+
+// Online-softmax fold of N masked logits whose max is bm.
+template <int N>
+__device__ __forceinline__ void softmax_fold_max(Part& p, float& mc, const float* z, float bm, float c)
+{
+    if (!(bm > -INFINITY)) return;
+    if (bm > p.m) {
+        const float nmc = bm * c;
+        p.S = (p.m == -INFINITY) ? 0.f : p.S * ex2(mc - nmc);
+        p.m = bm;
+        mc = nmc;
+    }
+    float e[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = ex2_scaled(z[i], c, mc);
+    p.S += tree_sum<N>(e);
+}
+
+// Draw fold of NB groups (ids base + u * stride + e); xslot = position of the one-hot draft or -1.
+template <int NB, int VE>
+__device__ __forceinline__ void draw_lazy(Part& p, const float* z, const float* E, const float* qv, int base, int stride,
+                                          int xslot, int code, float c, float MC, float invS)
+{
+    constexpr int N = NB * VE;
+    float sc[N];
+    int any = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float pe = ex2_scaled(z[i], c, MC) * invS;        // z = -inf gives 0
+        float w = pe;
+        if (code == kDecDrawQ) w = fmaxf(pe - qv[i], 0.f);
+        else if (code == kDecDrawOneHot && i == xslot) w = 0.f;
+        const bool cand = w > 0.f;
+        any |= cand ? 1 : 0;
+        sc[i] = cand ? w * fast_rcp(E[i]) : -1.f;
+    }
+    p.flag |= any;
+    const float bm = tree_max<N>(sc);
+    if (bm > 0.f && bm > p.best) {
+        int id = INT_MAX;
+#pragma unroll
+        for (int u = NB - 1; u >= 0; --u)
+#pragma unroll
+            for (int e = VE - 1; e >= 0; --e) id = (sc[u * VE + e] == bm) ? base + u * stride + e : id;
+        p.best = bm;
+        p.idx = id;
+    }
+}
+
 template <typename ET>
 struct Producer {
     const Args& a;
@@ -1303,36 +1415,44 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         const int n = min(G::kRowIds, hi - i0);
                         const int nvec = (n + VE - 1) / VE;
                         constexpr int NB = 4;
+                        constexpr uint32_t kFull = (1u << VE) - 1u;
                         for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
-                            float z[NB * VE];
-                            int ids[NB * VE];
+                            uint4 raw[NB];
+                            uint32_t bits[NB];
+                            bool full = true;
 #pragma unroll
                             for (int u = 0; u < NB; ++u) {
                                 const int v = vb + u * kConsumers;
-                                if (v < nvec) {
-                                    Elem<ET>::load(stg, v, z + u * VE);
-                                    if (has_mask) {
-                                        const uint32_t bits = vec_bits<VE>(sm, true, v);
-#pragma unroll
-                                        for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < VE; ++e) z[u * VE + e] = -INFINITY;
-                                }
-#pragma unroll
-                                for (int e = 0; e < VE; ++e) ids[u * VE + e] = i0 + v * VE + e;
+                                const bool in = v < nvec;
+                                const uint32_t ni = Raw<ET>::kNegInf;
+                                raw[u] = in ? reinterpret_cast<const uint4*>(stg)[v] : make_uint4(ni, ni, ni, ni);
+                                bits[u] = (in && has_mask) ? vec_bits<VE>(sm, true, v) : kFull;
+                                full = full && (bits[u] == kFull);
                             }
-                            if (greedy) {
-                                argmax_batch<NB * VE>(p, z, ids);
+                            float z[NB * VE];
+#pragma unroll
+                            for (int u = 0; u < NB; ++u) unpack_raw<ET>(raw[u], z + u * VE);
+                            float bm;
+                            if (full) {
+                                bm = raw_max<ET, NB>(raw, z);
                             } else {
-                                if (x >= i0 && x < i0 + n) {
 #pragma unroll
-                                    for (int q = 0; q < NB * VE; ++q)
-                                        if (ids[q] == x) p.zx = z[q];
-                                }
-                                softmax_batch<NB * VE>(p, mc, z, c);
+                                for (int u = 0; u < NB; ++u)
+#pragma unroll
+                                    for (int e = 0; e < VE; ++e)
+                                        z[u * VE + e] = ((bits[u] >> e) & 1u) ? z[u * VE + e] : -INFINITY;
+                                bm = tree_max<NB * VE>(z);
                             }
+                            if (greedy) argmax_lazy<NB, VE>(p, z, bm, i0 + vb * VE, kConsumers * VE);
+                            else softmax_fold_max<NB * VE>(p, mc, z, bm, c);
+                        }
+                        // the draft token's logit, read once by the thread that owns its group
+                        if (!greedy && x >= i0 && x < i0 + n && ct == ((x - i0) / VE) % kConsumers) {
+                            float zz[VE];
+                            Elem<ET>::load(stg, (x - i0) / VE, zz);
+#pragma unroll
+                            for (int e = 0; e < VE; ++e)
+                                if (e == (x - i0) % VE) p.zx = zz[e];
                         }
                         if (j == 0) SPECDEC_STAMP(9);
                         release(s);
@@ -1465,9 +1585,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             const int n = min(ids, hi - i0);
                             const int nvec = (n + VE - 1) / VE;
                             constexpr int NB = (VE == 4) ? 2 : 1;
+                            const int vxd = (code == kDecDrawOneHot && x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
                             for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
                                 float z[NB * VE], ev[NB * VE], qv[NB * VE];
-                                int ids[NB * VE];
+                                int xslot = -1;
 #pragma unroll
                                 for (int u = 0; u < NB; ++u) {
                                     const int v = vb + u * kConsumers;
@@ -1475,20 +1596,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                                     if (v < nvec) {
                                         Elem<ET>::load(stg, v, z + u * VE);
                                         const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
+                                        if (bits != (1u << VE) - 1u) {
 #pragma unroll
-                                        for (int e = 0; e < VE; ++e) {
-                                            z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
-                                            ev[u * VE + e] = se[e0 + e];
-                                            qv[u * VE + e] = wq ? sq[e0 + e] : 0.f;
+                                            for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
                                         }
+#pragma unroll
+                                        for (int h = 0; h < VE / 4; ++h) {
+                                            const float4 f = reinterpret_cast<const float4*>(se + e0)[h];
+                                            ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
+                                            if (wq) {
+                                                const float4 g4 = reinterpret_cast<const float4*>(sq + e0)[h];
+                                                qv[u * VE + 4 * h] = g4.x; qv[u * VE + 4 * h + 1] = g4.y; qv[u * VE + 4 * h + 2] = g4.z; qv[u * VE + 4 * h + 3] = g4.w;
+                                            } else {
+                                                qv[u * VE + 4 * h] = qv[u * VE + 4 * h + 1] = qv[u * VE + 4 * h + 2] = qv[u * VE + 4 * h + 3] = 0.f;
+                                            }
+                                        }
+                                        if (v == vxd) xslot = u * VE + (x - i0) % VE;
                                     } else {
 #pragma unroll
                                         for (int e = 0; e < VE; ++e) { z[u * VE + e] = -INFINITY; ev[u * VE + e] = 1.f; qv[u * VE + e] = 0.f; }
                                     }
-#pragma unroll
-                                    for (int e = 0; e < VE; ++e) ids[u * VE + e] = i0 + e0 + e;
                                 }
-                                draw_batch<NB * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
+                                draw_lazy<NB, VE>(dp, z, ev, qv, i0 + vb * VE, kConsumers * VE, xslot, code, c, MC, invS);
                             }
                             release(s);
                         }
