@@ -1730,15 +1730,18 @@ int device_sms()
     return sms;
 }
 
-// CTAs per request for the streaming kernel: enough requests-in-flight for every SM to hold two
-// CTAs, and no more CTAs per request than that (a request is a serial chain of row passes; more
-// CTAs per request shorten the chain, fewer keep the per-row exchange cheap).
+// CTAs per request for the streaming kernel. A request is a serial chain of row passes and
+// one CTA streams at about its fair share of HBM (~1/300 of it with two CTAs per SM), so small
+// batches split each row over a few CTAs to shorten the chains; large batches keep one CTA per
+// request and let the block scheduler balance them. (Measured on GB300: B=64 -> 4, B=128 -> 2,
+// B >= 256 -> 1 were the fastest of {1, 2, 4, 8}.)
 int stream_ctas_per_request(int32_t B, int sms)
 {
-    long long G = (2LL * sms + (B > 0 ? B : 1) - 1) / (B > 0 ? B : 1);
+    const int b = B > 0 ? B : 1;
+    int G = (256 * sms / 152) / b;
     if (G < 1) G = 1;
-    if (G > 8) G = 8;
-    return (int)G;
+    if (G > 4) G = 4;
+    return G;
 }
 
 specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, int32_t B, LaunchShape* out)
