@@ -91,19 +91,22 @@ def workload_for(cfg: int, rank: int) -> W.Workload:
 # algorithmic bytes: what the method must read / write given the accepted lengths
 # ------------------------------------------------------------------------------------------
 
-def _sector_bytes(allowed_row: np.ndarray) -> int:
-    """32-byte sectors of an fp32 row that hold at least one allowed id."""
+def _sector_bytes(allowed_row: np.ndarray, ids_per_sector: int) -> int:
+    """32-byte sectors of a row that hold at least one allowed id."""
     V = allowed_row.size
-    pad = (-V) % 8
-    a = np.concatenate([allowed_row, np.zeros(pad, dtype=bool)]).reshape(-1, 8)
+    pad = (-V) % ids_per_sector
+    a = np.concatenate([allowed_row, np.zeros(pad, dtype=bool)]).reshape(-1, ids_per_sector)
     return int(a.any(axis=1).sum()) * 32
 
 
 def algorithmic_bytes(w: W.Workload, acc: np.ndarray, status: np.ndarray) -> dict:
-    """Per-launch bytes the verify must move: logits and mask words of rows 0..a_b; for random
-    requests the exponential noise of the draw row, and on a rejected draft-model row its q row
-    plus q(x) of every tested draft; for masked rows the noise / q reads count only the 32-byte
-    sectors holding an allowed id; plus the small per-request arrays and the outputs."""
+    """Per-launch bytes the verify must move, given the accepted lengths a_b: for rows 0..a_b the
+    mask words and the logits, and for random requests the exponential noise of the draw row plus,
+    on a rejected draft-model row, its q row and q(x) of every tested draft; plus the small
+    per-request arrays and the outputs. On a row whose bitmask is not all ones only the 32-byte
+    sectors holding an allowed id are needed from the logits, noise and q (a forbidden token's
+    values cannot change any output). `row_total` counts whole rows instead (the plain
+    per-row figure, an upper bound)."""
     es = 2 if w.logits_dtype == W.BF16 else 4
     V, Wd = w.V, w.W
     cu = w.cu_num_draft
@@ -113,31 +116,47 @@ def algorithmic_bytes(w: W.Workload, acc: np.ndarray, status: np.ndarray) -> dic
     if w.draft_probs is not None:
         qmode[:] = True if w.has_q is None else (w.has_q != 0)
     logits = mask = noise = q = small = 0
+    row_total = 0
+
+    def sectors(t, ids_per_sector):
+        if w.bitmask is None or (w.bitmask[t] == -1).all():
+            return None
+        return _sector_bytes(W.unpack_mask_rows(w.bitmask[t], V)[0], ids_per_sector)
+
     for b in range(w.B):
         k = int(cu[b + 1] - cu[b])
         if status[b] & (8 | 16):
             continue
         a = int(acc[b])
         rows = a + 1
-        logits += rows * V * es
+        row0 = int(cu[b]) + b
+        for j in range(rows):
+            sl = sectors(row0 + j, 32 // es)
+            logits += V * es if sl is None else sl
+            row_total += V * es
         if w.bitmask is not None:
             mask += rows * 4 * Wd
-        small += 4 * 2 + 4 + 4 * k + 4 * (k + 1) + 4   # cu, temperature, ids, out_tokens, out_num_accepted
+            row_total += rows * 4 * Wd
+        sm_ = 4 * 2 + 4 + 4 * k + 4 * (k + 1) + 4      # cu, temperature, ids, out_tokens, out_num_accepted
+        small += sm_
+        row_total += sm_
         if greedy[b]:
             continue
         small += 4 * min(rows, k)                       # uniforms of the tested drafts
-        t = int(cu[b]) + b + a
-        if w.bitmask is not None and not (w.bitmask[t] == -1).all():
-            row_bytes = _sector_bytes(W.unpack_mask_rows(w.bitmask[t], V)[0])
-        else:
-            row_bytes = 4 * V
+        row_total += 4 * min(rows, k)
+        sl = sectors(row0 + a, 8)
+        row_bytes = 4 * V if sl is None else sl
         noise += row_bytes
+        row_total += 4 * V
         if qmode[b]:
             q += 4 * min(rows, k)
+            row_total += 4 * min(rows, k)
             if a < k:
                 q += row_bytes
+                row_total += 4 * V
     total = logits + mask + noise + q + small + 32
-    return {"total": total, "logits": logits, "mask": mask, "noise": noise, "q": q, "small": small}
+    return {"total": total, "logits": logits, "mask": mask, "noise": noise, "q": q, "small": small,
+            "row_total": row_total + 32}
 
 
 # ------------------------------------------------------------------------------------------
@@ -367,6 +386,7 @@ def main():
     mean_s = (tot_ms / args.steps) / 1e3
     peak, peak_kind = measured_peaks()
     achieved = ab["total"] / mean_s / 1e9
+    achieved_rows = ab["row_total"] / mean_s / 1e9
     traffic = traffic_from_profiles(w.name)
 
     # e2e through the public API with host buffers
@@ -426,7 +446,8 @@ def main():
                        "per_rank": "independent batch per rank (requests shard with no exchange)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "algorithmic_bytes_per_launch": ab},
+                         "algorithmic_bytes_per_launch": ab,
+                         "whole_row_gbs": achieved_rows, "whole_row_frac": achieved_rows / peak},
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": args.steps,
