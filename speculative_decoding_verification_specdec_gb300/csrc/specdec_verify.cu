@@ -707,8 +707,14 @@ constexpr int kStageBytes = 32 * 1024;
 constexpr int kStages = 3;
 constexpr int kSpec = 2;
 constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kListCap = kRingBytes / 4;       // sparse list entries (the ring's memory, reused)
-constexpr int kSegWords = 3072;                // mask words per sparse segment: <= kListCap groups
+// sparse requests reuse the ring's memory: a list of allowed 16-byte groups, then the data those
+// groups gather (cp.async), in batches
+constexpr int kListBytes = 32 * 1024;
+constexpr int kListCap = kListBytes / 4;       // list entries
+constexpr int kDataOff = kListBytes;
+constexpr int kDataBytes = kRingBytes - kListBytes;
+constexpr int kGatherCap = kDataBytes / 16;    // logits groups per gather batch
+constexpr int kSegWords = 5120;                // mask words scanned per pass (20 per consumer thread)
 
 enum : int { kDecNextRow = 1, kDecDrawP = 2, kDecDrawQ = 3, kDecDrawOneHot = 4, kDecDone = 5 };
 
@@ -734,7 +740,8 @@ template <typename ET> struct Geom {
     static_assert(kDrawIdsE * (ES + 4) + kDrawIdsE / 8 <= kStageBytes, "draw chunk overflows a stage");
     static_assert(kRowMaskOff % 16 == 0 && (kDrawIdsQ * ES) % 16 == 0 && (kDrawIdsE * ES) % 16 == 0,
                   "stage sections must be 16-byte aligned");
-    static_assert(kSegWords * (32 / Elem<ET>::VE) <= kListCap, "a sparse segment must fit the list");
+    static constexpr int kSafeWords = kListCap / (32 / Elem<ET>::VE);   // words whose groups always fit the list
+    static_assert(kSafeWords % 4 == 0 && kSafeWords <= kSegWords, "sparse segment sizes");
 };
 
 struct StreamShared {
@@ -791,6 +798,16 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
         if (mbar_try_wait_cluster(bar, parity)) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ float fast_rcp(float x)
@@ -1142,26 +1159,6 @@ struct Producer {
     }
 };
 
-// Load the 16-byte group g (VE ids) of row `row` of the logits (rows 16-byte aligned).
-template <typename ET>
-__device__ __forceinline__ uint4 gather_group(const Args& a, int64_t row, int g)
-{
-    return __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const ET*>(a.logits) + row * (int64_t)a.V) + g);
-}
-
-template <typename ET>
-__device__ __forceinline__ void unpack_group(const uint4 u, float z[Elem<ET>::VE])
-{
-    if constexpr (sizeof(ET) == 4) {
-        z[0] = __uint_as_float(u.x); z[1] = __uint_as_float(u.y); z[2] = __uint_as_float(u.z); z[3] = __uint_as_float(u.w);
-    } else {
-        z[0] = __uint_as_float(u.x << 16); z[1] = __uint_as_float(u.x & 0xffff0000u);
-        z[2] = __uint_as_float(u.y << 16); z[3] = __uint_as_float(u.y & 0xffff0000u);
-        z[4] = __uint_as_float(u.z << 16); z[5] = __uint_as_float(u.z & 0xffff0000u);
-        z[6] = __uint_as_float(u.w << 16); z[7] = __uint_as_float(u.w & 0xffff0000u);
-    }
-}
-
 template <typename ET>
 __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kernel(const Args a)
 {
@@ -1336,7 +1333,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // Sparse path: list the 16-byte groups of mask words [w0, w1) of row t that hold an
         // allowed id, in id order (block-wide exclusive scan). Returns the count.
         auto build_list = [&](int64_t t, int w0, int w1) -> int {
-            constexpr int kPer = kSegWords / kConsumers;                // 12 words per thread
+            constexpr int kPer = kSegWords / kConsumers;                // 20 words per thread
             static_assert(kPer % 4 == 0, "words are loaded 4 at a time");
             const uint4* mrow = reinterpret_cast<const uint4*>(a.bitmask + t * (int64_t)a.W);
             // each thread owns a contiguous run of words so that list order is id order
@@ -1378,6 +1375,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (w < cw) base += v;
                 total += v;
             }
+            if (total > kListCap) {                       // caller re-scans in smaller pieces
+                consumer_sync();
+                return -1;
+            }
 #pragma unroll
             for (int q = 0; q < kPer; ++q) {
                 uint32_t pres = presence(words[q], my0 + q);
@@ -1389,6 +1390,109 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             }
             consumer_sync();
             return total;
+        };
+
+        // Sparse statistics pass over list[0, n) of row t: the listed groups' logits are gathered
+        // with cp.async in batches of kGatherCap (all in flight at once), then folded from shared memory.
+        auto sparse_stats = [&](int64_t t, int x, int n, Part& p, float& mc) {
+            const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
+            const uint32_t dbase = smem_addr(ring + kDataOff);
+            const uint4* data = reinterpret_cast<const uint4*>(ring + kDataOff);
+            const uint32_t ni = Raw<ET>::kNegInf;
+            for (int b0 = 0; b0 < n; b0 += kGatherCap) {
+                const int nb = min(kGatherCap, n - b0);
+                for (int e = ct; e < nb; e += kConsumers)
+                    cp_async16(dbase + (uint32_t)e * 16u, lrow + (size_t)(list[b0 + e] >> 8) * 16u);
+                cp_async_wait_all();
+                consumer_sync();
+                constexpr int U = 4;
+                for (int e0 = ct; e0 < nb; e0 += kConsumers * U) {
+                    float z[U * VE];
+                    int ids[U * VE];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int e = e0 + u * kConsumers;
+                        const bool in = e < nb;
+                        const uint32_t ent = in ? list[b0 + e] : 0u;
+                        const uint4 raw = in ? data[e] : make_uint4(ni, ni, ni, ni);
+                        const uint32_t bits = ent & 0xffu;
+                        const int grp = (int)(ent >> 8);
+                        unpack_raw<ET>(raw, z + u * VE);
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) {
+                            z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                            ids[u * VE + q] = grp * VE + q;
+                        }
+                    }
+                    if (greedy) {
+                        argmax_batch<U * VE>(p, z, ids);
+                    } else {
+                        if (x >= 0) {
+#pragma unroll
+                            for (int q = 0; q < U * VE; ++q)
+                                if (ids[q] == x) p.zx = z[q];
+                        }
+                        softmax_batch<U * VE>(p, mc, z, c);
+                    }
+                }
+                consumer_sync();                          // the data region is free again
+            }
+        };
+        // Sparse draw pass over list[0, n) of row t: logits, noise and (q-mode) q of the listed
+        // groups, gathered with cp.async in batches sized to the data region.
+        auto sparse_draw = [&](int64_t t, int64_t d, int x, int n, int code, Part& dp, float MC, float invS) {
+            const bool wq = (code == kDecDrawQ);
+            const int per = 16 + 4 * VE + (wq ? 4 * VE : 0);
+            const int cap = kDataBytes / per;
+            unsigned char* dl = ring + kDataOff;
+            unsigned char* dn = dl + cap * 16;
+            unsigned char* dqp = dn + cap * 4 * VE;
+            const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
+            const unsigned char* erow = reinterpret_cast<const unsigned char*>(a.noise + t * (int64_t)a.V);
+            const unsigned char* qrow = wq ? reinterpret_cast<const unsigned char*>(a.q + d * (int64_t)a.V) : nullptr;
+            for (int b0 = 0; b0 < n; b0 += cap) {
+                const int nb = min(cap, n - b0);
+                for (int e = ct; e < nb; e += kConsumers) {
+                    const size_t grp = list[b0 + e] >> 8;
+                    cp_async16(smem_addr(dl + e * 16), lrow + grp * 16u);
+#pragma unroll
+                    for (int h = 0; h < VE / 4; ++h) {
+                        cp_async16(smem_addr(dn + e * 4 * VE + 16 * h), erow + grp * (4u * VE) + 16u * h);
+                        if (wq) cp_async16(smem_addr(dqp + e * 4 * VE + 16 * h), qrow + grp * (4u * VE) + 16u * h);
+                    }
+                }
+                cp_async_wait_all();
+                consumer_sync();
+                constexpr int U = (VE == 8) ? 1 : 2;
+                for (int e0 = ct; e0 < nb; e0 += kConsumers * U) {
+                    float z[U * VE], ev[U * VE], qv[U * VE];
+                    int ids[U * VE];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int e = e0 + u * kConsumers;
+                        const bool in = e < nb;
+                        const uint32_t ent = in ? list[b0 + e] : 0u;
+                        const uint32_t bits = ent & 0xffu;
+                        const int grp = (int)(ent >> 8);
+                        const uint32_t ni = Raw<ET>::kNegInf;
+                        unpack_raw<ET>(in ? reinterpret_cast<const uint4*>(dl)[e] : make_uint4(ni, ni, ni, ni), z + u * VE);
+#pragma unroll
+                        for (int h = 0; h < VE / 4; ++h) {
+                            const float4 f = in ? reinterpret_cast<const float4*>(dn + e * 4 * VE)[h] : make_float4(1.f, 1.f, 1.f, 1.f);
+                            const float4 g4 = (in && wq) ? reinterpret_cast<const float4*>(dqp + e * 4 * VE)[h] : make_float4(0.f, 0.f, 0.f, 0.f);
+                            ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
+                            qv[u * VE + 4 * h] = g4.x; qv[u * VE + 4 * h + 1] = g4.y; qv[u * VE + 4 * h + 2] = g4.z; qv[u * VE + 4 * h + 3] = g4.w;
+                        }
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) {
+                            z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                            ids[u * VE + q] = grp * VE + q;
+                        }
+                    }
+                    draw_batch<U * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
+                }
+                consumer_sync();
+            }
         };
 
         int acc_len = 0, emitted = -1;
@@ -1459,46 +1563,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     }
                 } else {
                     // ---- sparse: gather only the allowed 16-byte groups of the slice
-                    constexpr int U = 4;
+                    listed_row = -1;
                     for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
-                        const int n = build_list(t, w0, min(whi, w0 + kSegWords));
+                        const int w1 = min(whi, w0 + kSegWords);
+                        const int n = build_list(t, w0, w1);
                         if (w0 == wlo) SPECDEC_STAMP(2);
-                        listed_row = (whi - wlo <= kSegWords) ? j : -1;
-                        listed_n = n;
-                        const int gx = (!greedy && x >= 0) ? x / VE : -1;
-                        for (int e0 = ct; e0 < n; e0 += kConsumers * U) {
-                            uint32_t ent[U];
-                            uint4 raw[U];
-#pragma unroll
-                            for (int u = 0; u < U; ++u) {
-                                const int e = e0 + u * kConsumers;
-                                ent[u] = e < n ? list[e] : 0u;
-                            }
-#pragma unroll
-                            for (int u = 0; u < U; ++u)
-                                raw[u] = (ent[u] & 0xffu) ? gather_group<ET>(a, t, (int)(ent[u] >> 8)) : make_uint4(0u, 0u, 0u, 0u);
-                            float z[U * VE];
-                            int ids[U * VE];
-#pragma unroll
-                            for (int u = 0; u < U; ++u) {
-                                const uint32_t bits = ent[u] & 0xffu;
-                                const int grp = (int)(ent[u] >> 8);
-                                unpack_group<ET>(raw[u], z + u * VE);
-#pragma unroll
-                                for (int q = 0; q < VE; ++q) {
-                                    z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
-                                    ids[u * VE + q] = grp * VE + q;
-                                }
-                            }
-                            if (greedy) {
-                                argmax_batch<U * VE>(p, z, ids);
-                            } else {
-                                if (gx >= 0) {
-#pragma unroll
-                                    for (int q = 0; q < U * VE; ++q)
-                                        if (ids[q] == x) p.zx = z[q];
-                                }
-                                softmax_batch<U * VE>(p, mc, z, c);
+                        if (n >= 0) {
+                            sparse_stats(t, greedy ? -1 : x, n, p, mc);
+                            if (w1 - w0 == whi - wlo) { listed_row = j; listed_n = n; }   // the whole slice in one list
+                        } else {
+                            for (int s0 = w0; s0 < w1; s0 += G::kSafeWords) {
+                                const int n2 = build_list(t, s0, min(w1, s0 + G::kSafeWords));
+                                sparse_stats(t, greedy ? -1 : x, n2, p, mc);
                             }
                         }
                     }
@@ -1622,51 +1698,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             release(s);
                         }
                     } else {
-                        constexpr int U = 2;
-                        const float* Erow = a.noise + t * (int64_t)a.V;
-                        const float* Qrow = (code == kDecDrawQ) ? a.q + d * (int64_t)a.V : nullptr;
-                        for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
-                            const int n = (listed_row == j) ? listed_n : build_list(t, w0, min(whi, w0 + kSegWords));
-                            for (int e0 = ct; e0 < n; e0 += kConsumers * U) {
-                                uint32_t ent[U];
-                                uint4 raw[U];
-                                float4 ev[U][VE / 4], qv[U][VE / 4];
-#pragma unroll
-                                for (int u = 0; u < U; ++u) {
-                                    const int e = e0 + u * kConsumers;
-                                    ent[u] = e < n ? list[e] : 0u;
+                        if (listed_row == j) {
+                            sparse_draw(t, d, x, listed_n, code, dp, MC, invS);
+                        } else {
+                            for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
+                                const int w1 = min(whi, w0 + kSegWords);
+                                const int n = build_list(t, w0, w1);
+                                if (n >= 0) {
+                                    sparse_draw(t, d, x, n, code, dp, MC, invS);
+                                } else {
+                                    for (int s0 = w0; s0 < w1; s0 += G::kSafeWords)
+                                        sparse_draw(t, d, x, build_list(t, s0, min(w1, s0 + G::kSafeWords)), code, dp, MC, invS);
                                 }
-#pragma unroll
-                                for (int u = 0; u < U; ++u) {
-                                    const bool live = (ent[u] & 0xffu) != 0u;
-                                    const int grp = (int)(ent[u] >> 8);
-                                    raw[u] = live ? gather_group<ET>(a, t, grp) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                                    for (int h = 0; h < VE / 4; ++h) {
-                                        ev[u][h] = live ? __ldcs(reinterpret_cast<const float4*>(Erow + (int64_t)grp * VE) + h)
-                                                        : make_float4(1.f, 1.f, 1.f, 1.f);
-                                        qv[u][h] = (live && Qrow) ? __ldcs(reinterpret_cast<const float4*>(Qrow + (int64_t)grp * VE) + h)
-                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                                    }
-                                }
-                                float z[U * VE], evf[U * VE], qvf[U * VE];
-                                int ids[U * VE];
-#pragma unroll
-                                for (int u = 0; u < U; ++u) {
-                                    const uint32_t bits = ent[u] & 0xffu;
-                                    const int grp = (int)(ent[u] >> 8);
-                                    unpack_group<ET>(raw[u], z + u * VE);
-                                    const float* e4 = reinterpret_cast<const float*>(ev[u]);
-                                    const float* q4 = reinterpret_cast<const float*>(qv[u]);
-#pragma unroll
-                                    for (int q = 0; q < VE; ++q) {
-                                        z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
-                                        evf[u * VE + q] = e4[q];
-                                        qvf[u * VE + q] = q4[q];
-                                        ids[u * VE + q] = grp * VE + q;
-                                    }
-                                }
-                                draw_batch<U * VE>(dp, z, evf, qvf, ids, code, x, c, MC, invS);
                             }
                         }
                     }
