@@ -1339,6 +1339,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // each thread owns a contiguous run of words so that list order is id order
             const int my0 = w0 + ct * kPer;
             uint32_t words[kPer];
+            SPECDEC_STAMP(10);
 #pragma unroll
             for (int q4 = 0; q4 < kPer / 4; ++q4) {
                 const int w = my0 + 4 * q4;               // W and the slice bounds are multiples of 4 words
@@ -1358,6 +1359,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             int cnt = 0;
 #pragma unroll
             for (int q = 0; q < kPer; ++q) cnt += __popc(presence(words[q], my0 + q));
+            SPECDEC_STAMP(11);
             // exclusive scan of cnt over the consumers
             int incl = cnt;
 #pragma unroll
@@ -1375,19 +1377,23 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (w < cw) base += v;
                 total += v;
             }
+            SPECDEC_STAMP(12);
             if (total > kListCap) {                       // caller re-scans in smaller pieces
                 consumer_sync();
                 return -1;
             }
+            // fixed trip count (no loop over set bits): allowed ids come in runs, and a loop over
+            // set bits would serialise each warp on its densest word
 #pragma unroll
             for (int q = 0; q < kPer; ++q) {
-                uint32_t pres = presence(words[q], my0 + q);
-                while (pres) {
-                    const int pos = __ffs(pres) - 1;
-                    list[base++] = ((uint32_t)((my0 + q) * GPW + pos / VE) << 8) | ((words[q] >> pos) & ((1u << VE) - 1u));
-                    pres &= pres - 1u;
+                const uint32_t pres = presence(words[q], my0 + q);
+#pragma unroll
+                for (int h = 0; h < GPW; ++h) {
+                    if ((pres >> (h * VE)) & 1u)
+                        list[base++] = ((uint32_t)((my0 + q) * GPW + h) << 8) | ((words[q] >> (h * VE)) & ((1u << VE) - 1u));
                 }
             }
+            SPECDEC_STAMP(13);
             consumer_sync();
             return total;
         };
@@ -1405,6 +1411,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     cp_async16(dbase + (uint32_t)e * 16u, lrow + (size_t)(list[b0 + e] >> 8) * 16u);
                 cp_async_wait_all();
                 consumer_sync();
+                SPECDEC_STAMP(14);
                 constexpr int U = 4;
                 for (int e0 = ct; e0 < nb; e0 += kConsumers * U) {
                     float z[U * VE];
