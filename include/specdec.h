@@ -35,6 +35,7 @@
 #ifndef SPECDEC_H
 #define SPECDEC_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -94,6 +95,15 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  and S = sum_i exp(z_i / T - m) on random requests, (max_i z_i, NaN) on
  *                  greedy ones; (NaN, NaN) for rows not read. Entries of a request skipped
  *                  for SPECDEC_ST_BAD_OFFSETS are left untouched (its rows are unknown).
+ *   workspace      device scratch of at least specdec_workspace_size(B, V) bytes, 16-byte
+ *                  aligned, caller-owned, or NULL. With a workspace the verify runs as two kernels:
+ *                  the first walks each request's rows to its stop row and records the draw it
+ *                  needs; the second does all draws at once, chunk-parallel over the vocabulary, so
+ *                  the long draw passes no longer sit at the end of each request's serial chain.
+ *                  Without one, a single kernel does everything. Results are identical. The
+ *                  workspace needs no initialisation and holds nothing between calls; calls that
+ *                  share one workspace must not overlap in time (use one per stream).
+ *   workspace_bytes its size in bytes.
  *   stream         a cudaStream_t (NULL = legacy default stream).
  *
  * Rows after a request's first rejection are never read.
@@ -127,6 +137,8 @@ specdec_status_t specdec_verify(
     uint32_t* status,
     float* diag_accept_prob,
     float* diag_row_stats,
+    void* workspace,
+    size_t workspace_bytes,
     void* stream);
 
 /*
@@ -136,6 +148,9 @@ specdec_status_t specdec_verify(
  * stream reports an error.
  */
 specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
+
+/* Bytes of workspace specdec_verify uses for B requests of vocabulary size V (0 if B or V <= 0). */
+size_t specdec_workspace_size(int32_t B, int32_t V);
 
 /* Human-readable name of a status code (static storage). */
 const char* specdec_status_string(specdec_status_t status);

@@ -27,7 +27,8 @@ ST_K_TOO_LARGE = 8
 ST_BAD_OFFSETS = 16
 ST_DEVICE_TIMEOUT = 32
 
-EXPORTED = ("specdec_verify", "specdec_wait", "specdec_status_string", "specdec_launch_config")
+EXPORTED = ("specdec_verify", "specdec_wait", "specdec_status_string", "specdec_launch_config",
+            "specdec_workspace_size")
 
 _lib = None
 
@@ -49,7 +50,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.specdec_verify.restype = ctypes.c_int
     lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
-                                   vp, vp, vp, vp, vp, vp, vp]
+                                   vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.specdec_workspace_size.restype = ctypes.c_size_t
+    lib.specdec_workspace_size.argtypes = [i32, i32]
     lib.specdec_wait.restype = ctypes.c_int
     lib.specdec_wait.argtypes = [vp, i32]
     lib.specdec_status_string.restype = ctypes.c_char_p
@@ -74,6 +77,10 @@ def launch_config(V: int, dtype: int, B: int = 1024) -> dict:
             "slice_ids": w.value}
 
 
+def workspace_size(B: int, V: int) -> int:
+    return int(load().specdec_workspace_size(int(B), int(V)))
+
+
 def _p(t) -> Optional[int]:
     if t is None:
         return None
@@ -82,7 +89,8 @@ def _p(t) -> Optional[int]:
 
 def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
                    bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
-                   status=None, diag_accept_prob=None, diag_row_stats=None, stream=None, logits_dtype=None) -> None:
+                   status=None, diag_accept_prob=None, diag_row_stats=None, workspace=None, stream=None,
+                   logits_dtype=None) -> None:
     """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
     (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
     non-zero status."""
@@ -99,7 +107,8 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
                     ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
                     ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
                     ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
-                    ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats)):
+                    ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
+                    ("workspace", workspace)):
         if t is not None and hasattr(t, "is_cuda"):
             if not t.is_cuda:
                 raise ValueError(f"{name} must be a CUDA tensor")
@@ -113,9 +122,13 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
         _p(target_logits), int(logits_dtype), _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
         int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
-        _p(diag_row_stats), stream)
+        _p(diag_row_stats), _p(workspace), 0 if workspace is None else _nbytes(workspace), stream)
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_verify")
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size() if hasattr(t, "numel") else 0
 
 
 def specdec_wait(stream=None, timeout_ms: int = -1) -> None:

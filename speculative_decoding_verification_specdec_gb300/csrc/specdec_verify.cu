@@ -104,6 +104,31 @@ struct Args {
     int32_t G;              // CTAs per request (cluster size)
     int32_t bulk;           // 1: rows staged with bulk async copies; 0: plain loads
     int32_t vec_noise;      // 1: noise / q rows are 16-byte aligned (128-bit loads)
+    // two-phase mode (a caller workspace was given): the row kernel stops at the decision and
+    // leaves one draw descriptor per request; the draw kernel does the draws chunk-parallel
+    struct DrawDesc* desc;
+    struct DrawPartial* partials;
+    uint32_t* tickets;
+    int32_t draw_chunks;    // chunks of kDrawIds ids per row in the draw kernel
+};
+
+// What the draw kernel needs to finish request b (written by the row kernel's rank-0 leader).
+struct DrawDesc {
+    int64_t t;              // row of logits / noise / mask to draw from
+    int64_t d;              // draft slot of the q row (draft-model residual)
+    float MC;               // exponent reference round(m * c)
+    float invS;             // 1 / sum of exp2(z * c - MC)
+    float c;                // log2(e) / T
+    int32_t code;           // 0: no draw; else the draw kind (p, residual with q, one-hot residual)
+    int32_t x;              // draft token (excluded by the one-hot residual)
+    int32_t pad;
+};
+
+struct DrawPartial {
+    float best;
+    int32_t idx;
+    int32_t flag;
+    int32_t pad;
 };
 
 // Partial result of one row pass, combined thread -> warp -> CTA -> cluster.
@@ -1266,7 +1291,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             }
         }
         consumer_sync();
-        SPECDEC_STAMP(1);
+        SPECDEC_STAMP(sh.sparse ? 15 : 1);
         const int k = rs.k, g = sh.g;
         const bool greedy = sh.greedy != 0, qmode = sh.qmode != 0, sparse = sh.sparse != 0;
         const float c = sh.c;
@@ -1503,6 +1528,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         };
 
         int acc_len = 0, emitted = -1;
+        bool deferred = false;
+        if (writer && a.desc) {                          // no draw unless one is posted below
+            a.desc[b].code = 0;
+            a.tickets[b] = 0u;
+        }
         if (rs.skip == 0) {
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
@@ -1642,12 +1672,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         else code = qmode ? kDecDrawQ : kDecDrawOneHot;
                     }
                 }
-                post(code);
+                // two-phase mode: the draw is left to the draw kernel
+                const bool defer = stop && a.desc != nullptr &&
+                                   (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot);
+                if (defer && writer) {
+                    DrawDesc dd;
+                    dd.t = t;
+                    dd.d = d;
+                    dd.MC = MC;
+                    dd.invS = 1.f / S_mc;
+                    dd.c = c;
+                    dd.code = code;
+                    dd.x = x;
+                    dd.pad = 0;
+                    a.desc[b] = dd;
+                }
+                post(defer ? kDecDone : code);
                 if (!stop) continue;
 
                 // drain the chunks of row j+1 the producer queued before this decision
                 if (!sparse && j < k)
                     for (int ch = 0; ch < spec; ++ch) release(wait_full());
+                if (defer) { acc_len = j; deferred = true; break; }
 
                 // ---- a9/a10: draw pass(es) over the stop / bonus row
                 while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
@@ -1737,7 +1783,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // ---- a11: emit, count
         if (writer) {
             if (rs.skip == 0) {
-                a.out_tokens[rs.row0 + acc_len] = emitted;
+                if (!deferred) a.out_tokens[rs.row0 + acc_len] = emitted;
                 for (int j = acc_len + 1; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
                 atomicAdd(&a.counters[0], (unsigned long long)k);
                 atomicAdd(&a.counters[1], (unsigned long long)(k - g));
@@ -1754,6 +1800,156 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
     // a copy that missed its deadline marks the request (any CTA of it) after rank 0 wrote status
     if (NC > 1) cluster_sync_all();
     if (tid == 0 && sh.timed_out && a.status) atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------------------------
+// draw kernel (two-phase mode): the recovered / bonus draws, chunk-parallel
+// ---------------------------------------------------------------------------------------------
+//
+// One CTA per (request, chunk of kDrawIds ids). Each thread owns kDrawPer consecutive ids:
+// it loads their logits, noise and (draft-model residual) q with 128-bit loads -- only the
+// 16-byte groups the bitmask allows -- and scores them; the CTA's best (score, id) goes to the
+// workspace, and the last CTA of the request to finish (atomic ticket) combines the chunks in
+// order and writes the token. An empty draft-model residual (no positive weight anywhere)
+// falls back to p in that last CTA.
+
+constexpr int kDrawThreads = 256;
+constexpr int kDrawPer = 16;                           // ids per thread
+constexpr int kDrawIds = kDrawThreads * kDrawPer;      // ids per CTA
+
+template <typename ET>
+__device__ __forceinline__ Part draw_chunk_part(const Args& a, const DrawDesc& dd, int code, int i0, int n)
+{
+    constexpr int VE = Elem<ET>::VE;
+    constexpr int NG = kDrawPer / VE;                  // 16-byte groups of logits per thread
+    static_assert(kDrawPer % VE == 0 && kDrawPer % 4 == 0, "thread span");
+    const int j0 = i0 + (int)threadIdx.x * kDrawPer;   // first id of this thread
+    Part p = part_identity();
+    if (j0 >= i0 + n) return p;
+    const bool wq = (code == kDecDrawQ);
+    const ET* lrow = reinterpret_cast<const ET*>(a.logits) + dd.t * (int64_t)a.V;
+    const float* erow = a.noise + dd.t * (int64_t)a.V;
+    const float* qrow = wq ? a.q + dd.d * (int64_t)a.V : nullptr;
+    const int32_t* mrow = a.bitmask ? a.bitmask + dd.t * (int64_t)a.W : nullptr;
+    float z[kDrawPer], ev[kDrawPer], qv[kDrawPer];
+    if (a.bulk && j0 + kDrawPer <= a.V) {
+        // aligned layout and a whole span: 128-bit loads, skipped for groups the mask forbids
+        uint32_t bits = 0xffffu;
+        if (mrow) bits = ((uint32_t)__ldg(mrow + (j0 >> 5)) >> (j0 & 31)) & 0xffffu;
+        const uint32_t ni = Raw<ET>::kNegInf;
+#pragma unroll
+        for (int gq = 0; gq < NG; ++gq) {
+            const bool live = ((bits >> (gq * VE)) & ((1u << VE) - 1u)) != 0u;
+            const uint4 u = live ? __ldg(reinterpret_cast<const uint4*>(lrow + j0) + gq) : make_uint4(ni, ni, ni, ni);
+            unpack_raw<ET>(u, z + gq * VE);
+        }
+#pragma unroll
+        for (int h = 0; h < kDrawPer / 4; ++h) {
+            const bool live = ((bits >> (4 * h)) & 0xfu) != 0u;
+            const float4 f = live ? __ldcs(reinterpret_cast<const float4*>(erow + j0) + h) : make_float4(1.f, 1.f, 1.f, 1.f);
+            const float4 g4 = (live && wq) ? __ldcs(reinterpret_cast<const float4*>(qrow + j0) + h) : make_float4(0.f, 0.f, 0.f, 0.f);
+            ev[4 * h] = f.x; ev[4 * h + 1] = f.y; ev[4 * h + 2] = f.z; ev[4 * h + 3] = f.w;
+            qv[4 * h] = g4.x; qv[4 * h + 1] = g4.y; qv[4 * h + 2] = g4.z; qv[4 * h + 3] = g4.w;
+        }
+        if (mrow && bits != 0xffffu) {
+#pragma unroll
+            for (int e = 0; e < kDrawPer; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
+        }
+    } else {
+        // any layout: scalar loads with bounds
+#pragma unroll
+        for (int e = 0; e < kDrawPer; ++e) {
+            const int i = j0 + e;
+            const bool in = i < a.V && (!mrow || (((uint32_t)mrow[i >> 5] >> (i & 31)) & 1u));
+            float zz = -INFINITY;
+            if (in) {
+                if constexpr (sizeof(ET) == 4) zz = lrow[i];
+                else zz = __uint_as_float((uint32_t)lrow[i] << 16);
+            }
+            z[e] = zz;
+            ev[e] = in ? erow[i] : 1.f;
+            qv[e] = (in && wq) ? qrow[i] : 0.f;
+        }
+    }
+    const int xslot = (code == kDecDrawOneHot && dd.x >= j0 && dd.x < j0 + kDrawPer) ? dd.x - j0 : -1;
+    draw_lazy<1, kDrawPer>(p, z, ev, qv, j0, 0, xslot, code, dd.c, dd.MC, dd.invS);
+    return p;
+}
+
+__device__ __forceinline__ Part draw_block_reduce(Part p, Part* wsh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    p = warp_reduce(p, 0.f);
+    if (lane == 0) wsh[warp] = p;
+    __syncthreads();
+    Part r = part_identity();
+    if (threadIdx.x == 0)
+        for (int w = 0; w < kDrawThreads / 32; ++w) combine(r, wsh[w], 0.f);
+    return r;                                           // valid in thread 0
+}
+
+template <typename ET>
+__global__ void __launch_bounds__(kDrawThreads, 4) specdec_draw_kernel(const Args a)
+{
+    __shared__ Part wsh[kDrawThreads / 32];
+    __shared__ int last;
+    const int nch = a.draw_chunks;
+    const int b = blockIdx.x / nch, ch = blockIdx.x % nch;
+    const DrawDesc dd = a.desc[b];
+    if (dd.code == 0) return;
+    const int i0 = ch * kDrawIds;
+    const int n = min(kDrawIds, a.V - i0);
+
+    const Part r = draw_block_reduce(draw_chunk_part<ET>(a, dd, dd.code, i0, n), wsh);
+    if (threadIdx.x == 0) {
+        DrawPartial dp;
+        dp.best = r.best;
+        dp.idx = r.idx;
+        dp.flag = r.flag;
+        dp.pad = 0;
+        a.partials[(size_t)b * nch + ch] = dp;
+        __threadfence();
+        const unsigned ticket = atomicAdd(&a.tickets[b], 1u);
+        last = (ticket == (unsigned)(nch - 1));
+    }
+    __syncthreads();
+    if (!last) return;
+
+    // the last chunk of request b: combine the partials in chunk order (ties to the lower id)
+    __threadfence();
+    __shared__ int token_sh, empty_sh;
+    if (threadIdx.x == 0) {
+        Part q = part_identity();
+        for (int c2 = 0; c2 < nch; ++c2) {
+            const volatile DrawPartial* pp = &a.partials[(size_t)b * nch + c2];
+            Part o = part_identity();
+            o.best = pp->best;
+            o.idx = pp->idx;
+            o.flag = pp->flag;
+            combine(q, o, 0.f);
+        }
+        token_sh = q.idx == INT_MAX ? -1 : q.idx;
+        empty_sh = (dd.code == kDecDrawQ && !q.flag) ? 1 : 0;
+    }
+    __syncthreads();
+    int token = token_sh;
+    if (empty_sh) {
+        // empty residual: draw from p over the whole row (rare; one CTA)
+        Part q = part_identity();
+        for (int c2 = 0; c2 < nch; ++c2) {
+            const int j0 = c2 * kDrawIds;
+            const Part pr = draw_block_reduce(draw_chunk_part<ET>(a, dd, kDecDrawP, j0, min(kDrawIds, a.V - j0)), wsh);
+            if (threadIdx.x == 0) combine(q, pr, 0.f);
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) token_sh = q.idx == INT_MAX ? -1 : q.idx;
+        __syncthreads();
+        token = token_sh;
+    }
+    if (threadIdx.x == 0) {
+        a.out_tokens[dd.t] = token;
+        a.tickets[b] = 0u;
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1928,6 +2124,34 @@ specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t strea
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+inline size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// Workspace of the two-phase mode: draw descriptors [B], chunk partials [B * chunks], tickets [B].
+struct WorkspaceLayout {
+    size_t desc_off, part_off, ticket_off, bytes;
+    int chunks;
+};
+
+WorkspaceLayout workspace_layout(int32_t B, int32_t V)
+{
+    WorkspaceLayout L;
+    L.chunks = (int)(((long long)V + kDrawIds - 1) / kDrawIds);
+    L.desc_off = 0;
+    L.part_off = round16(L.desc_off + sizeof(DrawDesc) * (size_t)B);
+    L.ticket_off = round16(L.part_off + sizeof(DrawPartial) * (size_t)B * (size_t)L.chunks);
+    L.bytes = round16(L.ticket_off + sizeof(uint32_t) * (size_t)B);
+    return L;
+}
+
+template <typename ET>
+specdec_status_t launch_draws(const Args& args, int32_t B, cudaStream_t stream)
+{
+    const unsigned grid = (unsigned)B * (unsigned)args.draw_chunks;
+    specdec_draw_kernel<ET><<<grid, kDrawThreads, 0, stream>>>(args);
+    const cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
@@ -1949,7 +2173,8 @@ extern "C" specdec_status_t specdec_verify(
     const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
     int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
     const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
-    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* stream)
+    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* workspace, size_t workspace_bytes,
+    void* stream)
 {
     if (logits_dtype != SPECDEC_F32 && logits_dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     if (B < 0 || V < 1 || max_k < 0 || max_k > SPECDEC_KMAX) return SPECDEC_ERR_INVALID_ARG;
@@ -1997,9 +2222,32 @@ extern "C" specdec_status_t specdec_verify(
              (!bitmask || (aligned(bitmask, 16) && a.W % 4 == 0)) && aligned(exp_noise, 16) &&
              (!draft_probs || aligned(draft_probs, 16));
     a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
+    a.desc = nullptr;
+    a.partials = nullptr;
+    a.tickets = nullptr;
+    a.draw_chunks = 0;
+    const bool two_phase = workspace != nullptr && shape.stream;
+    if (two_phase) {
+        const WorkspaceLayout L = workspace_layout(B, V);
+        if (!aligned(workspace, 16) || workspace_bytes < L.bytes) return SPECDEC_ERR_INVALID_ARG;
+        unsigned char* ws = static_cast<unsigned char*>(workspace);
+        a.desc = reinterpret_cast<DrawDesc*>(ws + L.desc_off);
+        a.partials = reinterpret_cast<DrawPartial*>(ws + L.part_off);
+        a.tickets = reinterpret_cast<uint32_t*>(ws + L.ticket_off);
+        a.draw_chunks = L.chunks;
+        if ((long long)B * L.chunks > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
+    }
 
-    if (logits_dtype == SPECDEC_F32) return launch<float>(a, shape, B, (cudaStream_t)stream);
-    return launch<uint16_t>(a, shape, B, (cudaStream_t)stream);
+    const cudaStream_t st = (cudaStream_t)stream;
+    specdec_status_t rc2 = logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, B, st) : launch<uint16_t>(a, shape, B, st);
+    if (rc2 != SPECDEC_OK || !two_phase) return rc2;
+    return logits_dtype == SPECDEC_F32 ? launch_draws<float>(a, B, st) : launch_draws<uint16_t>(a, B, st);
+}
+
+extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)
+{
+    if (B <= 0 || V <= 0) return 0;
+    return workspace_layout(B, V).bytes;
 }
 
 extern "C" specdec_status_t specdec_wait(void* stream, int32_t timeout_ms)

@@ -49,6 +49,7 @@ class Outputs:
     status: object
     diag_accept_prob: Optional[object] = None
     diag_row_stats: Optional[object] = None
+    workspace: Optional[object] = None
 
     def numpy(self) -> Dict[str, np.ndarray]:
         d = {"out_tokens": self.out_tokens, "out_num_accepted": self.out_num_accepted,
@@ -68,9 +69,11 @@ class Outputs:
         return res
 
 
-def alloc_outputs(w: Workload, device="cuda", diag: bool = False) -> Outputs:
+def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: bool = True) -> Outputs:
+    """Output tensors (and, with workspace=True, the verify's scratch: the two-kernel mode)."""
     import torch
 
+    ws_bytes = _native.workspace_size(w.B, w.V) if workspace else 0
     return Outputs(
         out_tokens=torch.full((w.T,), -7, dtype=torch.int32, device=device),
         out_num_accepted=torch.full((w.B,), -7, dtype=torch.int32, device=device),
@@ -78,6 +81,7 @@ def alloc_outputs(w: Workload, device="cuda", diag: bool = False) -> Outputs:
         status=torch.zeros(w.B, dtype=torch.int32, device=device),
         diag_accept_prob=torch.full((max(w.N, 1),), float("nan"), dtype=torch.float32, device=device) if diag else None,
         diag_row_stats=torch.full((max(w.T, 1), 2), float("nan"), dtype=torch.float32, device=device) if diag else None,
+        workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None,
     )
 
 
@@ -87,15 +91,15 @@ def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> No
         dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
         w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
         out.out_tokens, out.out_num_accepted, out.counters, out.status,
-        out.diag_accept_prob, out.diag_row_stats, stream=stream)
+        out.diag_accept_prob, out.diag_row_stats, workspace=out.workspace, stream=stream)
 
 
-def run(w: Workload, device="cuda", diag: bool = True) -> Dict[str, np.ndarray]:
+def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True) -> Dict[str, np.ndarray]:
     """Copy, verify, synchronise, and return the outputs as numpy arrays."""
     import torch
 
     dev = device_tensors(w, device)
-    out = alloc_outputs(w, device, diag=diag)
+    out = alloc_outputs(w, device, diag=diag, workspace=workspace)
     verify(w, dev, out)
     torch.cuda.synchronize()
     return out.numpy()

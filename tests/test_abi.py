@@ -80,11 +80,12 @@ def _call(lib, **over):
     # fake, aligned, non-NULL device addresses: every case below fails (or returns) before any
     # CUDA call, so nothing is dereferenced
     a = dict(logits=4096, dtype=0, ids=4096, q=None, has_q=None, cu=4096, B=4, V=1000, max_k=3, mask=None,
-             temp=4096, u=4096, noise=4096, out=4096, acc=4096, ctr=4096, status=None, da=None, dr=None)
+             temp=4096, u=4096, noise=4096, out=4096, acc=4096, ctr=4096, status=None, da=None, dr=None,
+             ws=None, ws_bytes=0)
     a.update(over)
     return lib.specdec_verify(a["logits"], a["dtype"], a["ids"], a["q"], a["has_q"], a["cu"], a["B"], a["V"],
                               a["max_k"], a["mask"], a["temp"], a["u"], a["noise"], a["out"], a["acc"],
-                              a["ctr"], a["status"], a["da"], a["dr"], None)
+                              a["ctr"], a["status"], a["da"], a["dr"], a["ws"], a["ws_bytes"], None)
 
 
 def test_host_validation(lib, monkeypatch):
@@ -104,6 +105,18 @@ def test_host_validation(lib, monkeypatch):
     assert _call(lib, ctr=4100) == E.SPECDEC_ERR_INVALID_ARG      # counters need 8-byte alignment
     assert _call(lib, mask=4097) == E.SPECDEC_ERR_INVALID_ARG
     assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
+
+
+def test_workspace_size_and_validation(lib, monkeypatch):
+    E = _native
+    assert _native.workspace_size(0, 1000) == 0 and _native.workspace_size(4, 0) == 0
+    small, big = _native.workspace_size(4, 1000), _native.workspace_size(1024, 151936)
+    assert small > 0 and big > small and small % 16 == 0 and big % 16 == 0
+    assert big < 8 * 1024 * 1024                      # a few hundred bytes per request
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    # a workspace that is too small or misaligned is refused before anything runs
+    assert _call(lib, ws=4096, ws_bytes=small - 16) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, ws=4104, ws_bytes=small) == E.SPECDEC_ERR_INVALID_ARG
 
 
 def test_product_path_has_no_oracle_import():

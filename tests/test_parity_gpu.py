@@ -27,8 +27,11 @@ def cuda():
     return "cuda:0"
 
 
+_MODE = {"workspace": True}
+
+
 def check_parity(w, cuda, label=""):
-    got = device.run(w, device=cuda, diag=True)
+    got = device.run(w, device=cuda, diag=True, workspace=_MODE["workspace"])
     ref = oracle.verify(w)
     rep = parity.compare(w, got, ref)
     assert not (got["status"] & _native.ST_DEVICE_TIMEOUT).any()
@@ -38,13 +41,17 @@ def check_parity(w, cuda, label=""):
     return rep, got, ref
 
 
-KERNELS = ["stream", "cluster"]
+KERNELS = ["stream", "stream_fused", "cluster"]
 
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", request.param)
-    return request.param
+    """stream: the two-kernel mode (row kernel + draw kernel, with a workspace); stream_fused: the
+    streaming kernel alone (no workspace); cluster: the slice-resident cluster kernel."""
+    monkeypatch.setenv("SPECDEC_KERNEL", "cluster" if request.param == "cluster" else "stream")
+    _MODE["workspace"] = request.param == "stream"
+    yield request.param
+    _MODE["workspace"] = True
 
 
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3])
@@ -202,7 +209,7 @@ def test_rows_after_stop_are_never_read(cuda, kernel):
             poisoned.exp_noise[t] = np.nan
             n_poisoned += 1
     assert n_poisoned > 20
-    got = device.run(poisoned, device=cuda, diag=True)
+    got = device.run(poisoned, device=cuda, diag=True, workspace=_MODE["workspace"])
     rep = parity.compare(w, got, ref)
     assert rep.ok, rep.summary()
     # the library reports which rows it read: exactly rows 0..a_b of each request
@@ -221,7 +228,7 @@ def test_counters_accumulate_and_runs_are_deterministic(cuda, kernel):
                      q_mode="half", draft_sigma=0.5, mask="half", mask_density=0.1, mask_run_len=16,
                      forced_invalid_frac=0.2)
     dev = device.device_tensors(w, cuda)
-    out = device.alloc_outputs(w, cuda, diag=True)
+    out = device.alloc_outputs(w, cuda, diag=True, workspace=_MODE["workspace"])
     device.verify(w, dev, out)
     torch.cuda.synchronize()
     first = out.numpy()
@@ -269,7 +276,7 @@ def test_chi_square_on_gpu(cuda, kernel):
         "bonus_only": (_pins._chi2_batch(n, z1[None, :], 1.3, "mf", x_fixed=[], seed=74), z1, 1.3, None, 1),
     }
     for name, (w, z, T, al, stride) in variants.items():
-        got = device.run(w, device=cuda, diag=False)
+        got = device.run(w, device=cuda, diag=False, workspace=_MODE["workspace"])
         first = got["out_tokens"][0::stride]
         p = _pins._target_p(z, T, al)
         chi2, df = _pins._chi2(np.bincount(first, minlength=V), p)
