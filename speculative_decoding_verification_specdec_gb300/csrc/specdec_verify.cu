@@ -121,7 +121,7 @@ struct DrawDesc {
     float c;                // log2(e) / T
     int32_t code;           // 0: no draw; else the draw kind (p, residual with q, one-hot residual)
     int32_t x;              // draft token (excluded by the one-hot residual)
-    int32_t pad;
+    int32_t sparse;         // 1: the bitmask allows few ids (gather only allowed groups)
 };
 
 struct DrawPartial {
@@ -1684,7 +1684,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     dd.c = c;
                     dd.code = code;
                     dd.x = x;
-                    dd.pad = 0;
+                    dd.sparse = sparse ? 1 : 0;
                     a.desc[b] = dd;
                 }
                 post(defer ? kDecDone : code);
@@ -1803,29 +1803,40 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 }
 
 // ---------------------------------------------------------------------------------------------
-// draw kernel (two-phase mode): the recovered / bonus draws, chunk-parallel
+// draw kernel (two-kernel mode): the recovered / bonus draws of all requests, chunk-parallel
 // ---------------------------------------------------------------------------------------------
 //
-// One CTA per (request, chunk of kDrawIds ids). Each thread owns kDrawPer consecutive ids:
-// it loads their logits, noise and (draft-model residual) q with 128-bit loads -- only the
-// 16-byte groups the bitmask allows -- and scores them; the CTA's best (score, id) goes to the
-// workspace, and the last CTA of the request to finish (atomic ticket) combines the chunks in
-// order and writes the token. An empty draft-model residual (no positive weight anywhere)
-// falls back to p in that last CTA.
+// A persistent grid (two CTAs per SM) walks the units (request, chunk of kDrawIds ids) in a
+// fixed stride; units of requests without a draw are skipped by producer and consumers alike.
+// Dense units are staged by the producer warp with bulk async copies (logits, noise, q, mask
+// words) in a two-stage ring; units of sparse requests are gathered by the consumers directly,
+// only the 16-byte groups the bitmask allows. Each unit's best (score, id) goes to the workspace;
+// the CTA that completes the last unit of a request (atomic ticket) combines them in chunk order
+// and writes the token. An empty draft-model residual falls back to p in that CTA.
 
-constexpr int kDrawThreads = 256;
-constexpr int kDrawPer = 16;                           // ids per thread
-constexpr int kDrawIds = kDrawThreads * kDrawPer;      // ids per CTA
+constexpr int kDrawIds = 4096;                         // ids per unit
+constexpr int kDrawStages = 2;
+constexpr int kDrawPer = kDrawIds / kConsumers;        // ids per consumer thread in a unit (16)
 
+template <typename ET> struct DrawGeom {
+    static constexpr int ES = (int)sizeof(ET);
+    static constexpr int kNoiseOff = kDrawIds * ES;
+    static constexpr int kQOff = kDrawIds * (ES + 4);
+    static constexpr int kMaskOff = kDrawIds * (ES + 8);
+    static constexpr int kStageBytes = kMaskOff + kDrawIds / 8;
+    static_assert(kNoiseOff % 16 == 0 && kQOff % 16 == 0 && kMaskOff % 16 == 0 && kStageBytes % 16 == 0, "alignment");
+};
+
+// This consumer thread's partial over ids [j0, j0 + kDrawPer) of a unit, from global memory
+// (sparse requests, unaligned layouts, and the empty-residual fallback).
 template <typename ET>
-__device__ __forceinline__ Part draw_chunk_part(const Args& a, const DrawDesc& dd, int code, int i0, int n)
+__device__ __forceinline__ Part draw_span_global(const Args& a, const DrawDesc& dd, int code, int j0)
 {
     constexpr int VE = Elem<ET>::VE;
-    constexpr int NG = kDrawPer / VE;                  // 16-byte groups of logits per thread
+    constexpr int NG = kDrawPer / VE;
     static_assert(kDrawPer % VE == 0 && kDrawPer % 4 == 0, "thread span");
-    const int j0 = i0 + (int)threadIdx.x * kDrawPer;   // first id of this thread
     Part p = part_identity();
-    if (j0 >= i0 + n) return p;
+    if (j0 >= a.V) return p;
     const bool wq = (code == kDecDrawQ);
     const ET* lrow = reinterpret_cast<const ET*>(a.logits) + dd.t * (int64_t)a.V;
     const float* erow = a.noise + dd.t * (int64_t)a.V;
@@ -1833,7 +1844,6 @@ __device__ __forceinline__ Part draw_chunk_part(const Args& a, const DrawDesc& d
     const int32_t* mrow = a.bitmask ? a.bitmask + dd.t * (int64_t)a.W : nullptr;
     float z[kDrawPer], ev[kDrawPer], qv[kDrawPer];
     if (a.bulk && j0 + kDrawPer <= a.V) {
-        // aligned layout and a whole span: 128-bit loads, skipped for groups the mask forbids
         uint32_t bits = 0xffffu;
         if (mrow) bits = ((uint32_t)__ldg(mrow + (j0 >> 5)) >> (j0 & 31)) & 0xffffu;
         const uint32_t ni = Raw<ET>::kNegInf;
@@ -1856,7 +1866,6 @@ __device__ __forceinline__ Part draw_chunk_part(const Args& a, const DrawDesc& d
             for (int e = 0; e < kDrawPer; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
         }
     } else {
-        // any layout: scalar loads with bounds
 #pragma unroll
         for (int e = 0; e < kDrawPer; ++e) {
             const int i = j0 + e;
@@ -1876,80 +1885,178 @@ __device__ __forceinline__ Part draw_chunk_part(const Args& a, const DrawDesc& d
     return p;
 }
 
-__device__ __forceinline__ Part draw_block_reduce(Part p, Part* wsh)
+// The same partial from a staged unit in shared memory (stage = the unit's ids from i0).
+template <typename ET>
+__device__ __forceinline__ Part draw_span_smem(const Args& a, const DrawDesc& dd, const unsigned char* stg, int i0, int n)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    p = warp_reduce(p, 0.f);
-    if (lane == 0) wsh[warp] = p;
-    __syncthreads();
-    Part r = part_identity();
-    if (threadIdx.x == 0)
-        for (int w = 0; w < kDrawThreads / 32; ++w) combine(r, wsh[w], 0.f);
-    return r;                                           // valid in thread 0
+    using DG = DrawGeom<ET>;
+    constexpr int VE = Elem<ET>::VE;
+    constexpr int NG = kDrawPer / VE;
+    const int ct = (int)threadIdx.x - 32;
+    const int e0 = ct * kDrawPer;
+    Part p = part_identity();
+    if (e0 >= n) return p;
+    const bool wq = (dd.code == kDecDrawQ);
+    float z[kDrawPer], ev[kDrawPer], qv[kDrawPer];
+#pragma unroll
+    for (int gq = 0; gq < NG; ++gq)
+        unpack_raw<ET>(reinterpret_cast<const uint4*>(stg + (size_t)e0 * DG::ES)[gq], z + gq * VE);
+#pragma unroll
+    for (int h = 0; h < kDrawPer / 4; ++h) {
+        const float4 f = reinterpret_cast<const float4*>(stg + DG::kNoiseOff + (size_t)e0 * 4)[h];
+        ev[4 * h] = f.x; ev[4 * h + 1] = f.y; ev[4 * h + 2] = f.z; ev[4 * h + 3] = f.w;
+        if (wq) {
+            const float4 g4 = reinterpret_cast<const float4*>(stg + DG::kQOff + (size_t)e0 * 4)[h];
+            qv[4 * h] = g4.x; qv[4 * h + 1] = g4.y; qv[4 * h + 2] = g4.z; qv[4 * h + 3] = g4.w;
+        } else {
+            qv[4 * h] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
+        }
+    }
+    uint32_t bits = 0xffffu;
+    if (a.bitmask) bits = (reinterpret_cast<const uint32_t*>(stg + DG::kMaskOff)[e0 >> 5] >> (e0 & 31)) & 0xffffu;
+    if (e0 + kDrawPer > n) bits &= (1u << (n - e0)) - 1u;   // the row ends inside this span
+    if (bits != 0xffffu) {
+#pragma unroll
+        for (int e = 0; e < kDrawPer; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
+    }
+    const int j0 = i0 + e0;
+    const int xslot = (dd.code == kDecDrawOneHot && dd.x >= j0 && dd.x < j0 + kDrawPer) ? dd.x - j0 : -1;
+    draw_lazy<1, kDrawPer>(p, z, ev, qv, j0, 0, xslot, dd.code, dd.c, dd.MC, dd.invS);
+    return p;
 }
 
+struct DrawShared {
+    uint64_t full[kDrawStages];
+    uint64_t empty[kDrawStages];
+    Part wpart[2][kConsumerWarps];
+    int32_t last;
+};
+
 template <typename ET>
-__global__ void __launch_bounds__(kDrawThreads, 4) specdec_draw_kernel(const Args a)
+__global__ void __launch_bounds__(kStreamThreads, 2) specdec_draw_kernel(const Args a)
 {
-    __shared__ Part wsh[kDrawThreads / 32];
-    __shared__ int last;
+    using DG = DrawGeom<ET>;
+    extern __shared__ __align__(128) unsigned char dring[];
+    __shared__ DrawShared sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nch = a.draw_chunks;
-    const int b = blockIdx.x / nch, ch = blockIdx.x % nch;
-    const DrawDesc dd = a.desc[b];
-    if (dd.code == 0) return;
-    const int i0 = ch * kDrawIds;
-    const int n = min(kDrawIds, a.V - i0);
+    const long long units = (long long)a.B * nch;
 
-    const Part r = draw_block_reduce(draw_chunk_part<ET>(a, dd, dd.code, i0, n), wsh);
-    if (threadIdx.x == 0) {
-        DrawPartial dp;
-        dp.best = r.best;
-        dp.idx = r.idx;
-        dp.flag = r.flag;
-        dp.pad = 0;
-        a.partials[(size_t)b * nch + ch] = dp;
-        __threadfence();
-        const unsigned ticket = atomicAdd(&a.tickets[b], 1u);
-        last = (ticket == (unsigned)(nch - 1));
+    if (tid == 0) {
+        for (int s = 0; s < kDrawStages; ++s) {
+            mbar_init(smem_addr(&sh.full[s]), a.bulk ? 1u : 32u);
+            mbar_init(smem_addr(&sh.empty[s]), kConsumerWarps);
+        }
+        fence_mbar_init();
     }
     __syncthreads();
-    if (!last) return;
 
-    // the last chunk of request b: combine the partials in chunk order (ties to the lower id)
-    __threadfence();
-    __shared__ int token_sh, empty_sh;
-    if (threadIdx.x == 0) {
-        Part q = part_identity();
-        for (int c2 = 0; c2 < nch; ++c2) {
-            const volatile DrawPartial* pp = &a.partials[(size_t)b * nch + c2];
-            Part o = part_identity();
-            o.best = pp->best;
-            o.idx = pp->idx;
-            o.flag = pp->flag;
-            combine(q, o, 0.f);
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (a.bulk) {
+            uint32_t it = 0;
+            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+                const int b = (int)(u / nch), ch = (int)(u % nch);
+                const DrawDesc dd = a.desc[b];
+                if (dd.code == 0 || dd.sparse) continue;
+                const int s = (int)(it % kDrawStages);
+                if (!mbar_wait_bounded(smem_addr(&sh.empty[s]), ((it / kDrawStages) & 1u) ^ 1u) && lane == 0 && a.status)
+                    atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
+                if (lane == 0) {
+                    unsigned char* st = dring + (size_t)s * DG::kStageBytes;
+                    const int i0 = ch * kDrawIds;
+                    const int n = min(kDrawIds, a.V - i0);
+                    const bool wq = dd.code == kDecDrawQ;
+                    const uint32_t lb = (uint32_t)n * DG::ES, eb = (uint32_t)n * 4u, qb = wq ? eb : 0u;
+                    const int nw = (n + 31) / 32;
+                    const uint32_t mb = a.bitmask ? (uint32_t)nw * 4u : 0u;
+                    const uint32_t bar = smem_addr(&sh.full[s]);
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(bar, lb + eb + qb + mb);
+                    bulk_copy_g2s(smem_addr(st), reinterpret_cast<const ET*>(a.logits) + dd.t * (int64_t)a.V + i0, lb, bar);
+                    bulk_copy_g2s(smem_addr(st + DG::kNoiseOff), a.noise + dd.t * (int64_t)a.V + i0, eb, bar);
+                    if (qb) bulk_copy_g2s(smem_addr(st + DG::kQOff), a.q + dd.d * (int64_t)a.V + i0, qb, bar);
+                    if (mb) bulk_copy_g2s(smem_addr(st + DG::kMaskOff), a.bitmask + dd.t * (int64_t)a.W + (i0 >> 5), mb, bar);
+                }
+                ++it;
+            }
         }
-        token_sh = q.idx == INT_MAX ? -1 : q.idx;
-        empty_sh = (dd.code == kDecDrawQ && !q.flag) ? 1 : 0;
+    } else {
+        // ------------------------------------------------------------------ consumers
+        const int ct = tid - 32, cw = warp - 1;
+        const bool leader = (ct == 0);
+        uint32_t it = 0;
+        int par = 0;
+        auto reduce = [&](Part p) -> Part {
+            p = warp_reduce(p, 0.f);
+            if (lane == 0) sh.wpart[par][cw] = p;
+            consumer_sync();
+            Part r = part_identity();
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], 0.f);
+            par ^= 1;
+            return r;
+        };
+        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+            const int b = (int)(u / nch), ch = (int)(u % nch);
+            const DrawDesc dd = a.desc[b];
+            if (dd.code == 0) continue;
+            const int i0 = ch * kDrawIds;
+            const int n = min(kDrawIds, a.V - i0);
+            Part p;
+            if (a.bulk && !dd.sparse) {
+                const int s = (int)(it % kDrawStages);
+                if (!mbar_wait_bounded(smem_addr(&sh.full[s]), (it / kDrawStages) & 1u) && leader && a.status)
+                    atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
+                p = draw_span_smem<ET>(a, dd, dring + (size_t)s * DG::kStageBytes, i0, n);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_addr(&sh.empty[s]));
+                ++it;
+            } else {
+                p = draw_span_global<ET>(a, dd, dd.code, i0 + ct * kDrawPer);
+            }
+            const Part r = reduce(p);
+            if (leader) {
+                DrawPartial dp;
+                dp.best = r.best;
+                dp.idx = r.idx;
+                dp.flag = r.flag;
+                dp.pad = 0;
+                a.partials[(size_t)b * nch + ch] = dp;
+                __threadfence();
+                const unsigned ticket = atomicAdd(&a.tickets[b], 1u);
+                sh.last = (ticket == (unsigned)(nch - 1));
+            }
+            consumer_sync();
+            if (!sh.last) continue;
+
+            // the last unit of request b: combine the partials in chunk order (ties to the lower id)
+            __threadfence();
+            Part q = part_identity();
+            for (int c2 = 0; c2 < nch; ++c2) {
+                const volatile DrawPartial* pp = &a.partials[(size_t)b * nch + c2];
+                Part o = part_identity();
+                o.best = pp->best;
+                o.idx = pp->idx;
+                o.flag = pp->flag;
+                combine(q, o, 0.f);
+            }
+            if (dd.code == kDecDrawQ && !q.flag) {
+                // empty residual: draw from p over the whole row (rare), consumers only
+                q = part_identity();
+                for (int c2 = 0; c2 < nch; ++c2) {
+                    const Part pr = reduce(draw_span_global<ET>(a, dd, kDecDrawP, c2 * kDrawIds + ct * kDrawPer));
+                    combine(q, pr, 0.f);
+                }
+            }
+            if (leader) {
+                a.out_tokens[dd.t] = q.idx == INT_MAX ? -1 : q.idx;
+                a.tickets[b] = 0u;
+            }
+            consumer_sync();
+        }
     }
     __syncthreads();
-    int token = token_sh;
-    if (empty_sh) {
-        // empty residual: draw from p over the whole row (rare; one CTA)
-        Part q = part_identity();
-        for (int c2 = 0; c2 < nch; ++c2) {
-            const int j0 = c2 * kDrawIds;
-            const Part pr = draw_block_reduce(draw_chunk_part<ET>(a, dd, kDecDrawP, j0, min(kDrawIds, a.V - j0)), wsh);
-            if (threadIdx.x == 0) combine(q, pr, 0.f);
-            __syncthreads();
-        }
-        if (threadIdx.x == 0) token_sh = q.idx == INT_MAX ? -1 : q.idx;
-        __syncthreads();
-        token = token_sh;
-    }
-    if (threadIdx.x == 0) {
-        a.out_tokens[dd.t] = token;
-        a.tickets[b] = 0u;
-    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -2146,8 +2253,17 @@ WorkspaceLayout workspace_layout(int32_t B, int32_t V)
 template <typename ET>
 specdec_status_t launch_draws(const Args& args, int32_t B, cudaStream_t stream)
 {
-    const unsigned grid = (unsigned)B * (unsigned)args.draw_chunks;
-    specdec_draw_kernel<ET><<<grid, kDrawThreads, 0, stream>>>(args);
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(specdec_draw_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kDrawStages * DrawGeom<ET>::kStageBytes);
+    });
+    if (attr_err != cudaSuccess) return SPECDEC_ERR_CUDA;
+    const long long units = (long long)B * args.draw_chunks;
+    long long grid = 2LL * device_sms();
+    if (grid > units) grid = units;
+    specdec_draw_kernel<ET><<<(unsigned)grid, kStreamThreads, (size_t)kDrawStages * DrawGeom<ET>::kStageBytes, stream>>>(args);
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
