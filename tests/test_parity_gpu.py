@@ -83,6 +83,8 @@ SWEEP = [
     (40000, W.F32, 29, (1, 8), "none", "uniform(0.5,2.0)", "all"),
     (70008, W.BF16, 40, (1, 8), "half", "half_greedy(0.5,1.2)", "half"),
     (131072, W.F32, 24, (3, 6), "all", 0.8, "all"),
+    (4100, W.F32, 17, (1, 5), "all", 0.9, "none"),                    # last draw unit: 4 ids
+    (8200, W.BF16, 17, (1, 5), "half", "uniform(0.5,1.2)", "none"),   # last draw unit: 8 ids
 ]
 
 
