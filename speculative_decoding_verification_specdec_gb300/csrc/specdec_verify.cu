@@ -952,7 +952,7 @@ __device__ __forceinline__ void draw_batch(Part& p, const float* z, const float*
         float w = pe;
         if (code == kDecDrawQ) w = fmaxf(pe - qv[i], 0.f);
         else if (code == kDecDrawOneHot) w = (ids[i] == x) ? 0.f : pe;
-        const bool cand = w > 0.f;
+        const bool cand = w > 0.f && z[i] > -INFINITY;      // a forbidden / absent id never qualifies
         any |= cand ? 1 : 0;
         sc[i] = cand ? w * fast_rcp(E[i]) : -1.f;
     }
@@ -1062,7 +1062,7 @@ __device__ __forceinline__ void draw_lazy(Part& p, const float* z, const float* 
         float w = pe;
         if (code == kDecDrawQ) w = fmaxf(pe - qv[i], 0.f);
         else if (code == kDecDrawOneHot && i == xslot) w = 0.f;
-        const bool cand = w > 0.f;
+        const bool cand = w > 0.f && z[i] > -INFINITY;      // a forbidden / absent id never qualifies
         any |= cand ? 1 : 0;
         sc[i] = cand ? w * fast_rcp(E[i]) : -1.f;
     }
