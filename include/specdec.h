@@ -96,13 +96,16 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  greedy ones; (NaN, NaN) for rows not read. Entries of a request skipped
  *                  for SPECDEC_ST_BAD_OFFSETS are left untouched (its rows are unknown).
  *   workspace      device scratch of at least specdec_workspace_size(B, V) bytes, 16-byte
- *                  aligned, caller-owned, or NULL. With a workspace the verify runs as two kernels:
- *                  the first walks each request's rows to its stop row and records the draw it
- *                  needs; the second does all draws at once, chunk-parallel over the vocabulary, so
- *                  the long draw passes no longer sit at the end of each request's serial chain.
- *                  Without one, a single kernel does everything. Results are identical. The
- *                  workspace needs no initialisation and holds nothing between calls; calls that
- *                  share one workspace must not overlap in time (use one per stream).
+ *                  aligned, caller-owned, or NULL. With a workspace a one-CTA kernel first orders
+ *                  the requests by an estimate of their work, heaviest first, and the verify
+ *                  kernel takes them in that order (list scheduling by the longest-processing-
+ *                  time rule: a long request that sits late in the batch no longer runs on alone
+ *                  after the rest have finished). The schedule runs only when the batch needs more
+ *                  than one wave of resident CTAs (two per SM); the verify kernel then starts as a
+ *                  programmatic dependent of it. Without a workspace, requests start in index order.
+ *                  Results are identical either way; only the timing differs. The workspace
+ *                  needs no initialisation and holds nothing between calls; calls that share one
+ *                  workspace must not overlap in time (use one per stream).
  *   workspace_bytes its size in bytes.
  *   stream         a cudaStream_t (NULL = legacy default stream).
  *
@@ -114,11 +117,12 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * keeps each row slice on chip, a row wider than 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
  *
  * Kernels: by default each request is verified by a cluster of G CTAs (G = 1 for large
- * batches, up to 8 for small ones), each streaming its slice of every row through a ring of
+ * batches, up to 4 for small ones), each streaming its slice of every row through a ring of
  * 32 KB shared-memory stages filled by bulk async copies; requests whose bitmask allows few ids
  * gather only the allowed 16-byte groups instead. Setting the environment variable
  * SPECDEC_KERNEL=cluster selects the alternative kernel that keeps a slice of every row resident
- * in shared memory; SPECDEC_CTAS_PER_REQUEST=G forces G. All shapes compute identical results.
+ * in shared memory; SPECDEC_CTAS_PER_REQUEST=G forces G; SPECDEC_SCHEDULE=1 (0) forces the request
+ * schedule on (off) whenever a workspace is given. All shapes compute identical results.
  */
 specdec_status_t specdec_verify(
     const void* target_logits, specdec_dtype_t logits_dtype,
@@ -149,7 +153,8 @@ specdec_status_t specdec_verify(
  */
 specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
 
-/* Bytes of workspace specdec_verify uses for B requests of vocabulary size V (0 if B or V <= 0). */
+/* Bytes of workspace specdec_verify uses for B requests of vocabulary size V (0 if B or V <= 0):
+ * the request order (int32 per request) and one cost byte per request. */
 size_t specdec_workspace_size(int32_t B, int32_t V);
 
 /* Human-readable name of a status code (static storage). */

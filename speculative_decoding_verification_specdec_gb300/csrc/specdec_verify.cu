@@ -104,31 +104,9 @@ struct Args {
     int32_t G;              // CTAs per request (cluster size)
     int32_t bulk;           // 1: rows staged with bulk async copies; 0: plain loads
     int32_t vec_noise;      // 1: noise / q rows are 16-byte aligned (128-bit loads)
-    // two-phase mode (a caller workspace was given): the row kernel stops at the decision and
-    // leaves one draw descriptor per request; the draw kernel does the draws chunk-parallel
-    struct DrawDesc* desc;
-    struct DrawPartial* partials;
-    uint32_t* tickets;
-    int32_t draw_chunks;    // chunks of kDrawIds ids per row in the draw kernel
-};
-
-// What the draw kernel needs to finish request b (written by the row kernel's rank-0 leader).
-struct DrawDesc {
-    int64_t t;              // row of logits / noise / mask to draw from
-    int64_t d;              // draft slot of the q row (draft-model residual)
-    float MC;               // exponent reference round(m * c)
-    float invS;             // 1 / sum of exp2(z * c - MC)
-    float c;                // log2(e) / T
-    int32_t code;           // 0: no draw; else the draw kind (p, residual with q, one-hot residual)
-    int32_t x;              // draft token (excluded by the one-hot residual)
-    int32_t sparse;         // 1: the bitmask allows few ids (gather only allowed groups)
-};
-
-struct DrawPartial {
-    float best;
-    int32_t idx;
-    int32_t flag;
-    int32_t pad;
+    // request schedule: cluster i verifies request order[i] (a permutation of [0, B), heaviest
+    // expected work first), or request i when NULL
+    const int32_t* order;
 };
 
 // Partial result of one row pass, combined thread -> warp -> CTA -> cluster.
@@ -155,6 +133,19 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Programmatic dependent launch: the schedule kernel lets the verify kernel's CTAs start early;
+// they set up their barriers, then wait here until the schedule grid has completed and its
+// writes are visible. A kernel launched without the dependency returns at once.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -525,7 +516,6 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rank = (int)cluster_ctarank();
-    const int b = (int)cluster_id_x();
     const int64_t lo = (int64_t)rank * a.slice_units * kUnit;
     const int64_t hi = min((int64_t)a.V, lo + (int64_t)a.slice_units * kUnit);
     const int n = (int)max((int64_t)0, hi - lo);
@@ -540,6 +530,8 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
         fence_mbar_init();
         sh.timed_out = 0;
     }
+    grid_dependency_wait();                                        // the request order is ready
+    const int b = a.order ? a.order[cluster_id_x()] : (int)cluster_id_x();
 
     // ---- a1 ragged decode + a4 grammar-valid prefix (warp 0)
     const int32_t d0 = a.cu[b];
@@ -728,6 +720,7 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
 constexpr int kConsumers = 256;
 constexpr int kConsumerWarps = kConsumers / 32;
 constexpr int kStreamThreads = kConsumers + 32;
+constexpr int kResidentPerSM = 2;              // streaming CTAs per SM (registers and shared memory)
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kStages = 3;
 constexpr int kSpec = 2;
@@ -1196,7 +1189,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int NC = a.G;                                           // CTAs per request (cluster)
     const int rank = (int)cluster_ctarank();
-    const int b = (int)cluster_id_x();
     const int lo = rank * a.slice_units * kUnit;
     const int hi = min(a.V, lo + a.slice_units * kUnit);
     const int nrow_chunks = (hi - lo + G::kRowIds - 1) / G::kRowIds;
@@ -1218,6 +1210,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
     }
     // every CTA of the request has initialised its barriers before any partial is sent
     if (NC > 1) cluster_sync_all(); else __syncthreads();
+    grid_dependency_wait();                                        // the request order is ready
+    const int b = a.order ? a.order[cluster_id_x()] : (int)cluster_id_x();
 
     const ReqShape rs = request_shape(a, b);
 
@@ -1453,7 +1447,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
                         for (int q = 0; q < VE; ++q) {
                             z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
-                            ids[u * VE + q] = grp * VE + q;
+                            ids[u * VE + q] = in ? grp * VE + q : -1;   // an unused slot matches no draft
                         }
                     }
                     if (greedy) {
@@ -1518,7 +1512,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
                         for (int q = 0; q < VE; ++q) {
                             z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
-                            ids[u * VE + q] = grp * VE + q;
+                            ids[u * VE + q] = in ? grp * VE + q : -1;
                         }
                     }
                     draw_batch<U * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
@@ -1528,11 +1522,6 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         };
 
         int acc_len = 0, emitted = -1;
-        bool deferred = false;
-        if (writer && a.desc) {                          // no draw unless one is posted below
-            a.desc[b].code = 0;
-            a.tickets[b] = 0u;
-        }
         if (rs.skip == 0) {
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
@@ -1672,28 +1661,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         else code = qmode ? kDecDrawQ : kDecDrawOneHot;
                     }
                 }
-                // two-phase mode: the draw is left to the draw kernel
-                const bool defer = stop && a.desc != nullptr &&
-                                   (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot);
-                if (defer && writer) {
-                    DrawDesc dd;
-                    dd.t = t;
-                    dd.d = d;
-                    dd.MC = MC;
-                    dd.invS = 1.f / S_mc;
-                    dd.c = c;
-                    dd.code = code;
-                    dd.x = x;
-                    dd.sparse = sparse ? 1 : 0;
-                    a.desc[b] = dd;
-                }
-                post(defer ? kDecDone : code);
+                post(code);
                 if (!stop) continue;
 
                 // drain the chunks of row j+1 the producer queued before this decision
                 if (!sparse && j < k)
                     for (int ch = 0; ch < spec; ++ch) release(wait_full());
-                if (defer) { acc_len = j; deferred = true; break; }
 
                 // ---- a9/a10: draw pass(es) over the stop / bonus row
                 while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
@@ -1783,7 +1756,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // ---- a11: emit, count
         if (writer) {
             if (rs.skip == 0) {
-                if (!deferred) a.out_tokens[rs.row0 + acc_len] = emitted;
+                a.out_tokens[rs.row0 + acc_len] = emitted;
                 for (int j = acc_len + 1; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
                 atomicAdd(&a.counters[0], (unsigned long long)k);
                 atomicAdd(&a.counters[1], (unsigned long long)(k - g));
@@ -1803,260 +1776,120 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 }
 
 // ---------------------------------------------------------------------------------------------
-// draw kernel (two-kernel mode): the recovered / bonus draws of all requests, chunk-parallel
+// request schedule (longest-processing-time first)
 // ---------------------------------------------------------------------------------------------
 //
-// A persistent grid (two CTAs per SM) walks the units (request, chunk of kDrawIds ids) in a
-// fixed stride; units of requests without a draw are skipped by producer and consumers alike.
-// Dense units are staged by the producer warp with bulk async copies (logits, noise, q, mask
-// words) in a two-stage ring; units of sparse requests are gathered by the consumers directly,
-// only the 16-byte groups the bitmask allows. Each unit's best (score, id) goes to the workspace;
-// the CTA that completes the last unit of a request (atomic ticket) combines them in chunk order
-// and writes the token. An empty draft-model residual falls back to p in that CTA.
+// The requests of a batch are independent chains of row passes whose lengths differ by more
+// than 10x: a greedy request streams logits rows only, a sampled one adds a draw pass over the
+// stop row's logits, noise and (draft model) q, and a request with a sparse bitmask gathers a
+// fraction of every row. The block scheduler starts clusters in index order as slots free up,
+// so a heavy request that sits late in the batch runs on alone after the others have finished.
+// Ordering the requests heaviest first (the longest-processing-time rule of list scheduling)
+// lets the light ones fill in behind. The order only affects timing: every request's outputs
+// are the same under any order.
+//
+// One CTA computes an integer cost key per request and a stable counting sort of the keys,
+// descending, into order[B]. The key estimates the request's HBM work in units of 1/16 of a
+// dense logits row, without knowing where it will stop:
+//   rows: (k + 1) * 0.6 (greedy) or * 0.35 (sampled: a rejection ends the chain sooner),
+//   draw: 0.85 * (bytes per id of logits + noise [+ q]) / (bytes per id of logits),
+//   sparse requests (the same test the verify kernel applies): a quarter of that.
 
-constexpr int kDrawIds = 4096;                         // ids per unit
-constexpr int kDrawStages = 2;
-constexpr int kDrawPer = kDrawIds / kConsumers;        // ids per consumer thread in a unit (16)
+constexpr int kSchedThreads = 1024;
+constexpr int kSchedWarps = kSchedThreads / 32;
+constexpr int kSchedKeys = 256;
 
-template <typename ET> struct DrawGeom {
-    static constexpr int ES = (int)sizeof(ET);
-    static constexpr int kNoiseOff = kDrawIds * ES;
-    static constexpr int kQOff = kDrawIds * (ES + 4);
-    static constexpr int kMaskOff = kDrawIds * (ES + 8);
-    static constexpr int kStageBytes = kMaskOff + kDrawIds / 8;
-    static_assert(kNoiseOff % 16 == 0 && kQOff % 16 == 0 && kMaskOff % 16 == 0 && kStageBytes % 16 == 0, "alignment");
-};
-
-// This consumer thread's partial over ids [j0, j0 + kDrawPer) of a unit, from global memory
-// (sparse requests, unaligned layouts, and the empty-residual fallback).
 template <typename ET>
-__device__ __forceinline__ Part draw_span_global(const Args& a, const DrawDesc& dd, int code, int j0)
+__device__ __forceinline__ int request_cost_key(const Args& a, int b)
 {
-    constexpr int VE = Elem<ET>::VE;
-    constexpr int NG = kDrawPer / VE;
-    static_assert(kDrawPer % VE == 0 && kDrawPer % 4 == 0, "thread span");
-    Part p = part_identity();
-    if (j0 >= a.V) return p;
-    const bool wq = (code == kDecDrawQ);
-    const ET* lrow = reinterpret_cast<const ET*>(a.logits) + dd.t * (int64_t)a.V;
-    const float* erow = a.noise + dd.t * (int64_t)a.V;
-    const float* qrow = wq ? a.q + dd.d * (int64_t)a.V : nullptr;
-    const int32_t* mrow = a.bitmask ? a.bitmask + dd.t * (int64_t)a.W : nullptr;
-    float z[kDrawPer], ev[kDrawPer], qv[kDrawPer];
-    if (a.bulk && j0 + kDrawPer <= a.V) {
-        uint32_t bits = 0xffffu;
-        if (mrow) bits = ((uint32_t)__ldg(mrow + (j0 >> 5)) >> (j0 & 31)) & 0xffffu;
-        const uint32_t ni = Raw<ET>::kNegInf;
-#pragma unroll
-        for (int gq = 0; gq < NG; ++gq) {
-            const bool live = ((bits >> (gq * VE)) & ((1u << VE) - 1u)) != 0u;
-            const uint4 u = live ? __ldg(reinterpret_cast<const uint4*>(lrow + j0) + gq) : make_uint4(ni, ni, ni, ni);
-            unpack_raw<ET>(u, z + gq * VE);
+    const ReqShape rs = request_shape(a, b);
+    if (rs.skip != 0) return 0;
+    const float T = a.temperature[b];
+    const bool tvalid = (T == 0.f) || (T >= FLT_MIN && T <= FLT_MAX);
+    const bool greedy = !(T > 0.f) || !tvalid;
+    const bool qmode = a.q != nullptr && (a.has_q == nullptr || a.has_q[b] != 0);
+    bool sparse = false;
+    if (a.bitmask != nullptr && a.bulk) {
+        // the verify kernel's test, one thread instead of one warp: fewer than half of the
+        // first min(W, 32) mask words' bits set (rows are 16-byte aligned on this path)
+        const int nw = min(a.W, 32);
+        const uint4* m = reinterpret_cast<const uint4*>(a.bitmask + rs.row0 * (int64_t)a.W);
+        int ones = 0;
+        for (int i = 0; i < nw / 4; ++i) {
+            const uint4 u = __ldg(m + i);
+            ones += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
         }
-#pragma unroll
-        for (int h = 0; h < kDrawPer / 4; ++h) {
-            const bool live = ((bits >> (4 * h)) & 0xfu) != 0u;
-            const float4 f = live ? __ldcs(reinterpret_cast<const float4*>(erow + j0) + h) : make_float4(1.f, 1.f, 1.f, 1.f);
-            const float4 g4 = (live && wq) ? __ldcs(reinterpret_cast<const float4*>(qrow + j0) + h) : make_float4(0.f, 0.f, 0.f, 0.f);
-            ev[4 * h] = f.x; ev[4 * h + 1] = f.y; ev[4 * h + 2] = f.z; ev[4 * h + 3] = f.w;
-            qv[4 * h] = g4.x; qv[4 * h + 1] = g4.y; qv[4 * h + 2] = g4.z; qv[4 * h + 3] = g4.w;
-        }
-        if (mrow && bits != 0xffffu) {
-#pragma unroll
-            for (int e = 0; e < kDrawPer; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kDrawPer; ++e) {
-            const int i = j0 + e;
-            const bool in = i < a.V && (!mrow || (((uint32_t)mrow[i >> 5] >> (i & 31)) & 1u));
-            float zz = -INFINITY;
-            if (in) {
-                if constexpr (sizeof(ET) == 4) zz = lrow[i];
-                else zz = __uint_as_float((uint32_t)lrow[i] << 16);
-            }
-            z[e] = zz;
-            ev[e] = in ? erow[i] : 1.f;
-            qv[e] = (in && wq) ? qrow[i] : 0.f;
-        }
+        sparse = 2 * ones < nw * 32;
     }
-    const int xslot = (code == kDecDrawOneHot && dd.x >= j0 && dd.x < j0 + kDrawPer) ? dd.x - j0 : -1;
-    draw_lazy<1, kDrawPer>(p, z, ev, qv, j0, 0, xslot, code, dd.c, dd.MC, dd.invS);
-    return p;
+    constexpr float es = (float)sizeof(ET);
+    float cost = (float)(rs.k + 1) * (greedy ? 0.6f : 0.35f);
+    if (!greedy) cost += 0.85f * (es + 4.f + (qmode ? 4.f : 0.f)) / es;
+    if (sparse) cost *= 0.25f;
+    return min(kSchedKeys - 1, (int)(cost * 16.f + 0.5f));
 }
 
-// The same partial from a staged unit in shared memory (stage = the unit's ids from i0).
-template <typename ET>
-__device__ __forceinline__ Part draw_span_smem(const Args& a, const DrawDesc& dd, const unsigned char* stg, int i0, int n)
-{
-    using DG = DrawGeom<ET>;
-    constexpr int VE = Elem<ET>::VE;
-    constexpr int NG = kDrawPer / VE;
-    const int ct = (int)threadIdx.x - 32;
-    const int e0 = ct * kDrawPer;
-    Part p = part_identity();
-    if (e0 >= n) return p;
-    const bool wq = (dd.code == kDecDrawQ);
-    float z[kDrawPer], ev[kDrawPer], qv[kDrawPer];
-#pragma unroll
-    for (int gq = 0; gq < NG; ++gq)
-        unpack_raw<ET>(reinterpret_cast<const uint4*>(stg + (size_t)e0 * DG::ES)[gq], z + gq * VE);
-#pragma unroll
-    for (int h = 0; h < kDrawPer / 4; ++h) {
-        const float4 f = reinterpret_cast<const float4*>(stg + DG::kNoiseOff + (size_t)e0 * 4)[h];
-        ev[4 * h] = f.x; ev[4 * h + 1] = f.y; ev[4 * h + 2] = f.z; ev[4 * h + 3] = f.w;
-        if (wq) {
-            const float4 g4 = reinterpret_cast<const float4*>(stg + DG::kQOff + (size_t)e0 * 4)[h];
-            qv[4 * h] = g4.x; qv[4 * h + 1] = g4.y; qv[4 * h + 2] = g4.z; qv[4 * h + 3] = g4.w;
-        } else {
-            qv[4 * h] = qv[4 * h + 1] = qv[4 * h + 2] = qv[4 * h + 3] = 0.f;
-        }
-    }
-    uint32_t bits = 0xffffu;
-    if (a.bitmask) bits = (reinterpret_cast<const uint32_t*>(stg + DG::kMaskOff)[e0 >> 5] >> (e0 & 31)) & 0xffffu;
-    if (e0 + kDrawPer > n) bits &= (1u << (n - e0)) - 1u;   // the row ends inside this span
-    if (bits != 0xffffu) {
-#pragma unroll
-        for (int e = 0; e < kDrawPer; ++e) z[e] = ((bits >> e) & 1u) ? z[e] : -INFINITY;
-    }
-    const int j0 = i0 + e0;
-    const int xslot = (dd.code == kDecDrawOneHot && dd.x >= j0 && dd.x < j0 + kDrawPer) ? dd.x - j0 : -1;
-    draw_lazy<1, kDrawPer>(p, z, ev, qv, j0, 0, xslot, dd.code, dd.c, dd.MC, dd.invS);
-    return p;
-}
-
-struct DrawShared {
-    uint64_t full[kDrawStages];
-    uint64_t empty[kDrawStages];
-    Part wpart[2][kConsumerWarps];
-    int32_t last;
+struct SchedShared {
+    int32_t cursor[kSchedKeys];                   // next output slot per key
+    int32_t wcnt[kSchedWarps][kSchedKeys];        // requests per (warp, key) in the current tile
 };
 
+// order[B]: the permutation; keys[B]: one byte per request (scratch).
 template <typename ET>
-__global__ void __launch_bounds__(kStreamThreads, 2) specdec_draw_kernel(const Args a)
+__global__ void __launch_bounds__(kSchedThreads) specdec_schedule_kernel(const Args a, int32_t* order, uint8_t* keys)
 {
-    using DG = DrawGeom<ET>;
-    extern __shared__ __align__(128) unsigned char dring[];
-    __shared__ DrawShared sh;
+    __shared__ SchedShared sh;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nch = a.draw_chunks;
-    const long long units = (long long)a.B * nch;
+    const int B = a.B;
+    allow_dependent_launch();          // the verify grid may start; it waits for this grid to finish
 
-    if (tid == 0) {
-        for (int s = 0; s < kDrawStages; ++s) {
-            mbar_init(smem_addr(&sh.full[s]), a.bulk ? 1u : 32u);
-            mbar_init(smem_addr(&sh.empty[s]), kConsumerWarps);
-        }
-        fence_mbar_init();
+    for (int i = tid; i < kSchedKeys; i += kSchedThreads) sh.cursor[i] = 0;
+    __syncthreads();
+    // pass 1: keys and their histogram
+    for (int b = tid; b < B; b += kSchedThreads) {
+        const int key = request_cost_key<ET>(a, b);
+        keys[b] = (uint8_t)key;
+        atomicAdd(&sh.cursor[key], 1);
     }
     __syncthreads();
-
+    // exclusive prefix over keys in descending order: first slot of each key (warp 0, 8 keys a lane)
     if (warp == 0) {
-        // ------------------------------------------------------------------ producer
-        if (a.bulk) {
-            uint32_t it = 0;
-            for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-                const int b = (int)(u / nch), ch = (int)(u % nch);
-                const DrawDesc dd = a.desc[b];
-                if (dd.code == 0 || dd.sparse) continue;
-                const int s = (int)(it % kDrawStages);
-                if (!mbar_wait_bounded(smem_addr(&sh.empty[s]), ((it / kDrawStages) & 1u) ^ 1u) && lane == 0 && a.status)
-                    atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
-                if (lane == 0) {
-                    unsigned char* st = dring + (size_t)s * DG::kStageBytes;
-                    const int i0 = ch * kDrawIds;
-                    const int n = min(kDrawIds, a.V - i0);
-                    const bool wq = dd.code == kDecDrawQ;
-                    const uint32_t lb = (uint32_t)n * DG::ES, eb = (uint32_t)n * 4u, qb = wq ? eb : 0u;
-                    const int nw = (n + 31) / 32;
-                    const uint32_t mb = a.bitmask ? (uint32_t)nw * 4u : 0u;
-                    const uint32_t bar = smem_addr(&sh.full[s]);
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar, lb + eb + qb + mb);
-                    bulk_copy_g2s(smem_addr(st), reinterpret_cast<const ET*>(a.logits) + dd.t * (int64_t)a.V + i0, lb, bar);
-                    bulk_copy_g2s(smem_addr(st + DG::kNoiseOff), a.noise + dd.t * (int64_t)a.V + i0, eb, bar);
-                    if (qb) bulk_copy_g2s(smem_addr(st + DG::kQOff), a.q + dd.d * (int64_t)a.V + i0, qb, bar);
-                    if (mb) bulk_copy_g2s(smem_addr(st + DG::kMaskOff), a.bitmask + dd.t * (int64_t)a.W + (i0 >> 5), mb, bar);
-                }
-                ++it;
-            }
-        }
-    } else {
-        // ------------------------------------------------------------------ consumers
-        const int ct = tid - 32, cw = warp - 1;
-        const bool leader = (ct == 0);
-        uint32_t it = 0;
-        int par = 0;
-        auto reduce = [&](Part p) -> Part {
-            p = warp_reduce(p, 0.f);
-            if (lane == 0) sh.wpart[par][cw] = p;
-            consumer_sync();
-            Part r = part_identity();
+        int v[kSchedKeys / 32], sum = 0;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], 0.f);
-            par ^= 1;
-            return r;
-        };
-        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-            const int b = (int)(u / nch), ch = (int)(u % nch);
-            const DrawDesc dd = a.desc[b];
-            if (dd.code == 0) continue;
-            const int i0 = ch * kDrawIds;
-            const int n = min(kDrawIds, a.V - i0);
-            Part p;
-            if (a.bulk && !dd.sparse) {
-                const int s = (int)(it % kDrawStages);
-                if (!mbar_wait_bounded(smem_addr(&sh.full[s]), (it / kDrawStages) & 1u) && leader && a.status)
-                    atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
-                p = draw_span_smem<ET>(a, dd, dring + (size_t)s * DG::kStageBytes, i0, n);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_addr(&sh.empty[s]));
-                ++it;
-            } else {
-                p = draw_span_global<ET>(a, dd, dd.code, i0 + ct * kDrawPer);
-            }
-            const Part r = reduce(p);
-            if (leader) {
-                DrawPartial dp;
-                dp.best = r.best;
-                dp.idx = r.idx;
-                dp.flag = r.flag;
-                dp.pad = 0;
-                a.partials[(size_t)b * nch + ch] = dp;
-                __threadfence();
-                const unsigned ticket = atomicAdd(&a.tickets[b], 1u);
-                sh.last = (ticket == (unsigned)(nch - 1));
-            }
-            consumer_sync();
-            if (!sh.last) continue;
-
-            // the last unit of request b: combine the partials in chunk order (ties to the lower id)
-            __threadfence();
-            Part q = part_identity();
-            for (int c2 = 0; c2 < nch; ++c2) {
-                const volatile DrawPartial* pp = &a.partials[(size_t)b * nch + c2];
-                Part o = part_identity();
-                o.best = pp->best;
-                o.idx = pp->idx;
-                o.flag = pp->flag;
-                combine(q, o, 0.f);
-            }
-            if (dd.code == kDecDrawQ && !q.flag) {
-                // empty residual: draw from p over the whole row (rare), consumers only
-                q = part_identity();
-                for (int c2 = 0; c2 < nch; ++c2) {
-                    const Part pr = reduce(draw_span_global<ET>(a, dd, kDecDrawP, c2 * kDrawIds + ct * kDrawPer));
-                    combine(q, pr, 0.f);
-                }
-            }
-            if (leader) {
-                a.out_tokens[dd.t] = q.idx == INT_MAX ? -1 : q.idx;
-                a.tickets[b] = 0u;
-            }
-            consumer_sync();
+        for (int e = 0; e < kSchedKeys / 32; ++e) { v[e] = sh.cursor[kSchedKeys - 1 - (lane * 8 + e)]; sum += v[e]; }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
         }
+        int run = incl - sum;
+#pragma unroll
+        for (int e = 0; e < kSchedKeys / 32; ++e) { sh.cursor[kSchedKeys - 1 - (lane * 8 + e)] = run; run += v[e]; }
     }
     __syncthreads();
+    // pass 2: stable placement, one tile of kSchedThreads requests at a time in index order
+    const unsigned lt = (1u << lane) - 1u;
+    for (int t0 = 0; t0 < B; t0 += kSchedThreads) {
+        for (int i = tid; i < kSchedWarps * kSchedKeys; i += kSchedThreads) (&sh.wcnt[0][0])[i] = 0;
+        __syncthreads();
+        const int b = t0 + tid;
+        const int key = b < B ? (int)keys[b] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (key >= 0 && (peers & lt) == 0u) sh.wcnt[warp][key] = __popc(peers);
+        __syncthreads();
+        if (key >= 0) {
+            int pos = sh.cursor[key] + __popc(peers & lt);
+            for (int w = 0; w < warp; ++w) pos += sh.wcnt[w][key];
+            order[pos] = b;
+        }
+        __syncthreads();
+        for (int k2 = tid; k2 < kSchedKeys; k2 += kSchedThreads) {
+            int add = 0;
+            for (int w = 0; w < kSchedWarps; ++w) add += sh.wcnt[w][k2];
+            sh.cursor[k2] += add;
+        }
+        __syncthreads();
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -2085,13 +1918,14 @@ int device_sms()
 
 // CTAs per request for the streaming kernel. A request is a serial chain of row passes and
 // one CTA streams at about its fair share of HBM (~1/300 of it with two CTAs per SM), so small
-// batches split each row over a few CTAs to shorten the chains; large batches keep one CTA per
-// request and let the block scheduler balance them. (Measured on GB300: B=64 -> 4, B=128 -> 2,
-// B >= 256 -> 1 were the fastest of {1, 2, 4, 8}.)
+// batches split each row over a few CTAs to shorten the chains; from about one request per SM
+// on, one CTA per request is fastest (the per-row exchange of a cluster costs more than the
+// shorter chain gains). (Measured on GB300: B=64 -> 2 or 4, B >= 128 -> 1 were the fastest of
+// {1, 2, 4}.)
 int stream_ctas_per_request(int32_t B, int sms)
 {
     const int b = B > 0 ? B : 1;
-    int G = (256 * sms / 152) / b;
+    int G = (128 * sms / 152) / b;
     if (G < 1) G = 1;
     if (G > 4) G = 4;
     return G;
@@ -2180,7 +2014,7 @@ int schedulable_cluster(void (*kernel)(Args), int G, int smem, int threads, cuda
 }
 
 template <typename ET>
-specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream)
+specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream, bool after_schedule)
 {
     if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
     void (*kernel)(Args) = sh.stream ? specdec_verify_stream_kernel<ET> : specdec_verify_kernel<ET>;
@@ -2214,13 +2048,15 @@ specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t strea
     cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)sh.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)sh.G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_schedule ? 2 : 1;
     cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, args);
     if (err != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2233,39 +2069,35 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
 
-// Workspace of the two-phase mode: draw descriptors [B], chunk partials [B * chunks], tickets [B].
-struct WorkspaceLayout {
-    size_t desc_off, part_off, ticket_off, bytes;
-    int chunks;
+// The schedule's scratch inside a caller workspace: order int32[B], then keys uint8[B].
+struct ScheduleLayout {
+    size_t order_off, keys_off, bytes;
 };
 
-WorkspaceLayout workspace_layout(int32_t B, int32_t V)
+ScheduleLayout schedule_layout(int32_t B)
 {
-    WorkspaceLayout L;
-    L.chunks = (int)(((long long)V + kDrawIds - 1) / kDrawIds);
-    L.desc_off = 0;
-    L.part_off = round16(L.desc_off + sizeof(DrawDesc) * (size_t)B);
-    L.ticket_off = round16(L.part_off + sizeof(DrawPartial) * (size_t)B * (size_t)L.chunks);
-    L.bytes = round16(L.ticket_off + sizeof(uint32_t) * (size_t)B);
+    ScheduleLayout L;
+    L.order_off = 0;
+    L.keys_off = round16(sizeof(int32_t) * (size_t)B);
+    L.bytes = round16(L.keys_off + (size_t)B);
     return L;
 }
 
 template <typename ET>
-specdec_status_t launch_draws(const Args& args, int32_t B, cudaStream_t stream)
+specdec_status_t launch_schedule(const Args& args, int32_t* order, uint8_t* keys, cudaStream_t stream)
 {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(specdec_draw_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kDrawStages * DrawGeom<ET>::kStageBytes);
-    });
-    if (attr_err != cudaSuccess) return SPECDEC_ERR_CUDA;
-    const long long units = (long long)B * args.draw_chunks;
-    long long grid = 2LL * device_sms();
-    if (grid > units) grid = units;
-    specdec_draw_kernel<ET><<<(unsigned)grid, kStreamThreads, (size_t)kDrawStages * DrawGeom<ET>::kStageBytes, stream>>>(args);
-    const cudaError_t err = cudaGetLastError();
-    return err == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kSchedThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    if (cudaLaunchKernelEx(&cfg, specdec_schedule_kernel<ET>, args, order, keys) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SPECDEC_ERR_CUDA;
+    }
+    return SPECDEC_OK;
 }
 
 }  // namespace
@@ -2338,32 +2170,36 @@ extern "C" specdec_status_t specdec_verify(
              (!bitmask || (aligned(bitmask, 16) && a.W % 4 == 0)) && aligned(exp_noise, 16) &&
              (!draft_probs || aligned(draft_probs, 16));
     a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
-    a.desc = nullptr;
-    a.partials = nullptr;
-    a.tickets = nullptr;
-    a.draw_chunks = 0;
-    const bool two_phase = workspace != nullptr && shape.stream;
-    if (two_phase) {
-        const WorkspaceLayout L = workspace_layout(B, V);
-        if (!aligned(workspace, 16) || workspace_bytes < L.bytes) return SPECDEC_ERR_INVALID_ARG;
-        unsigned char* ws = static_cast<unsigned char*>(workspace);
-        a.desc = reinterpret_cast<DrawDesc*>(ws + L.desc_off);
-        a.partials = reinterpret_cast<DrawPartial*>(ws + L.part_off);
-        a.tickets = reinterpret_cast<uint32_t*>(ws + L.ticket_off);
-        a.draw_chunks = L.chunks;
-        if ((long long)B * L.chunks > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
-    }
-
+    a.order = nullptr;
     const cudaStream_t st = (cudaStream_t)stream;
-    specdec_status_t rc2 = logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, B, st) : launch<uint16_t>(a, shape, B, st);
-    if (rc2 != SPECDEC_OK || !two_phase) return rc2;
-    return logits_dtype == SPECDEC_F32 ? launch_draws<float>(a, B, st) : launch_draws<uint16_t>(a, B, st);
+    if (workspace != nullptr) {
+        const ScheduleLayout L = schedule_layout(B);
+        if (!aligned(workspace, 16) || workspace_bytes < L.bytes) return SPECDEC_ERR_INVALID_ARG;
+    }
+    // heaviest requests first, when the grid does not fit in one wave of resident CTAs (with
+    // everything resident at once the order changes nothing): the schedule kernel writes the
+    // order the verify kernel reads
+    bool schedule = workspace != nullptr && (long long)B * shape.G > (long long)kResidentPerSM * device_sms();
+    if (const char* env = std::getenv("SPECDEC_SCHEDULE"))        // tests and comparison runs
+        schedule = workspace != nullptr && std::strcmp(env, "0") != 0;
+    if (schedule) {
+        const ScheduleLayout L = schedule_layout(B);
+        unsigned char* ws = static_cast<unsigned char*>(workspace);
+        int32_t* order = reinterpret_cast<int32_t*>(ws + L.order_off);
+        uint8_t* keys = ws + L.keys_off;
+        const specdec_status_t rs = logits_dtype == SPECDEC_F32 ? launch_schedule<float>(a, order, keys, st)
+                                                                : launch_schedule<uint16_t>(a, order, keys, st);
+        if (rs != SPECDEC_OK) return rs;
+        a.order = order;
+    }
+    const bool dep = a.order != nullptr;
+    return logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, B, st, dep) : launch<uint16_t>(a, shape, B, st, dep);
 }
 
 extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)
 {
     if (B <= 0 || V <= 0) return 0;
-    return workspace_layout(B, V).bytes;
+    return schedule_layout(B).bytes;
 }
 
 extern "C" specdec_status_t specdec_wait(void* stream, int32_t timeout_ms)

@@ -70,7 +70,7 @@ class Outputs:
 
 
 def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: bool = True) -> Outputs:
-    """Output tensors (and, with workspace=True, the verify's scratch: the two-kernel mode)."""
+    """Output tensors (and, with workspace=True, the verify's scratch: the request schedule)."""
     import torch
 
     ws_bytes = _native.workspace_size(w.B, w.V) if workspace else 0

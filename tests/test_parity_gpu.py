@@ -41,15 +41,17 @@ def check_parity(w, cuda, label=""):
     return rep, got, ref
 
 
-KERNELS = ["stream", "stream_fused", "cluster"]
+KERNELS = ["stream", "stream_index_order", "cluster"]
 
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    """stream: the two-kernel mode (row kernel + draw kernel, with a workspace); stream_fused: the
-    streaming kernel alone (no workspace); cluster: the slice-resident cluster kernel."""
+    """stream: the streaming kernel with a workspace (requests scheduled heaviest first);
+    stream_index_order: the same kernel without one (requests in index order); cluster: the
+    slice-resident cluster kernel (scheduled)."""
     monkeypatch.setenv("SPECDEC_KERNEL", "cluster" if request.param == "cluster" else "stream")
-    _MODE["workspace"] = request.param == "stream"
+    monkeypatch.setenv("SPECDEC_SCHEDULE", "0" if request.param == "stream_index_order" else "1")
+    _MODE["workspace"] = request.param != "stream_index_order"
     yield request.param
     _MODE["workspace"] = True
 
@@ -193,6 +195,28 @@ def test_mixed_density_rows(cuda, kernel):
             check_parity(w, cuda)
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_sparse_draft_in_first_group(cuda, kernel, dtype):
+    """Sparse rows (few allowed ids) whose draft sits in the row's first 16-byte group, with a
+    short list of allowed groups: the draft's logit must survive the unused list slots."""
+    V, ks = 512, [2, 2, 2, 2, 1, 1]
+    B, N = len(ks), sum(ks)
+    T = N + B
+    rng = np.random.default_rng(5)
+    logits = rng.normal(0.0, 2.0, size=(T, V)).astype(np.float32)
+    allowed = np.zeros((T, V), dtype=bool)
+    allowed[:, :8] = True
+    allowed[:, [100, 201, 333, 511]] = True
+    drafts = [1, 5, 3, 0, 7, 2, 6, 4, 1, 3][:N]
+    q = rng.random((N, V)).astype(np.float32) + 0.01
+    q /= q.sum(axis=1, keepdims=True)
+    u = np.full(T, 0.01, dtype=np.float32)
+    w = batch(V=V, ks=ks, logits=logits, draft_ids=drafts, temperature=[1.0, 0.8, 0.0, 1.3, 1.0, 0.0],
+              q=q, has_q=[1, 0, 1, 0, 1, 0], allowed=allowed, uniforms=u, dtype=dtype, name=f"first_group_{dtype}")
+    rep, got, ref = check_parity(w, cuda)
+    assert (ref.out_num_accepted > 0).any()          # some drafts are accepted: p(x) was read
+
+
 def test_rows_after_stop_are_never_read(cuda, kernel):
     w = W.make_batch(300, B=40, V=3000, k=(2, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
@@ -286,3 +310,47 @@ def test_chi_square_on_gpu(cuda, kernel):
         ref = oracle.verify(w)
         rep = parity.compare(w, got, ref)
         assert rep.ok, (name, rep.summary())
+
+
+def _schedule(w, cuda):
+    """Run one scheduled verify and return (order, keys) read back from the workspace."""
+    import torch
+
+    dev = device.device_tensors(w, cuda)
+    out = device.alloc_outputs(w, cuda, workspace=True)
+    device.verify(w, dev, out)
+    torch.cuda.synchronize()
+    ws = out.workspace.cpu().numpy()
+    order = ws[: 4 * w.B].view(np.int32).copy()
+    koff = (4 * w.B + 15) // 16 * 16
+    keys = ws[koff: koff + w.B].copy()
+    return order, keys, out.numpy()
+
+
+@pytest.mark.parametrize("B", [1, 37, 1024, 2500])
+def test_schedule_is_a_stable_descending_permutation(cuda, B, monkeypatch):
+    """The request order the schedule kernel writes: every request exactly once, cost keys
+    non-increasing along it, equal keys in index order (one and several 1024-request tiles)."""
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    monkeypatch.setenv("SPECDEC_SCHEDULE", "1")        # small batches fit one wave: force it
+    w = W.make_batch(23, name=f"sched_B{B}", B=B, V=1024, k=(0, 6), logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
+                     mask="half", mask_density=0.05, mask_run_len=16, forced_invalid_frac=0.2)
+    order, keys, _ = _schedule(w, cuda)
+    assert sorted(order.tolist()) == list(range(B))
+    ko = keys[order].astype(np.int64)
+    assert (np.diff(ko) <= 0).all()
+    same = np.diff(ko) == 0
+    assert (np.diff(order)[same] > 0).all()
+    if B > 1:
+        assert len(set(keys.tolist())) > 1          # the batch mixes request kinds
+
+
+def test_scheduled_parity_across_tiles(cuda, monkeypatch):
+    """More requests than one schedule tile, mixed kinds: identical to the oracle."""
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)   # 2100 CTAs: scheduled by default
+    w = W.make_batch(29, name="sched_parity_B2100", B=2100, V=640, k=(0, 5), logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
+                     mask="half", mask_density=0.1, mask_run_len=8, forced_invalid_frac=0.2)
+    check_parity(w, cuda)
