@@ -146,6 +146,51 @@ specdec_status_t specdec_verify(
     void* stream);
 
 /*
+ * specdec_verify_noalloc -- specdec_verify for callers that cannot hand the library scratch
+ * memory. The pages have no counterpart to this: it is a calling convention of this library,
+ * not a step of the method.
+ *
+ * Same arguments, semantics and results as specdec_verify, without workspace / workspace_bytes:
+ * the request schedule's scratch (an int32 order and a cost byte per request) is a fixed array
+ * inside the library, file-scope device memory of 80 KiB per device holding up to
+ * SPECDEC_NOALLOC_MAX_REQUESTS requests. The call allocates nothing (no cudaMalloc, no
+ * allocating library routine) and needs no memory from the caller beyond the batch itself.
+ * It serves callers that have no device allocator of their own (a plain C or C++ host program
+ * that links this library directly) and serving loops that must not allocate inside a decode
+ * step (cudaMalloc synchronises the device; a caching allocator may have to grow its pool).
+ *
+ *   B > SPECDEC_NOALLOC_MAX_REQUESTS: SPECDEC_ERR_UNSUPPORTED, checked before any CUDA call;
+ *   nothing is launched or written. Every other error is specdec_verify's.
+ *   Zeroing: nothing in the scratch has to start at zero; each call writes every entry it reads.
+ *   Set-up: the first call with B > 0 on a device looks the array's address up with
+ *   cudaGetSymbolAddress (once per device, then cached; SPECDEC_ERR_CUDA if that fails). Make
+ *   that first call on each device before any stream capture begins on it.
+ *   Concurrency: all calls on a device share the one array. Two calls that overlap in time (on
+ *   different streams, or from host threads whose calls are not stream-ordered) race on it, and
+ *   the outputs and counters of both are then undefined. Queue such calls on one stream, or use
+ *   specdec_verify with one workspace per stream.
+ */
+#define SPECDEC_NOALLOC_MAX_REQUESTS 16384
+specdec_status_t specdec_verify_noalloc(
+    const void* target_logits, specdec_dtype_t logits_dtype,
+    const int32_t* draft_ids,
+    const float* draft_probs,
+    const uint8_t* has_q,
+    const int32_t* cu_num_draft,
+    int32_t B, int32_t V, int32_t max_k,
+    const int32_t* bitmask,
+    const float* temperature,
+    const float* uniforms,
+    const float* exp_noise,
+    int32_t* out_tokens,
+    int32_t* out_num_accepted,
+    unsigned long long* counters,
+    uint32_t* status,
+    float* diag_accept_prob,
+    float* diag_row_stats,
+    void* stream);
+
+/*
  * specdec_wait -- block the calling host thread until all work queued on `stream` has
  * finished, or until timeout_ms milliseconds have passed (polling; timeout_ms < 0 waits
  * without limit). Returns SPECDEC_OK, SPECDEC_ERR_TIMEOUT, or SPECDEC_ERR_CUDA when the

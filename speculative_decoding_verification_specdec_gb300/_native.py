@@ -27,8 +27,9 @@ ST_K_TOO_LARGE = 8
 ST_BAD_OFFSETS = 16
 ST_DEVICE_TIMEOUT = 32
 
-EXPORTED = ("specdec_verify", "specdec_wait", "specdec_status_string", "specdec_launch_config",
-            "specdec_workspace_size")
+EXPORTED = ("specdec_verify", "specdec_verify_noalloc", "specdec_wait", "specdec_status_string",
+            "specdec_launch_config", "specdec_workspace_size")
+NOALLOC_MAX_REQUESTS = 16384            # SPECDEC_NOALLOC_MAX_REQUESTS
 
 _lib = None
 
@@ -51,6 +52,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specdec_verify.restype = ctypes.c_int
     lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.specdec_verify_noalloc.restype = ctypes.c_int
+    lib.specdec_verify_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
+                                           vp, vp, vp, vp, vp, vp, vp]
     lib.specdec_workspace_size.restype = ctypes.c_size_t
     lib.specdec_workspace_size.argtypes = [i32, i32]
     lib.specdec_wait.restype = ctypes.c_int
@@ -87,13 +91,7 @@ def _p(t) -> Optional[int]:
     return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
 
 
-def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
-                   bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
-                   status=None, diag_accept_prob=None, diag_row_stats=None, workspace=None, stream=None,
-                   logits_dtype=None) -> None:
-    """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
-    (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
-    non-zero status."""
+def _marshal(target_logits, logits_dtype, stream, tensors):
     import torch
 
     if logits_dtype is None:
@@ -103,12 +101,7 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
             logits_dtype = SPECDEC_F32
         else:
             raise SpecdecError(SPECDEC_ERR_UNSUPPORTED, f"logits dtype {target_logits.dtype}")
-    for name, t in (("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
-                    ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
-                    ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
-                    ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
-                    ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
-                    ("workspace", workspace)):
+    for name, t in tensors:
         if t is not None and hasattr(t, "is_cuda"):
             if not t.is_cuda:
                 raise ValueError(f"{name} must be a CUDA tensor")
@@ -118,13 +111,50 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
         stream = torch.cuda.current_stream().cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
+    return int(logits_dtype), stream
+
+
+def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
+                   bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
+                   status=None, diag_accept_prob=None, diag_row_stats=None, workspace=None, stream=None,
+                   logits_dtype=None) -> None:
+    """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
+    (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
+    non-zero status."""
+    dt, stream = _marshal(target_logits, logits_dtype, stream, (
+        ("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
+        ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
+        ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
+        ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
+        ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
+        ("workspace", workspace)))
     rc = load().specdec_verify(
-        _p(target_logits), int(logits_dtype), _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
+        _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
         int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
         _p(diag_row_stats), _p(workspace), 0 if workspace is None else _nbytes(workspace), stream)
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_verify")
+
+
+def specdec_verify_noalloc(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int,
+                           max_k: int, bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted,
+                           counters, status=None, diag_accept_prob=None, diag_row_stats=None, stream=None,
+                           logits_dtype=None) -> None:
+    """specdec_verify with the library's own schedule scratch (no workspace argument)."""
+    dt, stream = _marshal(target_logits, logits_dtype, stream, (
+        ("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
+        ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
+        ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
+        ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
+        ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats)))
+    rc = load().specdec_verify_noalloc(
+        _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
+        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
+        _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
+        _p(diag_row_stats), stream)
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_verify_noalloc")
 
 
 def _nbytes(t) -> int:

@@ -2100,6 +2100,36 @@ specdec_status_t launch_schedule(const Args& args, int32_t* order, uint8_t* keys
     return SPECDEC_OK;
 }
 
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+// Schedule scratch owned by the library, for specdec_verify_noalloc: the request order and cost
+// keys of up to SPECDEC_NOALLOC_MAX_REQUESTS requests (80 KiB per device), laid out as in a
+// caller workspace. Shared by every specdec_verify_noalloc call on a device.
+constexpr size_t kNoallocScratchBytes = ((size_t)SPECDEC_NOALLOC_MAX_REQUESTS * 4 + 15) / 16 * 16 +
+                                        ((size_t)SPECDEC_NOALLOC_MAX_REQUESTS + 15) / 16 * 16;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on device `dev`, looked up once per device and cached.
+void* noalloc_scratch(int dev)
+{
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 }  // namespace
 
 extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
@@ -2194,6 +2224,31 @@ extern "C" specdec_status_t specdec_verify(
     }
     const bool dep = a.order != nullptr;
     return logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, B, st, dep) : launch<uint16_t>(a, shape, B, st, dep);
+}
+
+extern "C" specdec_status_t specdec_verify_noalloc(
+    const void* target_logits, specdec_dtype_t logits_dtype, const int32_t* draft_ids,
+    const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
+    int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
+    const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
+    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* stream)
+{
+    static_assert(kNoallocScratchBytes >= sizeof(int32_t) * SPECDEC_NOALLOC_MAX_REQUESTS + SPECDEC_NOALLOC_MAX_REQUESTS,
+                  "scratch holds the order and the keys");
+    if (B > SPECDEC_NOALLOC_MAX_REQUESTS) return SPECDEC_ERR_UNSUPPORTED;     // before any CUDA call
+    void* scratch = nullptr;
+    if (B > 0) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+            (void)cudaGetLastError();
+            return SPECDEC_ERR_CUDA;
+        }
+        scratch = noalloc_scratch(dev);
+        if (scratch == nullptr) return SPECDEC_ERR_CUDA;
+    }
+    return specdec_verify(target_logits, logits_dtype, draft_ids, draft_probs, has_q, cu_num_draft, B, V, max_k,
+                          bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters, status,
+                          diag_accept_prob, diag_row_stats, scratch, scratch ? kNoallocScratchBytes : 0, stream);
 }
 
 extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)
