@@ -818,6 +818,12 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     }
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
@@ -900,17 +906,16 @@ __device__ __forceinline__ float tree_sum(const float* v)
     return t[0];
 }
 
-// Greedy fold of N values whose ids are ids[i] (increasing in i): max, lowest id on ties.
+// Greedy fold of N values with ids ids[i] (in any order): max, lowest id on ties.
 template <int N>
 __device__ __forceinline__ void argmax_batch(Part& p, const float* z, const int* ids)
 {
     const float bm = tree_max<N>(z);
-    if (bm > p.best) {                         // strict: an equal earlier best keeps its lower id
+    if (bm > -INFINITY && bm >= p.best) {
         int id = INT_MAX;
 #pragma unroll
-        for (int i = N - 1; i >= 0; --i) id = (z[i] == bm) ? ids[i] : id;
-        p.best = bm;
-        p.idx = id;
+        for (int i = 0; i < N; ++i) id = (z[i] == bm) ? min(id, ids[i]) : id;
+        if (bm > p.best || id < p.idx) { p.best = bm; p.idx = id; }
     }
 }
 
@@ -932,7 +937,8 @@ __device__ __forceinline__ void softmax_batch(Part& p, float& mc, const float* z
     p.S += tree_sum<N>(e);
 }
 
-// Draw fold of N candidates: w from p (and q), score w / E; -1 marks "no candidate".
+// Draw fold of N candidates with ids ids[i] (in any order): w from p (and q), score w / E;
+// -1 marks "no candidate".
 template <int N>
 __device__ __forceinline__ void draw_batch(Part& p, const float* z, const float* E, const float* qv, const int* ids,
                                            int code, int x, float c, float MC, float invS)
@@ -951,12 +957,11 @@ __device__ __forceinline__ void draw_batch(Part& p, const float* z, const float*
     }
     p.flag |= any;
     const float bm = tree_max<N>(sc);
-    if (bm > 0.f && bm > p.best) {
+    if (bm > 0.f && bm >= p.best) {            // ids in any order: lowest id on ties
         int id = INT_MAX;
 #pragma unroll
-        for (int i = N - 1; i >= 0; --i) id = (sc[i] == bm) ? ids[i] : id;
-        p.best = bm;
-        p.idx = id;
+        for (int i = 0; i < N; ++i) id = (sc[i] == bm) ? min(id, ids[i]) : id;
+        if (bm > p.best || id < p.idx) { p.best = bm; p.idx = id; }
     }
 }
 
@@ -1217,7 +1222,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
-        if (rs.skip == 0 && !request_is_sparse(a, rs.row0, lane)) {
+        const bool sp = rs.skip == 0 && request_is_sparse(a, rs.row0, lane);
+        if (sp && lane == 0) {
+            // sparse request: the consumers read every row's mask words first; start them into L2
+            const int wlo = lo >> 5, whi = (hi + 31) >> 5;
+            for (int j = 0; j <= rs.k; ++j)
+                prefetch_l2(a.bitmask + (rs.row0 + j) * (int64_t)a.W + wlo, (uint32_t)(whi - wlo) * 4u);
+        }
+        if (rs.skip == 0 && !sp) {
             Producer<ET> pr(a, sh, ring, lane, lo, hi);
             uint32_t dec_round = 0;
             int issued_next = 0;
@@ -1317,7 +1329,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // with the other CTAs of the request: consumer thread i stores this CTA's partial into
         // CTA i's slot and arrives on CTA i's barrier; every CTA folds the NC partials in rank
         // order, so all of them hold bit-identical results.
-        auto reduce = [&](Part p) -> Part {
+        auto reduce_cta = [&](Part p) -> Part {
             p = warp_reduce(p, c);
             if (lane == 0) sh.wpart[par][cw] = p;
             consumer_sync();
@@ -1325,6 +1337,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], c);
             par ^= 1;
+            return r;
+        };
+        auto reduce = [&](Part p) -> Part {
+            const Part r = reduce_cta(p);
             if (NC == 1) return r;
             const int slot = (int)(xround & 1u);
             if (ct < NC) {
@@ -1525,9 +1541,150 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         if (rs.skip == 0) {
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
-            for (int j = 0; j <= k; ++j) {
+
+            // ---- decision on row j from its reduced partial r (identical in every consumer thread
+            // of every CTA of the request); returns the next code (a draw kind, next row, done)
+            auto decide = [&](int j, const Part& r, bool& stop, float& MC, float& S_mc) -> int {
                 const int64_t t = rs.row0 + j;
                 const int64_t d = (int64_t)rs.d0 + j;
+                const bool bonus = (j == k);
+                const int x = bonus ? -1 : sh.xs[j];
+                (void)d;
+                int code = kDecDone;
+                stop = true;
+                MC = 0.f;
+                S_mc = 1.f;
+                if (greedy) {
+                    if (r.idx == INT_MAX) {
+                        st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                        if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
+                        acc_len = j; emitted = -1;
+                    } else {
+                        if (writer && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
+                        if (bonus) {
+                            emitted = r.idx;
+                        } else {
+                            const bool accept = (j < g) && (x == r.idx);
+                            if (writer && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
+                            if (accept) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                            else { acc_len = j; emitted = r.idx; }
+                        }
+                    }
+                } else if (r.m == -INFINITY) {
+                    st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
+                    acc_len = j; emitted = -1;
+                } else {
+                    MC = r.m * c;
+                    // S against MC = round(M*c), the reference the draw terms use
+                    S_mc = fmaf(r.S, fmaf(r.m, c, -MC) * 0.69314718f, r.S);
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
+                    code = kDecDrawP;
+                    if (!bonus) {
+                        float alpha = 0.f;
+                        if (j < g) {
+                            const float px = (r.zx > -INFINITY) ? ex2_scaled(r.zx, c, MC) / S_mc : 0.f;
+                            if (qmode) {
+                                const float qx = sh.qxs[j];
+                                alpha = (px <= 0.f) ? 0.f : (qx <= px ? 1.f : px / qx);
+                            } else {
+                                alpha = px;
+                            }
+                        }
+                        if (writer && a.diag_alpha) a.diag_alpha[d] = alpha;
+                        if (sh.us[j] < alpha) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
+                        else code = qmode ? kDecDrawQ : kDecDrawOneHot;
+                    }
+                }
+                return code;
+            };
+
+            // ---- a9/a10: draw pass(es) over the stop / bonus row j
+            auto draw_row = [&](int j, int code, float MC, float S_mc) {
+                const int64_t t = rs.row0 + j;
+                const int64_t d = (int64_t)rs.d0 + j;
+                const int x = (j == k) ? -1 : sh.xs[j];
+                while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
+                    SPECDEC_STAMP(5);
+                    const float invS = 1.f / S_mc;
+                    Part dp = part_identity();
+                    if (!sparse) {
+                        const bool wq = (code == kDecDrawQ);
+                        const int ids = G::draw_ids(wq);
+                        const int nd = (hi - lo + ids - 1) / ids;
+                        for (int ch = 0; ch < nd; ++ch) {
+                            const int s = wait_full();
+                            const unsigned char* stg = ring + (size_t)s * kStageBytes;
+                            const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::dmask_off(wq));
+                            const float* se = reinterpret_cast<const float*>(stg + G::noise_off(wq));
+                            const float* sq = reinterpret_cast<const float*>(stg + G::q_off(wq));
+                            const int i0 = lo + ch * ids;
+                            const int n = min(ids, hi - i0);
+                            const int nvec = (n + VE - 1) / VE;
+                            constexpr int NB = (VE == 4) ? 2 : 1;
+                            const int vxd = (code == kDecDrawOneHot && x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
+                            for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
+                                float z[NB * VE], ev[NB * VE], qv[NB * VE];
+                                int xslot = -1;
+#pragma unroll
+                                for (int u = 0; u < NB; ++u) {
+                                    const int v = vb + u * kConsumers;
+                                    const int e0 = v * VE;
+                                    if (v < nvec) {
+                                        Elem<ET>::load(stg, v, z + u * VE);
+                                        const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
+                                        if (bits != (1u << VE) - 1u) {
+#pragma unroll
+                                            for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
+                                        }
+#pragma unroll
+                                        for (int h = 0; h < VE / 4; ++h) {
+                                            const float4 f = reinterpret_cast<const float4*>(se + e0)[h];
+                                            ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
+                                            if (wq) {
+                                                const float4 g4 = reinterpret_cast<const float4*>(sq + e0)[h];
+                                                qv[u * VE + 4 * h] = g4.x; qv[u * VE + 4 * h + 1] = g4.y; qv[u * VE + 4 * h + 2] = g4.z; qv[u * VE + 4 * h + 3] = g4.w;
+                                            } else {
+                                                qv[u * VE + 4 * h] = qv[u * VE + 4 * h + 1] = qv[u * VE + 4 * h + 2] = qv[u * VE + 4 * h + 3] = 0.f;
+                                            }
+                                        }
+                                        if (v == vxd) xslot = u * VE + (x - i0) % VE;
+                                    } else {
+#pragma unroll
+                                        for (int e = 0; e < VE; ++e) { z[u * VE + e] = -INFINITY; ev[u * VE + e] = 1.f; qv[u * VE + e] = 0.f; }
+                                    }
+                                }
+                                draw_lazy<NB, VE>(dp, z, ev, qv, i0 + vb * VE, kConsumers * VE, xslot, code, c, MC, invS);
+                            }
+                            release(s);
+                        }
+                    } else {
+                        if (listed_row == j) {
+                            sparse_draw(t, d, x, listed_n, code, dp, MC, invS);
+                        } else {
+                            for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
+                                const int w1 = min(whi, w0 + kSegWords);
+                                const int n = build_list(t, w0, w1);
+                                if (n >= 0) {
+                                    sparse_draw(t, d, x, n, code, dp, MC, invS);
+                                } else {
+                                    for (int s0 = w0; s0 < w1; s0 += G::kSafeWords)
+                                        sparse_draw(t, d, x, build_list(t, s0, min(w1, s0 + G::kSafeWords)), code, dp, MC, invS);
+                                }
+                            }
+                        }
+                    }
+                    SPECDEC_STAMP(6);
+                    const Part dr = reduce(dp);
+                    if (code == kDecDrawQ && !dr.flag) { code = kDecDrawP; post(code); continue; }   // empty residual
+                    emitted = dr.idx == INT_MAX ? -1 : dr.idx;
+                    post(kDecDone);
+                    break;
+                }
+            };
+
+            for (int j = 0; j <= k; ++j) {
+                const int64_t t = rs.row0 + j;
                 const bool bonus = (j == k);
                 const int x = bonus ? -1 : sh.xs[j];
                 Part p = part_identity();
@@ -1615,137 +1772,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 const Part r = reduce(p);
                 SPECDEC_STAMP(4);
 
-                // ---- decision (identical in every consumer thread of every CTA of the request)
-                int code = kDecDone;
-                bool stop = true;
-                float MC = 0.f, S_mc = 1.f;
-                if (greedy) {
-                    if (r.idx == INT_MAX) {
-                        st |= SPECDEC_ST_EMPTY_MASK_ROW;
-                        if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = NAN; }
-                        acc_len = j; emitted = -1;
-                    } else {
-                        if (writer && a.diag_row) { a.diag_row[2 * t] = r.best; a.diag_row[2 * t + 1] = NAN; }
-                        if (bonus) {
-                            emitted = r.idx;
-                        } else {
-                            const bool accept = (j < g) && (x == r.idx);
-                            if (writer && a.diag_alpha) a.diag_alpha[d] = accept ? 1.f : 0.f;
-                            if (accept) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
-                            else { acc_len = j; emitted = r.idx; }
-                        }
-                    }
-                } else if (r.m == -INFINITY) {
-                    st |= SPECDEC_ST_EMPTY_MASK_ROW;
-                    if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
-                    acc_len = j; emitted = -1;
-                } else {
-                    MC = r.m * c;
-                    // S against MC = round(M*c), the reference the draw terms use
-                    S_mc = fmaf(r.S, fmaf(r.m, c, -MC) * 0.69314718f, r.S);
-                    if (writer && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
-                    code = kDecDrawP;
-                    if (!bonus) {
-                        float alpha = 0.f;
-                        if (j < g) {
-                            const float px = (r.zx > -INFINITY) ? ex2_scaled(r.zx, c, MC) / S_mc : 0.f;
-                            if (qmode) {
-                                const float qx = sh.qxs[j];
-                                alpha = (px <= 0.f) ? 0.f : (qx <= px ? 1.f : px / qx);
-                            } else {
-                                alpha = px;
-                            }
-                        }
-                        if (writer && a.diag_alpha) a.diag_alpha[d] = alpha;
-                        if (sh.us[j] < alpha) { if (writer) a.out_tokens[t] = x; stop = false; code = kDecNextRow; }
-                        else code = qmode ? kDecDrawQ : kDecDrawOneHot;
-                    }
-                }
+                bool stop;
+                float MC, S_mc;
+                const int code = decide(j, r, stop, MC, S_mc);
                 post(code);
                 if (!stop) continue;
 
                 // drain the chunks of row j+1 the producer queued before this decision
                 if (!sparse && j < k)
                     for (int ch = 0; ch < spec; ++ch) release(wait_full());
-
-                // ---- a9/a10: draw pass(es) over the stop / bonus row
-                while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
-                    SPECDEC_STAMP(5);
-                    const float invS = 1.f / S_mc;
-                    Part dp = part_identity();
-                    if (!sparse) {
-                        const bool wq = (code == kDecDrawQ);
-                        const int ids = G::draw_ids(wq);
-                        const int nd = (hi - lo + ids - 1) / ids;
-                        for (int ch = 0; ch < nd; ++ch) {
-                            const int s = wait_full();
-                            const unsigned char* stg = ring + (size_t)s * kStageBytes;
-                            const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::dmask_off(wq));
-                            const float* se = reinterpret_cast<const float*>(stg + G::noise_off(wq));
-                            const float* sq = reinterpret_cast<const float*>(stg + G::q_off(wq));
-                            const int i0 = lo + ch * ids;
-                            const int n = min(ids, hi - i0);
-                            const int nvec = (n + VE - 1) / VE;
-                            constexpr int NB = (VE == 4) ? 2 : 1;
-                            const int vxd = (code == kDecDrawOneHot && x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
-                            for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
-                                float z[NB * VE], ev[NB * VE], qv[NB * VE];
-                                int xslot = -1;
-#pragma unroll
-                                for (int u = 0; u < NB; ++u) {
-                                    const int v = vb + u * kConsumers;
-                                    const int e0 = v * VE;
-                                    if (v < nvec) {
-                                        Elem<ET>::load(stg, v, z + u * VE);
-                                        const uint32_t bits = vec_bits<VE>(sm, has_mask, v);
-                                        if (bits != (1u << VE) - 1u) {
-#pragma unroll
-                                            for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
-                                        }
-#pragma unroll
-                                        for (int h = 0; h < VE / 4; ++h) {
-                                            const float4 f = reinterpret_cast<const float4*>(se + e0)[h];
-                                            ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
-                                            if (wq) {
-                                                const float4 g4 = reinterpret_cast<const float4*>(sq + e0)[h];
-                                                qv[u * VE + 4 * h] = g4.x; qv[u * VE + 4 * h + 1] = g4.y; qv[u * VE + 4 * h + 2] = g4.z; qv[u * VE + 4 * h + 3] = g4.w;
-                                            } else {
-                                                qv[u * VE + 4 * h] = qv[u * VE + 4 * h + 1] = qv[u * VE + 4 * h + 2] = qv[u * VE + 4 * h + 3] = 0.f;
-                                            }
-                                        }
-                                        if (v == vxd) xslot = u * VE + (x - i0) % VE;
-                                    } else {
-#pragma unroll
-                                        for (int e = 0; e < VE; ++e) { z[u * VE + e] = -INFINITY; ev[u * VE + e] = 1.f; qv[u * VE + e] = 0.f; }
-                                    }
-                                }
-                                draw_lazy<NB, VE>(dp, z, ev, qv, i0 + vb * VE, kConsumers * VE, xslot, code, c, MC, invS);
-                            }
-                            release(s);
-                        }
-                    } else {
-                        if (listed_row == j) {
-                            sparse_draw(t, d, x, listed_n, code, dp, MC, invS);
-                        } else {
-                            for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
-                                const int w1 = min(whi, w0 + kSegWords);
-                                const int n = build_list(t, w0, w1);
-                                if (n >= 0) {
-                                    sparse_draw(t, d, x, n, code, dp, MC, invS);
-                                } else {
-                                    for (int s0 = w0; s0 < w1; s0 += G::kSafeWords)
-                                        sparse_draw(t, d, x, build_list(t, s0, min(w1, s0 + G::kSafeWords)), code, dp, MC, invS);
-                                }
-                            }
-                        }
-                    }
-                    SPECDEC_STAMP(6);
-                    const Part dr = reduce(dp);
-                    if (code == kDecDrawQ && !dr.flag) { code = kDecDrawP; post(code); continue; }   // empty residual
-                    emitted = dr.idx == INT_MAX ? -1 : dr.idx;
-                    post(kDecDone);
-                    break;
-                }
+                draw_row(j, code, MC, S_mc);
                 acc_len = j;
                 break;
             }
@@ -1802,23 +1838,27 @@ constexpr int kSchedKeys = 256;
 template <typename ET>
 __device__ __forceinline__ int request_cost_key(const Args& a, int b)
 {
+    // the loads that depend on nothing are issued together; only the mask words wait for cu[b]
+    const float T = __ldg(a.temperature + b);
+    const bool hq = a.has_q == nullptr || __ldg(a.has_q + b) != 0;
     const ReqShape rs = request_shape(a, b);
     if (rs.skip != 0) return 0;
-    const float T = a.temperature[b];
     const bool tvalid = (T == 0.f) || (T >= FLT_MIN && T <= FLT_MAX);
     const bool greedy = !(T > 0.f) || !tvalid;
-    const bool qmode = a.q != nullptr && (a.has_q == nullptr || a.has_q[b] != 0);
+    const bool qmode = a.q != nullptr && hq;
     bool sparse = false;
     if (a.bitmask != nullptr && a.bulk) {
         // the verify kernel's test, one thread instead of one warp: fewer than half of the
         // first min(W, 32) mask words' bits set (rows are 16-byte aligned on this path)
+        // (W % 4 == 0 on this path; the eight 16-byte loads are all in flight at once)
         const int nw = min(a.W, 32);
         const uint4* m = reinterpret_cast<const uint4*>(a.bitmask + rs.row0 * (int64_t)a.W);
+        uint4 u[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u[i] = (4 * i < nw) ? __ldg(m + i) : make_uint4(0u, 0u, 0u, 0u);
         int ones = 0;
-        for (int i = 0; i < nw / 4; ++i) {
-            const uint4 u = __ldg(m + i);
-            ones += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
-        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ones += __popc(u[i].x) + __popc(u[i].y) + __popc(u[i].z) + __popc(u[i].w);
         sparse = 2 * ones < nw * 32;
     }
     constexpr float es = (float)sizeof(ET);
@@ -1828,12 +1868,16 @@ __device__ __forceinline__ int request_cost_key(const Args& a, int b)
     return min(kSchedKeys - 1, (int)(cost * 16.f + 0.5f));
 }
 
+constexpr int kSchedSmemKeys = 8192;               // batches up to this size keep their keys on chip
+
 struct SchedShared {
     int32_t cursor[kSchedKeys];                   // next output slot per key
     int32_t wcnt[kSchedWarps][kSchedKeys];        // requests per (warp, key) in the current tile
+    uint8_t keys[kSchedSmemKeys];
 };
 
-// order[B]: the permutation; keys[B]: one byte per request (scratch).
+// order[B]: the permutation; keys[B]: each request's cost key (read back here only when
+// B > kSchedSmemKeys; smaller batches keep a copy on chip).
 template <typename ET>
 __global__ void __launch_bounds__(kSchedThreads) specdec_schedule_kernel(const Args a, int32_t* order, uint8_t* keys)
 {
@@ -1841,14 +1885,20 @@ __global__ void __launch_bounds__(kSchedThreads) specdec_schedule_kernel(const A
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = a.B;
     allow_dependent_launch();          // the verify grid may start; it waits for this grid to finish
+    uint8_t* kp = B <= kSchedSmemKeys ? sh.keys : keys;
 
     for (int i = tid; i < kSchedKeys; i += kSchedThreads) sh.cursor[i] = 0;
     __syncthreads();
-    // pass 1: keys and their histogram
-    for (int b = tid; b < B; b += kSchedThreads) {
-        const int key = request_cost_key<ET>(a, b);
-        keys[b] = (uint8_t)key;
-        atomicAdd(&sh.cursor[key], 1);
+    // pass 1: keys and their histogram (one shared-memory atomic per distinct key in a warp)
+    for (int b0 = 0; b0 < B; b0 += kSchedThreads) {
+        const int b = b0 + tid;
+        const int key = b < B ? request_cost_key<ET>(a, b) : -1;
+        if (b < B) {
+            keys[b] = (uint8_t)key;                        // kept in the workspace for inspection
+            if (kp != keys) kp[b] = (uint8_t)key;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sh.cursor[key], __popc(peers));
     }
     __syncthreads();
     // exclusive prefix over keys in descending order: first slot of each key (warp 0, 8 keys a lane)
@@ -1873,7 +1923,7 @@ __global__ void __launch_bounds__(kSchedThreads) specdec_schedule_kernel(const A
         for (int i = tid; i < kSchedWarps * kSchedKeys; i += kSchedThreads) (&sh.wcnt[0][0])[i] = 0;
         __syncthreads();
         const int b = t0 + tid;
-        const int key = b < B ? (int)keys[b] : -1;
+        const int key = b < B ? (int)kp[b] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (key >= 0 && (peers & lt) == 0u) sh.wcnt[warp][key] = __popc(peers);
         __syncthreads();
@@ -1917,16 +1967,16 @@ int device_sms()
 }
 
 // CTAs per request for the streaming kernel. A request is a serial chain of row passes and
-// one CTA streams at about its fair share of HBM (~1/300 of it with two CTAs per SM), so small
-// batches split each row over a few CTAs to shorten the chains; from about one request per SM
-// on, one CTA per request is fastest (the per-row exchange of a cluster costs more than the
-// shorter chain gains). (Measured on GB300: B=64 -> 2 or 4, B >= 128 -> 1 were the fastest of
-// {1, 2, 4}.)
+// one CTA streams at about its fair share of HBM (~1/300 of it with two CTAs per SM), so a batch
+// far smaller than one wave of resident CTAs splits each row over as many CTAs as still fit in
+// that wave (3 or 4); otherwise one CTA per request (the per-row exchange of a cluster of two
+// costs about what the shorter chain gains). Measured on GB300: B=64 -> 3 or 4 (4 CTAs 24.6 us,
+// 2 CTAs 25.6, 1 CTA 28.7); B=128 -> 1 (78 us vs 83 with 2); B >= 256 -> 1.
 int stream_ctas_per_request(int32_t B, int sms)
 {
     const int b = B > 0 ? B : 1;
-    int G = (128 * sms / 152) / b;
-    if (G < 1) G = 1;
+    int G = (kResidentPerSM * sms) / b;
+    if (G < 3) G = 1;
     if (G > 4) G = 4;
     return G;
 }
