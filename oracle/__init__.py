@@ -49,7 +49,10 @@ class _Diag(ctypes.Structure):
         ("emit_top2", ctypes.c_void_p),
         ("emit_scores", ctypes.c_void_p),
         ("score_request", ctypes.c_int32),
+        ("telemetry", ctypes.c_void_p),
     ]
+
+TELEMETRY_SHAPE = (4, 33)   # rows: drafts, eligible, accepted by position; histogram of accepted
 
 
 _loaded = {}
@@ -80,7 +83,8 @@ def _ptr(a: Optional[np.ndarray]):
 
 class OracleResult(dict):
     """out_tokens [T], out_num_accepted [B], counters [4] (R, I, D, A), status [B],
-    alpha [N], row_m [T], row_S [T], emit_top1 [B], emit_top2 [B], emit_scores [V]."""
+    alpha [N], row_m [T], row_S [T], emit_top1 [B], emit_top2 [B], emit_scores [V],
+    telemetry [4, 33] (see specdec_ref.h)."""
 
     def __getattr__(self, k):
         try:
@@ -104,8 +108,9 @@ def verify(w, *, score_request: int = -1, counters: Optional[np.ndarray] = None,
     top1 = np.empty(B, dtype=np.float64)
     top2 = np.empty(B, dtype=np.float64)
     scores = np.empty(V, dtype=np.float64)
+    telemetry = np.zeros(TELEMETRY_SHAPE, dtype=np.uint64)
     diag = _Diag(alpha.ctypes.data, row_m.ctypes.data, row_S.ctypes.data, top1.ctypes.data,
-                 top2.ctypes.data, scores.ctypes.data, int(score_request))
+                 top2.ctypes.data, scores.ctypes.data, int(score_request), telemetry.ctypes.data)
     logits = np.ascontiguousarray(w.logits)
     dtype = 1 if w.logits_dtype == "bf16" else 0
     args = [np.ascontiguousarray(a) if a is not None else None for a in
@@ -119,4 +124,4 @@ def verify(w, *, score_request: int = -1, counters: Optional[np.ndarray] = None,
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return OracleResult(out_tokens=out_tokens, out_num_accepted=out_num, counters=ctr, status=status,
                         alpha=alpha, row_m=row_m, row_S=row_S, emit_top1=top1, emit_top2=top2,
-                        emit_scores=scores)
+                        emit_scores=scores, telemetry=telemetry)

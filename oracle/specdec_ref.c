@@ -295,6 +295,14 @@ static void verify_request(ref_call* c, int32_t b)
     c->counters[1] += (uint64_t)(k - g);    /* I: grammar-invalidated */
     c->counters[2] += (uint64_t)g;          /* D = R - I: eligible */
     c->counters[3] += (uint64_t)a;          /* A: accepted */
+    /* per-position telemetry (row layout in specdec_ref.h) */
+    if (c->diag && c->diag->telemetry) {
+        uint64_t* tm = c->diag->telemetry;
+        for (int32_t j = 0; j < k; ++j) tm[0 * 33 + j] += 1;
+        for (int32_t j = 0; j < g; ++j) tm[1 * 33 + j] += 1;
+        for (int32_t j = 0; j < a; ++j) tm[2 * 33 + j] += 1;
+        tm[3 * 33 + a] += 1;
+    }
     if (c->status) c->status[b] = st;
 }
 

@@ -60,6 +60,14 @@ typedef struct {
     double* emit_top2;    /* [B]   runner-up score of that race (0 when it had one candidate), else NaN */
     double* emit_scores;  /* [V]   all race scores of request score_request (0 where w_i = 0), else NaN */
     int32_t score_request;/*       request whose race scores fill emit_scores (-1: none) */
+    uint64_t* telemetry;  /* [4][33] ADDED to, or NULL: per position j, row 0 counts drafts
+                           * (j < k_b), row 1 grammar-eligible drafts (j < g_b), row 2 drafts
+                           * accepted through position j (j < a_b); row 3 [a] counts requests
+                           * that accepted exactly a drafts. Skipped requests are not counted.
+                           * ("vLLM tour part 2", section "Telemetry and tuning": per-position
+                           * draft / accepted counts and the acceptance histogram; "Speculative
+                           * decoding -- code walkthrough", section 7.2: the per-position count
+                           * is of drafts accepted all the way through that position.) */
 } specdec_ref_diag;
 
 /* Returns 0 on success, 1 on invalid arguments (nothing written). counters[4] =

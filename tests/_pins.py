@@ -5,6 +5,7 @@ deliberately broken copies of the oracle.
 """
 from __future__ import annotations
 
+import dataclasses
 import json
 import os
 
@@ -507,8 +508,55 @@ def check_residual_excludes_draft(lib_path=None, seed=61):
         assert n_checked > 50
 
 
+# ---------------------------------------------------------------------------------------------
+# per-position telemetry ("vLLM tour part 2", section "Telemetry and tuning"; "Speculative
+# decoding -- code walkthrough", section 7.2: a position counts drafts accepted all the way
+# through it)
+# ---------------------------------------------------------------------------------------------
+
+def _telemetry_expect(entry, k):
+    t = np.zeros((4, 33), dtype=np.uint64)
+    t[0, :k] = entry["drafts_by_position"]
+    t[1, :k] = entry["eligible_by_position"]
+    t[2, :k] = entry["accepted_through_position"]
+    for a, n in entry["accepted_length_histogram"].items():
+        t[3, int(a)] = n
+    return t
+
+
+def check_telemetry(lib_path=None, seed=71):
+    kw = {} if lib_path is None else {"lib_path": lib_path}
+    g = _golden("telemetry_worked_example.json")
+    r = oracle.verify(_greedy_counter_batch(40, 120, 40), **kw)
+    assert np.array_equal(r.telemetry, _telemetry_expect(g["worked_example"], 5)), r.telemetry[:, :6]
+    r3 = oracle.verify(_greedy_counter_batch(0, 60, 40, k=3, seed=3), **kw)
+    assert np.array_equal(r3.telemetry, _telemetry_expect(g["mean_acceptance_length_example"], 3)), r3.telemetry[:, :4]
+    # identities with the counters on mixed batches (every mode, masks, forced-invalid drafts,
+    # a request with k > max_k that is skipped)
+    for s in range(3):
+        w = W.make_batch(seed + s, B=60, V=300, k=(0, 7), logit_sigma=2.0, temperature="half_greedy(0.5,1.2)",
+                         q_mode="half", draft_sigma=0.3, mf_argmax_frac=0.5, mask="half", mask_density=0.2,
+                         mask_run_len=8, forced_invalid_frac=0.2)
+        if s == 2:
+            w = dataclasses.replace(w, max_k=int(w.k.max()) - 1)       # the longest requests are skipped
+        r = oracle.verify(w, **kw)
+        tm = r.telemetry.astype(np.int64)
+        R, I, D, A = (int(c) for c in r.counters)
+        assert tm[0].sum() == R and tm[1].sum() == D and tm[2].sum() == A, (tm.sum(axis=1), r.counters)
+        done = (r.status & 24) == 0
+        assert tm[3].sum() == int(done.sum())
+        assert int((np.arange(33) * tm[3]).sum()) == A
+        assert (tm[2] <= tm[1]).all() and (tm[1] <= tm[0]).all()
+        assert (np.diff(tm[:3], axis=1) <= 0).all()                    # non-increasing by position
+        kk = w.k[done]
+        assert tm[0].tolist() == [int((kk > j).sum()) for j in range(33)]
+        if s == 2:
+            assert not done.all()
+
+
 ALL_PINS = [
     check_worked_counter_example,
+    check_telemetry,
     check_strict_accept_comparison,
     check_edge_cases,
     check_residual_excludes_draft,

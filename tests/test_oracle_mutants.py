@@ -38,6 +38,11 @@ MUTANTS = {
     "softmax_not_normalised": ("for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;", "(void)0;"),
     "empty_row_not_flagged": ("if (live == 0) {", "if (live < 0) {"),
     "model_free_alpha_is_one": ("if (!qmode) return px;", "if (!qmode) return 1.0;"),
+    "telemetry_accepted_through_stop_row": ("for (int32_t j = 0; j < a; ++j) tm[2 * 33 + j] += 1;",
+                                            "for (int32_t j = 0; j <= a; ++j) tm[2 * 33 + j] += 1;"),
+    "telemetry_eligible_counts_every_draft": ("for (int32_t j = 0; j < g; ++j) tm[1 * 33 + j] += 1;",
+                                              "for (int32_t j = 0; j < k; ++j) tm[1 * 33 + j] += 1;"),
+    "telemetry_histogram_of_k": ("tm[3 * 33 + a] += 1;", "tm[3 * 33 + k] += 1;"),
     "no_stop_at_rejection": ("        a = j;\n        emitted = exponential_race(c, t, b);\n        break;",
                              "        a = j;\n        emitted = exponential_race(c, t, b);\n        c->out_tokens[t] = emitted;\n        continue;"),
 }
@@ -59,6 +64,7 @@ def _run_pins(lib):
     failures = []
     checks = [
         ("worked_counter_example", lambda: _pins.check_worked_counter_example(lib)),
+        ("telemetry", lambda: _pins.check_telemetry(lib)),
         ("strict_accept_comparison", lambda: _pins.check_strict_accept_comparison(lib)),
         ("edge_cases", lambda: _pins.check_edge_cases(lib)),
         ("residual_excludes_draft", lambda: _pins.check_residual_excludes_draft(lib)),

@@ -40,3 +40,7 @@ def test_edge_cases():
 
 def test_residual_excludes_draft():
     _pins.check_residual_excludes_draft()
+
+
+def test_telemetry_by_position():
+    _pins.check_telemetry()
