@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="verify only the first N requests of the workload (profiler captures); 0 = all")
     return ap.parse_args()
 
 
@@ -82,9 +84,13 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload_for(cfg: int, rank: int) -> W.Workload:
-    # rank 0 verifies the recipe's own seeded batch; other ranks verify independent batches
-    return W.config(cfg, seed=cfg + 1000 * rank)
+def workload_for(cfg: int, rank: int, requests: int = 0) -> W.Workload:
+    # rank 0 verifies the recipe's own seeded batch; other ranks verify independent batches;
+    # requests > 0 keeps the first `requests` requests (smaller cases for profiler captures)
+    w = W.config(cfg, seed=cfg + 1000 * rank)
+    if 0 < requests < w.B:
+        w = w.subset(range(requests), name=f"{w.name}_first{requests}")
+    return w
 
 
 # ------------------------------------------------------------------------------------------
@@ -253,7 +259,7 @@ def run_reference(args, world, rank):
         return
     import oracle
 
-    w = workload_for(args.config, 0)
+    w = workload_for(args.config, 0, args.requests)
     oracle.load()
     budget_total = 150.0
     per_step = max(0.05, min(5.0, budget_total / max(1, args.steps + args.warmup)))
@@ -331,7 +337,7 @@ def main():
         pg.barrier()
     _native.load()
 
-    w = workload_for(args.config, rank)
+    w = workload_for(args.config, rank, args.requests)
     host = device.host_tensors(w)
     dev_in = device.device_tensors(w, dev, host)
     out = device.alloc_outputs(w, dev, diag=False)
@@ -446,11 +452,14 @@ def main():
                        "per_rank": "independent batch per rank (requests shard with no exchange)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel": "specdec_verify_stream_kernel",
+                         "time": ("whole step: request-schedule kernel + verify kernel"
+                                  if shape["kernels_with_workspace"] == 2 else "verify kernel"),
                          "algorithmic_bytes_per_launch": ab,
                          "whole_row_gbs": achieved_rows, "whole_row_frac": achieved_rows / peak},
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * shape["kernels_with_workspace"],
             "clocks": clocks,
             "kernel_ms": {"median": statistics.median(kernel_ms), "min": min(kernel_ms), "max": max(kernel_ms)},
             "counters_per_step": [int(c) // args.steps for c in ctr],

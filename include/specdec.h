@@ -209,13 +209,15 @@ const char* specdec_status_string(specdec_status_t status);
  * specdec_launch_config -- the launch shape specdec_verify uses for a batch of B requests of
  * vocabulary size V (host arithmetic; the SM count comes from the current device, 152 when none
  * is visible): CTAs per request (a thread-block cluster that splits every vocabulary row into
- * contiguous slices), threads per CTA, dynamic shared memory per CTA in bytes, and vocabulary ids
- * per slice. Any output pointer may be NULL. Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED
- * like specdec_verify.
+ * contiguous slices), threads per CTA, dynamic shared memory per CTA in bytes, vocabulary ids
+ * per slice, and the number of kernels one call launches when given a workspace (2 when the
+ * request schedule runs, else 1; without a workspace it is always 1). Any output pointer may be
+ * NULL. Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED like specdec_verify.
  */
 specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                        int32_t* ctas_per_request, int32_t* threads_per_cta,
-                                       int32_t* smem_bytes, int32_t* slice_ids);
+                                       int32_t* smem_bytes, int32_t* slice_ids,
+                                       int32_t* kernels_with_workspace);
 
 #ifdef __cplusplus
 }

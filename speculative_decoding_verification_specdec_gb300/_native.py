@@ -62,7 +62,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specdec_status_string.restype = ctypes.c_char_p
     lib.specdec_status_string.argtypes = [ctypes.c_int]
     lib.specdec_launch_config.restype = ctypes.c_int
-    lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp]
+    lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -72,13 +72,13 @@ def status_string(status: int) -> str:
 
 
 def launch_config(V: int, dtype: int, B: int = 1024) -> dict:
-    c, t, s, w = (ctypes.c_int32() for _ in range(4))
+    c, t, s, w, k = (ctypes.c_int32() for _ in range(5))
     rc = load().specdec_launch_config(int(B), int(V), int(dtype), ctypes.byref(c), ctypes.byref(t),
-                                      ctypes.byref(s), ctypes.byref(w))
+                                      ctypes.byref(s), ctypes.byref(w), ctypes.byref(k))
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_launch_config")
     return {"ctas_per_request": c.value, "threads_per_cta": t.value, "smem_bytes": s.value,
-            "slice_ids": w.value}
+            "slice_ids": w.value, "kernels_with_workspace": k.value}
 
 
 def workspace_size(B: int, V: int) -> int:

@@ -2119,6 +2119,15 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
 
+// Whether a call with a workspace runs the schedule kernel first: only when the grid does not fit
+// in one wave of resident CTAs (with everything resident at once the order changes nothing).
+// SPECDEC_SCHEDULE=1 / 0 forces it on / off (tests and comparison runs).
+bool schedule_wanted(int32_t B, int G)
+{
+    if (const char* env = std::getenv("SPECDEC_SCHEDULE")) return std::strcmp(env, "0") != 0;
+    return (long long)B * G > (long long)kResidentPerSM * device_sms();
+}
+
 // The schedule's scratch inside a caller workspace: order int32[B], then keys uint8[B].
 struct ScheduleLayout {
     size_t order_off, keys_off, bytes;
@@ -2184,7 +2193,8 @@ void* noalloc_scratch(int dev)
 
 extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                                   int32_t* ctas_per_request, int32_t* threads_per_cta,
-                                                  int32_t* smem_bytes, int32_t* slice_ids)
+                                                  int32_t* smem_bytes, int32_t* slice_ids,
+                                                  int32_t* kernels_with_workspace)
 {
     LaunchShape s;
     const specdec_status_t rc = shape_for(V, logits_dtype, B, &s);
@@ -2193,6 +2203,7 @@ extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_
     if (threads_per_cta) *threads_per_cta = s.threads;
     if (smem_bytes) *smem_bytes = s.smem;
     if (slice_ids) *slice_ids = s.slice_units * kUnit;
+    if (kernels_with_workspace) *kernels_with_workspace = (B > 0 && schedule_wanted(B, s.G)) ? 2 : 1;
     return SPECDEC_OK;
 }
 
@@ -2256,13 +2267,8 @@ extern "C" specdec_status_t specdec_verify(
         const ScheduleLayout L = schedule_layout(B);
         if (!aligned(workspace, 16) || workspace_bytes < L.bytes) return SPECDEC_ERR_INVALID_ARG;
     }
-    // heaviest requests first, when the grid does not fit in one wave of resident CTAs (with
-    // everything resident at once the order changes nothing): the schedule kernel writes the
-    // order the verify kernel reads
-    bool schedule = workspace != nullptr && (long long)B * shape.G > (long long)kResidentPerSM * device_sms();
-    if (const char* env = std::getenv("SPECDEC_SCHEDULE"))        // tests and comparison runs
-        schedule = workspace != nullptr && std::strcmp(env, "0") != 0;
-    if (schedule) {
+    // heaviest requests first: the schedule kernel writes the order the verify kernel reads
+    if (workspace != nullptr && schedule_wanted(B, shape.G)) {
         const ScheduleLayout L = schedule_layout(B);
         unsigned char* ws = static_cast<unsigned char*>(workspace);
         int32_t* order = reinterpret_cast<int32_t*>(ws + L.order_off);

@@ -61,6 +61,20 @@ def test_launch_config_covers_the_row(lib, V, dtype, kernel, B, monkeypatch):
             assert G == 1                            # enough requests to fill the GPU
 
 
+def test_launch_config_reports_the_schedule(lib, monkeypatch):
+    """Two kernels per call with a workspace once the grid exceeds one wave of resident CTAs
+    (two per SM; 152 SMs when no device is visible), one otherwise; the override forces either."""
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)
+    assert _native.launch_config(151936, 1, B=1024)["kernels_with_workspace"] == 2
+    assert _native.launch_config(151936, 0, B=128)["kernels_with_workspace"] == 1
+    assert _native.launch_config(32000, 0, B=64)["kernels_with_workspace"] == 1
+    monkeypatch.setenv("SPECDEC_SCHEDULE", "1")
+    assert _native.launch_config(32000, 0, B=64)["kernels_with_workspace"] == 2
+    monkeypatch.setenv("SPECDEC_SCHEDULE", "0")
+    assert _native.launch_config(151936, 1, B=1024)["kernels_with_workspace"] == 1
+
+
 def test_launch_config_rejects(lib, monkeypatch):
     monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
     with pytest.raises(_native.SpecdecError) as e:
