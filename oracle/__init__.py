@@ -73,6 +73,10 @@ def load(path: str = _LIB):
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.POINTER(_Diag)]
+    ng = lib.specdec_ngram_ref
+    ng.restype = ctypes.c_int
+    ng.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     _loaded[path] = lib
     return lib
 
@@ -125,3 +129,28 @@ def verify(w, *, score_request: int = -1, counters: Optional[np.ndarray] = None,
     return OracleResult(out_tokens=out_tokens, out_num_accepted=out_num, counters=ctr, status=status,
                         alpha=alpha, row_m=row_m, row_S=row_S, emit_top1=top1, emit_top2=top2,
                         emit_scores=scores, telemetry=telemetry)
+
+
+def ngram_propose(histories, *, min_n: int = 2, max_n: int = 4, k: int = 3, lib_path: str = _LIB):
+    """N-gram proposer on the host (specdec_ngram_ref). `histories` is a list of token sequences,
+    or a pair (tokens int32 [total], cu_hist int64 [B+1]). Returns (drafts [B, k] with -1 padding,
+    num [B], match [B]) as numpy arrays."""
+    lib = load(lib_path)
+    if isinstance(histories, tuple):
+        tokens, cu = (np.ascontiguousarray(histories[0], dtype=np.int32),
+                      np.ascontiguousarray(histories[1], dtype=np.int64))
+    else:
+        lens = [len(h) for h in histories]
+        cu = np.zeros(len(histories) + 1, dtype=np.int64)
+        cu[1:] = np.cumsum(lens)
+        tokens = (np.concatenate([np.asarray(h, dtype=np.int32) for h in histories])
+                  if histories and cu[-1] > 0 else np.zeros(1, dtype=np.int32))
+    B = cu.size - 1
+    drafts = np.full((B, max(k, 1)), -7, dtype=np.int32)
+    num = np.full(B, -7, dtype=np.int32)
+    match = np.full(B, -7, dtype=np.int32)
+    rc = lib.specdec_ngram_ref(_ptr(tokens), _ptr(cu), B, int(min_n), int(max_n), int(k), _ptr(drafts),
+                               _ptr(num), _ptr(match))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the n-gram arguments (rc={rc})")
+    return drafts[:, :k], num, match

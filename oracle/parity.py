@@ -39,12 +39,13 @@ class ParityReport:
     row_m_max_rel: float = 0.0
     row_S_max_rel: float = 0.0
     row_bad: List[tuple] = dataclasses.field(default_factory=list)
+    telemetry_mismatch: str = ""
     compared_tokens: int = 0
 
     @property
     def ok(self) -> bool:
         return not (self.token_mismatches or self.accepted_mismatches or self.status_mismatches
-                    or self.counter_mismatch or self.alpha_bad or self.row_bad)
+                    or self.counter_mismatch or self.alpha_bad or self.row_bad or self.telemetry_mismatch)
 
     def summary(self) -> str:
         return (f"requests={self.requests} excluded_requests={self.excluded_requests} "
@@ -52,7 +53,8 @@ class ParityReport:
                 f"token_mismatches={len(self.token_mismatches)} accepted_mismatches={len(self.accepted_mismatches)} "
                 f"status_mismatches={len(self.status_mismatches)} counters='{self.counter_mismatch}' "
                 f"alpha_max_rel={self.alpha_max_rel:.3g} row_m_max_rel={self.row_m_max_rel:.3g} "
-                f"row_S_max_rel={self.row_S_max_rel:.3g} alpha_bad={len(self.alpha_bad)} row_bad={len(self.row_bad)}")
+                f"row_S_max_rel={self.row_S_max_rel:.3g} alpha_bad={len(self.alpha_bad)} row_bad={len(self.row_bad)} "
+                f"telemetry='{self.telemetry_mismatch}'")
 
 
 def _rel(a, b):
@@ -69,6 +71,7 @@ def compare(w, gpu: dict, ref: dict, counters_before=(0, 0, 0, 0)) -> ParityRepo
         (w.temperature > 0) & (w.temperature < np.float32(1.17549435e-38)))
     excluded_A_gpu = 0
     excluded_A_ref = 0
+    excluded_pairs = []          # (oracle a_b, library a_b) of requests cut at a near-tie
     g_tok, r_tok = gpu["out_tokens"], ref["out_tokens"]
     g_acc, r_acc = gpu["out_num_accepted"], ref["out_num_accepted"]
     for b in range(w.B):
@@ -96,6 +99,7 @@ def compare(w, gpu: dict, ref: dict, counters_before=(0, 0, 0, 0)) -> ParityRepo
             rep.excluded_positions += k + 1 - cut
             excluded_A_gpu += int(g_acc[b])
             excluded_A_ref += a_ref
+            excluded_pairs.append((a_ref, int(g_acc[b])))
             for j in range(cut):
                 rep.compared_tokens += 1
                 if g_tok[row0 + j] != r_tok[row0 + j]:
@@ -114,6 +118,20 @@ def compare(w, gpu: dict, ref: dict, counters_before=(0, 0, 0, 0)) -> ParityRepo
         rep.counter_mismatch = f"R/I/D gpu={list(gc[:3])} oracle={list(rc[:3])}"
     elif int(gc[3]) - excluded_A_gpu != int(rc[3]) - excluded_A_ref:
         rep.counter_mismatch = f"A (outside exclusions) gpu={int(gc[3]) - excluded_A_gpu} oracle={int(rc[3]) - excluded_A_ref}"
+
+    if gpu.get("telemetry") is not None and ref.get("telemetry") is not None:
+        # drafts and eligible drafts by position are exact; accepted-through counts and the
+        # histogram are exact outside the excluded requests, whose library a_b replaces the oracle's
+        gt = np.asarray(gpu["telemetry"], dtype=np.int64).reshape(4, -1)
+        want = np.asarray(ref["telemetry"], dtype=np.int64).reshape(4, -1).copy()
+        for a_r, a_g in excluded_pairs:
+            want[2, :a_r] -= 1
+            want[3, a_r] -= 1
+            want[2, :a_g] += 1
+            want[3, a_g] += 1
+        if gt.shape != want.shape or not np.array_equal(gt, want):
+            bad = [(int(r), int(j), int(gt[r, j]), int(want[r, j])) for r, j in zip(*np.nonzero(gt != want))][:8]
+            rep.telemetry_mismatch = f"(row, position, library, oracle): {bad}"
 
     if "diag_accept_prob" in gpu:
         ga = gpu["diag_accept_prob"][: w.N].astype(np.float64)

@@ -352,3 +352,43 @@ int specdec_verify_ref(
     free(c.z); free(c.p); free(c.w);
     return 0;
 }
+
+
+/* ---------------------------------------------------------------------------------------------
+ * N-gram proposer (see specdec_ref.h): the rule of the infra-guide's section 6 hands-on, window
+ * lengths from long to short, start positions from front to back, first hit wins.
+ * ------------------------------------------------------------------------------------------- */
+int specdec_ngram_ref(const int32_t* tokens, const int64_t* cu_hist, int32_t B, int32_t min_n,
+                      int32_t max_n, int32_t k, int32_t* out_drafts, int32_t* out_num,
+                      int32_t* out_match)
+{
+    if (B < 0 || min_n < 1 || k < 0 || !cu_hist || !out_num || !out_match) return 1;
+    if (B > 0 && (!tokens || (k > 0 && !out_drafts))) return 1;
+    for (int32_t b = 0; b < B; ++b)
+        if (cu_hist[b + 1] < cu_hist[b] || cu_hist[b] < 0) return 1;
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t* h = tokens + cu_hist[b];
+        const int64_t L = cu_hist[b + 1] - cu_hist[b];
+        int32_t hit_n = 0;
+        int64_t hit_start = -1;
+        const int64_t n_hi = (int64_t)max_n < L - 1 ? (int64_t)max_n : L - 1;
+        for (int64_t n = n_hi; n >= min_n && hit_n == 0; --n) {
+            const int32_t* tail = h + (L - n);
+            for (int64_t start = 0; start < L - n; ++start) {
+                int64_t i = 0;
+                while (i < n && h[start + i] == tail[i]) ++i;
+                if (i == n) { hit_n = (int32_t)n; hit_start = start; break; }
+            }
+        }
+        int32_t num = 0;
+        if (hit_n > 0) {
+            const int64_t from = hit_start + hit_n;
+            for (int64_t j = 0; j < k && from + j < L; ++j) out_drafts[(int64_t)b * k + j] = h[from + j];
+            num = (int32_t)((L - from) < k ? (L - from) : k);
+        }
+        for (int64_t j = num; j < k; ++j) out_drafts[(int64_t)b * k + j] = -1;
+        out_num[b] = num;
+        out_match[b] = hit_n;
+    }
+    return 0;
+}

@@ -89,6 +89,20 @@ int specdec_verify_ref(
     uint32_t* status,                                  /* [B] or NULL */
     specdec_ref_diag* diag);                           /* or NULL */
 
+/*
+ * N-gram proposer ("5.2 Draft models and model-free methods", infra-guide, sections 4.1 and 6):
+ * for request b with history h = tokens[cu_hist[b] .. cu_hist[b+1]) of length L, try window
+ * lengths n from min(max_n, L - 1) down to min_n; for each n scan start positions 0, 1, ...,
+ * L - n - 1 (the tail itself excluded) for h[start, start + n) == h[L - n, L); the first hit
+ * proposes h[start + n, start + n + k) cut at L. out_drafts[b * k + j] holds the proposal
+ * (-1 after it), out_num[b] its length, out_match[b] the window length n (0 on a miss).
+ * Returns 0, or 1 on invalid arguments (min_n < 1, k < 0, B < 0, a NULL pointer, or
+ * decreasing offsets); nothing is written then.
+ */
+int specdec_ngram_ref(const int32_t* tokens, const int64_t* cu_hist, int32_t B, int32_t min_n,
+                      int32_t max_n, int32_t k, int32_t* out_drafts, int32_t* out_num,
+                      int32_t* out_match);
+
 #ifdef __cplusplus
 }
 #endif

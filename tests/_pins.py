@@ -554,9 +554,66 @@ def check_telemetry(lib_path=None, seed=71):
             assert not done.all()
 
 
+# ---------------------------------------------------------------------------------------------
+# n-gram proposer ("5.2 Draft models and model-free methods", sections 4.1 and 6)
+# ---------------------------------------------------------------------------------------------
+
+def _ngram_check_one(h, min_n, max_n, k, drafts, num, match):
+    """The proposal against numpy sliding windows: the window is the longest length in
+    [min_n, min(max_n, L - 1)] whose last-n tail occurs earlier, at its earliest start."""
+    h = np.asarray(h, dtype=np.int64)
+    L = h.size
+    cap = min(max_n, L - 1)
+    best = None
+    for n in range(cap, min_n - 1, -1):
+        if n < 1 or L - n < 1:
+            continue
+        win = np.lib.stride_tricks.sliding_window_view(h[: L - 1], n)     # windows starting at 0 .. L-n-1
+        eq = np.flatnonzero((win == h[L - n:]).all(axis=1))
+        if eq.size:
+            best = (n, int(eq[0]))
+            break
+    if best is None:
+        assert match == 0 and num == 0 and (np.asarray(drafts) == -1).all(), (h, match, num, drafts)
+        return False
+    n, start = best
+    want = h[start + n: start + n + k]
+    assert match == n and num == want.size, (h.tolist(), n, start, match, num)
+    assert np.array_equal(np.asarray(drafts[:num]), want) and (np.asarray(drafts[num:]) == -1).all()
+    return True
+
+
+def check_ngram_proposer(lib_path=None, seed=81):
+    kw = {} if lib_path is None else {"lib_path": lib_path}
+    g = _golden("ngram_worked_example.json")
+    for c in g["cases"]:
+        d, num, match = oracle.ngram_propose([c["history"]], min_n=c["min_n"], max_n=c["max_n"], k=c["k"], **kw)
+        want_match = 0 if c["match"] is None else c["match"]
+        assert int(match[0]) == want_match and d[0, : int(num[0])].tolist() == c["drafts"], (c["name"], d, num, match)
+    # random histories over a small vocabulary (plenty of repeats), every parameter combination
+    rng = np.random.default_rng(seed)
+    hits = 0
+    for _ in range(400):
+        L = int(rng.integers(0, 40))
+        h = rng.integers(0, int(rng.integers(2, 6)), size=L).tolist()
+        min_n = int(rng.integers(1, 5))
+        max_n = int(rng.integers(min_n - 1, 7))
+        k = int(rng.integers(0, 6))
+        d, num, match = oracle.ngram_propose([h], min_n=min_n, max_n=max_n, k=k, **kw)
+        hits += _ngram_check_one(h, min_n, max_n, k, d[0], int(num[0]), int(match[0]))
+    assert hits > 100
+    # a batch gives the same answers as one request at a time
+    hs = [rng.integers(0, 4, size=int(rng.integers(0, 30))).tolist() for _ in range(50)]
+    d, num, match = oracle.ngram_propose(hs, min_n=2, max_n=5, k=4, **kw)
+    for b, h in enumerate(hs):
+        d1, n1, m1 = oracle.ngram_propose([h], min_n=2, max_n=5, k=4, **kw)
+        assert np.array_equal(d[b], d1[0]) and num[b] == n1[0] and match[b] == m1[0]
+
+
 ALL_PINS = [
     check_worked_counter_example,
     check_telemetry,
+    check_ngram_proposer,
     check_strict_accept_comparison,
     check_edge_cases,
     check_residual_excludes_draft,

@@ -43,6 +43,12 @@ MUTANTS = {
     "telemetry_eligible_counts_every_draft": ("for (int32_t j = 0; j < g; ++j) tm[1 * 33 + j] += 1;",
                                               "for (int32_t j = 0; j < k; ++j) tm[1 * 33 + j] += 1;"),
     "telemetry_histogram_of_k": ("tm[3 * 33 + a] += 1;", "tm[3 * 33 + k] += 1;"),
+    "ngram_tail_matches_itself": ("for (int64_t start = 0; start < L - n; ++start) {",
+                                  "for (int64_t start = 0; start <= L - n; ++start) {"),
+    "ngram_latest_start": ("for (int64_t start = 0; start < L - n; ++start) {\n                int64_t i = 0;\n                while (i < n && h[start + i] == tail[i]) ++i;\n                if (i == n) { hit_n = (int32_t)n; hit_start = start; break; }",
+                           "for (int64_t start = 0; start < L - n; ++start) {\n                int64_t i = 0;\n                while (i < n && h[start + i] == tail[i]) ++i;\n                if (i == n) { hit_n = (int32_t)n; hit_start = start; }"),
+    "ngram_short_windows_first": ("for (int64_t n = n_hi; n >= min_n && hit_n == 0; --n) {",
+                                  "for (int64_t n = min_n; n <= n_hi && hit_n == 0; ++n) {"),
     "no_stop_at_rejection": ("        a = j;\n        emitted = exponential_race(c, t, b);\n        break;",
                              "        a = j;\n        emitted = exponential_race(c, t, b);\n        c->out_tokens[t] = emitted;\n        continue;"),
 }
@@ -65,6 +71,7 @@ def _run_pins(lib):
     checks = [
         ("worked_counter_example", lambda: _pins.check_worked_counter_example(lib)),
         ("telemetry", lambda: _pins.check_telemetry(lib)),
+        ("ngram", lambda: _pins.check_ngram_proposer(lib)),
         ("strict_accept_comparison", lambda: _pins.check_strict_accept_comparison(lib)),
         ("edge_cases", lambda: _pins.check_edge_cases(lib)),
         ("residual_excludes_draft", lambda: _pins.check_residual_excludes_draft(lib)),

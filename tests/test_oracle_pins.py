@@ -44,3 +44,7 @@ def test_residual_excludes_draft():
 
 def test_telemetry_by_position():
     _pins.check_telemetry()
+
+
+def test_ngram_proposer():
+    _pins.check_ngram_proposer()
