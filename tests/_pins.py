@@ -509,9 +509,8 @@ def check_residual_excludes_draft(lib_path=None, seed=61):
 
 
 # ---------------------------------------------------------------------------------------------
-# per-position telemetry ("vLLM tour part 2", section "Telemetry and tuning"; "Speculative
-# decoding -- code walkthrough", section 7.2: a position counts drafts accepted all the way
-# through it)
+# per-position telemetry ("vLLM tour part 2", section "Telemetry and tuning"; "5.2 Draft models
+# and model-free methods", section 7.2: a position counts drafts accepted all the way through it)
 # ---------------------------------------------------------------------------------------------
 
 def _telemetry_expect(entry, k):
@@ -608,6 +607,52 @@ def check_ngram_proposer(lib_path=None, seed=81):
     for b, h in enumerate(hs):
         d1, n1, m1 = oracle.ngram_propose([h], min_n=2, max_n=5, k=4, **kw)
         assert np.array_equal(d[b], d1[0]) and num[b] == n1[0] and match[b] == m1[0]
+
+
+# ---------------------------------------------------------------------------------------------
+# bitmask scatter ("vLLM tour part 2", section "Grammar gates: structured output")
+# ---------------------------------------------------------------------------------------------
+
+def _rows(cu, b):
+    return np.arange(int(cu[b]) + b, int(cu[b + 1]) + b + 1)
+
+
+def check_bitmask_scatter(seed=91):
+    """Round trip: compacting a batch-order mask with numpy fancy indexing (constrained requests in
+    a random scheduler order) and scattering it back gives the mask on the constrained rows and
+    all-ones elsewhere; identity and empty cases; the readings for malformed lists."""
+    from oracle import bitmask_ref
+
+    rng = np.random.default_rng(seed)
+    for trial in range(30):
+        B = int(rng.integers(1, 40))
+        V = int(rng.integers(1, 200))
+        W = (V + 31) // 32
+        ks = rng.integers(0, 6, size=B)
+        cu = np.zeros(B + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(ks)
+        T = int(cu[B]) + B
+        full = rng.integers(-2 ** 31, 2 ** 31, size=(T, W), dtype=np.int64).astype(np.int32)
+        order = rng.permutation(B)[: int(rng.integers(0, B + 1))]
+        rows = np.concatenate([_rows(cu, b) for b in order]) if order.size else np.zeros(0, dtype=np.int64)
+        compact = full[rows]
+        out = bitmask_ref.bitmask_scatter(compact, order, cu, B, V)
+        want = np.full((T, W), -1, dtype=np.int32)
+        for b in order:
+            want[_rows(cu, b)] = full[_rows(cu, b)]
+        assert np.array_equal(out, want), trial
+        # every request constrained, in batch order: the identity
+        assert np.array_equal(bitmask_ref.bitmask_scatter(full, np.arange(B), cu, B, V), full)
+        # nothing constrained: all ones
+        assert (bitmask_ref.bitmask_scatter(full[:0], [], cu, B, V) == -1).all()
+    # malformed lists: an out-of-range id owns no rows; a repeat keeps its first rows; rows past the
+    # end of the compact array allow nothing
+    cu = np.array([0, 1, 3], dtype=np.int32)                      # request 0: 2 rows, request 1: 3 rows
+    comp = np.arange(10, dtype=np.int32).reshape(-1, 1) + 100     # 10 rows of one word (V <= 32)
+    out = bitmask_ref.bitmask_scatter(comp, [7, 1, -3, 1, 0], cu, 2, 20)
+    assert out[:, 0].tolist() == [106, 107, 100, 101, 102]        # request 0 after 1's two listings
+    out = bitmask_ref.bitmask_scatter(comp[:4], [1, 0], cu, 2, 20)
+    assert out[:, 0].tolist() == [103, 0, 100, 101, 102]          # request 0's second row is past the end
 
 
 ALL_PINS = [

@@ -48,3 +48,7 @@ def test_telemetry_by_position():
 
 def test_ngram_proposer():
     _pins.check_ngram_proposer()
+
+
+def test_bitmask_scatter():
+    _pins.check_bitmask_scatter()
