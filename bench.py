@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ngram", action="store_true",
+                    help="time the n-gram proposer (model-free drafter) instead of the verify")
+    ap.add_argument("--scatter", action="store_true",
+                    help="time the bitmask scatter (compact scheduler-order masks -> batch rows) instead")
     ap.add_argument("--requests", type=int, default=0,
                     help="verify only the first N requests of the workload (profiler captures); 0 = all")
     return ap.parse_args()
@@ -68,11 +72,9 @@ def dist_env():
 
 
 def kernel_hash() -> str:
-    h = hashlib.sha256()
-    for p in (KERNEL_SRC, os.path.join(ROOT, "include", "specdec.h")):
-        with open(p, "rb") as f:
-            h.update(f.read())
-    return h.hexdigest()[:16]
+    """Hash of the verify kernels' source: profiler counters are tied to the code they measured."""
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def measured_peaks():
@@ -313,11 +315,150 @@ def traffic_from_profiles(config_name: str):
     return e.get("dram_bytes_per_launch")
 
 
+def telemetry_summary(tm: np.ndarray, steps: int) -> dict:
+    """Per-step drafts / eligible / accepted-through counts by position and the accepted-length
+    histogram, trimmed to the longest position with drafts."""
+    tm = np.asarray(tm, dtype=np.int64).reshape(4, -1) // max(steps, 1)
+    n = int(np.flatnonzero(tm[0]).max()) + 1 if tm[0].any() else 0
+    return {"drafts_by_position": tm[0, :n].tolist(), "eligible_by_position": tm[1, :n].tolist(),
+            "accepted_through_position": tm[2, :n].tolist(), "accepted_length_histogram": tm[3, :n + 1].tolist()}
+
+
+def run_ngram(args, world, rank, local):
+    """The n-gram proposer on 1024 synthetic histories of 1-8 K tokens (half of them ending inside
+    a repeated span): proposals (requests) per second; roofline on the history bytes it must read."""
+    import torch
+
+    from speculative_decoding_verification_specdec_gb300 import _native, build
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if rank == 0 and build.needs_rebuild():
+        build.build_library()
+    _native.load()
+    min_n, max_n, k = 2, 5, 8
+    hs = W.ngram_histories(7 + 1000 * rank, B=1024 if args.requests <= 0 else args.requests, L=(1024, 8192))
+    tokens = torch.from_numpy(hs.tokens).to(dev)
+    cu = torch.from_numpy(hs.cu_hist).to(dev)
+    B = hs.B
+    d = torch.empty((B, k), dtype=torch.int32, device=dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    m = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        _native.ngram_propose(tokens, cu, B, min_n, max_n, k, d, n, m, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler.mark("t0")
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        _native.ngram_propose(tokens, cu, B, min_n, max_n, k, d, n, m, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks = sampler.stop()
+    mean_s = sum(ms) / len(ms) / 1e3
+    # algorithmic bytes: every token of every history once, the offsets, the outputs
+    alg = 4 * int(hs.tokens.size) + 8 * (B + 1) + 4 * B * (k + 2)
+    peak, peak_kind = measured_peaks()
+    hits = float((m.cpu().numpy() > 0).mean())
+    line = {
+        "metric": "n-gram proposals/s (requests drafted per second)", "value": B / mean_s, "unit": "proposals/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": hs.name, "B": B, "tokens": int(hs.tokens.size), "min_n": min_n, "max_n": max_n, "k": k,
+                   "hit_rate": hits, "l2": "flushed between timed steps (268 MB write)"},
+        "roofline": {"bound": "hbm", "achieved": alg / mean_s / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / mean_s / 1e9 / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "specdec_ngram_kernel", "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "kernel_ms": {"median": statistics.median(ms), "min": min(ms), "max": max(ms)},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_scatter(args, world, rank, local):
+    """The bitmask scatter on the large mixed batch's masks (B=1024, V=151936, k~U{1..8}; the masked
+    half constrained, in a random scheduler order): rows per second; roofline on the bytes it must
+    move (read the constrained rows, write every row)."""
+    import torch
+
+    from speculative_decoding_verification_specdec_gb300 import _native, build
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if rank == 0 and build.needs_rebuild():
+        build.build_library()
+    _native.load()
+    w = workload_for(4, rank, args.requests)
+    cu = w.cu_num_draft
+    masked = [b for b in range(w.B) if not (w.bitmask[w.row(b, 0)] == -1).all()]
+    order = np.random.default_rng(4 + rank).permutation(np.asarray(masked, dtype=np.int32))
+    rows = np.concatenate([np.arange(int(cu[b]) + b, int(cu[b + 1]) + b + 1) for b in order])
+    compact = torch.from_numpy(np.ascontiguousarray(w.bitmask[rows])).to(dev)
+    ids = torch.from_numpy(order).to(dev)
+    cut = torch.from_numpy(cu).to(dev)
+    out = torch.empty((w.T, w.W), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    def step():
+        _native.bitmask_scatter(compact, compact.shape[0], ids, ids.numel(), cut, w.B, w.V, out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), w.bitmask)       # the batch's own masks, unmasked rows all ones
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler.mark("t0")
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks = sampler.stop()
+    mean_s = sum(ms) / len(ms) / 1e3
+    alg = 4 * w.W * (rows.size + w.T) + 4 * (ids.numel() + w.B + 1)
+    peak, peak_kind = measured_peaks()
+    line = {
+        "metric": "bitmask rows placed per second (batch-order rows written)", "value": w.T / mean_s,
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"{w.name}_bitmask_scatter", "B": w.B, "V": w.V, "rows": w.T,
+                   "constrained_requests": int(ids.numel()), "compact_rows": int(rows.size),
+                   "l2": "flushed between timed steps (268 MB write)"},
+        "roofline": {"bound": "hbm", "achieved": alg / mean_s / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": alg / mean_s / 1e9 / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "specdec_bitmask_scatter_kernel", "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "kernel_ms": {"median": statistics.median(ms), "min": min(ms), "max": max(ms)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.ngram:
+        return run_ngram(args, world, rank, local)
+    if args.scatter:
+        return run_scatter(args, world, rank, local)
 
     import torch
 
@@ -340,7 +481,7 @@ def main():
     w = workload_for(args.config, rank, args.requests)
     host = device.host_tensors(w)
     dev_in = device.device_tensors(w, dev, host)
-    out = device.alloc_outputs(w, dev, diag=False)
+    out = device.alloc_outputs(w, dev, diag=False, telemetry=True)   # per-position counts, every step
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
@@ -463,6 +604,7 @@ def main():
             "clocks": clocks,
             "kernel_ms": {"median": statistics.median(kernel_ms), "min": min(kernel_ms), "max": max(kernel_ms)},
             "counters_per_step": [int(c) // args.steps for c in ctr],
+            "telemetry_per_step": telemetry_summary(res["telemetry"], args.steps),
             "kernel_hash": kernel_hash(),
         }
         print(json.dumps(line), flush=True)

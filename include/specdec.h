@@ -43,6 +43,7 @@ extern "C" {
 #endif
 
 #define SPECDEC_KMAX 32           /* largest supported max_k (drafts per request) */
+#define SPECDEC_TELEMETRY_ROW (SPECDEC_KMAX + 1)   /* entries per telemetry row */
 
 typedef enum {
     SPECDEC_OK = 0,
@@ -95,6 +96,15 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  and S = sum_i exp(z_i / T - m) on random requests, (max_i z_i, NaN) on
  *                  greedy ones; (NaN, NaN) for rows not read. Entries of a request skipped
  *                  for SPECDEC_ST_BAD_OFFSETS are left untouched (its rows are unknown).
+ *   telemetry      [4 * SPECDEC_TELEMETRY_ROW] uint64 or NULL, ADDED to (never cleared), 8-byte
+ *                  aligned: per position j, row 0 counts drafts (k_b > j), row 1 grammar-eligible
+ *                  drafts (g_b > j, g_b the grammar-valid prefix behind I and D), row 2 drafts
+ *                  accepted all the way through position j (a_b > j); row 3 [a] counts requests
+ *                  that accepted exactly a drafts. Requests skipped for K_TOO_LARGE or BAD_OFFSETS
+ *                  are not counted. Rows 0..2 sum to R, D and A. ("vLLM tour part 2", section
+ *                  "Telemetry and tuning": per-position draft / accepted counts and the histogram
+ *                  of accepted lengths; "5.2 Draft models and model-free methods", section 7.2:
+ *                  a position counts drafts accepted through it.)
  *   workspace      device scratch of at least specdec_workspace_size(B, V) bytes, 16-byte
  *                  aligned, caller-owned, or NULL. With a workspace a one-CTA kernel first orders
  *                  the requests by an estimate of their work, heaviest first, and the verify
@@ -113,7 +123,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
  * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
  * pointer (draft_ids may be NULL), B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
- * element; SPECDEC_ERR_UNSUPPORTED for an unknown dtype (or, with the cluster kernel that
+ * element (telemetry: 8 bytes); SPECDEC_ERR_UNSUPPORTED for an unknown dtype (or, with the cluster kernel that
  * keeps each row slice on chip, a row wider than 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
  *
  * Kernels: by default each request is verified by a cluster of G CTAs (G = 1 for large
@@ -141,6 +151,7 @@ specdec_status_t specdec_verify(
     uint32_t* status,
     float* diag_accept_prob,
     float* diag_row_stats,
+    unsigned long long* telemetry,
     void* workspace,
     size_t workspace_bytes,
     void* stream);
@@ -188,7 +199,62 @@ specdec_status_t specdec_verify_noalloc(
     uint32_t* status,
     float* diag_accept_prob,
     float* diag_row_stats,
+    unsigned long long* telemetry,
     void* stream);
+
+/*
+ * specdec_ngram_propose -- model-free drafts for a batch: the n-gram proposer of "5.2 Draft
+ * models and model-free methods" (infra-guide), sections 4.1 and 6 (stream-ordered,
+ * asynchronous). For request b with history h = tokens[cu_hist[b] .. cu_hist[b+1]) of length L,
+ * the window length is the longest n in [min_n, min(max_n, L - 1)] such that the last n tokens of
+ * h also occur earlier in h (the tail itself excluded), taking the earliest such occurrence; the
+ * proposal is the (up to) k tokens that follow it, cut at the end of h. The drafts go to the
+ * verify as model-free drafts (no q): accepted with probability p(x).
+ *
+ *   tokens         [cu_hist[B]] int32 token ids, the histories back to back (device).
+ *   cu_hist        [B+1] int64 offsets; a request with cu_hist[b+1] < cu_hist[b] or a negative
+ *                  offset counts as an empty history (a miss).
+ *   B              requests (>= 0).
+ *   min_n, max_n   window lengths tried, 1 <= min_n; max_n <= SPECDEC_NGRAM_MAX_N (64);
+ *                  max_n < min_n means no window is tried.
+ *   k              proposal length, 0 <= k <= SPECDEC_KMAX.
+ *   out_drafts     [B, k] int32: the proposal, then -1.
+ *   out_num        [B] int32 proposal lengths (0 on a miss).
+ *   out_match      [B] int32 window length of the match (0 on a miss).
+ * Returns SPECDEC_OK once queued; SPECDEC_ERR_INVALID_ARG for a bad size, a NULL required pointer
+ * or a misaligned one (nothing launched); SPECDEC_ERR_UNSUPPORTED for max_n > 64;
+ * SPECDEC_ERR_CUDA if the launch fails.
+ */
+#define SPECDEC_NGRAM_MAX_N 64
+specdec_status_t specdec_ngram_propose(const int32_t* tokens, const int64_t* cu_hist, int32_t B,
+                                       int32_t min_n, int32_t max_n, int32_t k, int32_t* out_drafts,
+                                       int32_t* out_num, int32_t* out_match, void* stream);
+
+/*
+ * specdec_bitmask_scatter -- the grammar bitmask of one verify step in batch order, from the
+ * compacted masks in scheduler order ("vLLM tour part 2", section "Grammar gates: structured
+ * output": masks arrive compacted to the constrained requests in scheduler order, while the batch
+ * has its own order and per-request speculative offsets). Stream-ordered, asynchronous.
+ *
+ *   compact        [compact_rows, W] int32, W = ceil(V / 32): for each constrained request in
+ *                  scheduler order, its k_b + 1 rows (draft positions, then the bonus position).
+ *   constrained    [n] int32: the batch index b of each constrained request, scheduler order.
+ *   cu_num_draft   [B+1] int32 batch-order draft offsets (the verify's layout: row t(b, j) =
+ *                  cu[b] + b + j, j in [0, k_b]).
+ *   bitmask        [T, W] int32 output, T = cu[B] + B: the rows of each constrained request take
+ *                  its compact rows; rows of every other request are all ones (-1: all allowed).
+ * Readings for malformed input: an id outside [0, B) owns no compact rows; a request listed twice
+ * takes the rows of its first listing (the second listing's rows are skipped over); a row past the
+ * end of `compact` gets zeros (nothing allowed; the verify then reports an empty mask row); a
+ * request with malformed offsets (as SPECDEC_ST_BAD_OFFSETS) owns no rows and its rows are not
+ * written. Returns SPECDEC_OK once queued; SPECDEC_ERR_INVALID_ARG for a bad size, a NULL
+ * required pointer or a misaligned one; SPECDEC_ERR_UNSUPPORTED for V > 2^26; SPECDEC_ERR_CUDA if
+ * the launch fails.
+ */
+specdec_status_t specdec_bitmask_scatter(const int32_t* compact, int64_t compact_rows,
+                                         const int32_t* constrained, int32_t n,
+                                         const int32_t* cu_num_draft, int32_t B, int32_t V,
+                                         int32_t* bitmask, void* stream);
 
 /*
  * specdec_wait -- block the calling host thread until all work queued on `stream` has

@@ -21,17 +21,22 @@ def bitmask_scatter(compact: np.ndarray, constrained, cu_num_draft: np.ndarray, 
     Readings (the pages are silent on malformed input): an id outside [0, B) owns no rows; a
     request listed twice takes the rows of its first listing (the second listing's rows are
     skipped over); rows a request would take beyond the end of `compact` allow nothing (zero
-    words), which the verify reports as an empty mask row."""
+    words), which the verify reports as an empty mask row; a request whose offsets are malformed
+    (cu[0] != 0, cu[b] < 0, cu[b+1] < cu[b] or cu[b+1] > cu[B], as the verify's BAD_OFFSETS) owns
+    no rows and its output rows are left as they were (all ones here)."""
     W = (V + 31) // 32
     cu = np.asarray(cu_num_draft, dtype=np.int64)
-    T = int(cu[B]) + B
+    T = max(int(cu[B]), 0) + B
     out = np.full((T, W), -1, dtype=np.int32)
     R_c = int(compact.shape[0]) if compact is not None else 0
     off = 0
     placed = set()
+    def malformed(b):
+        return cu[0] != 0 or cu[b] < 0 or cu[b + 1] < cu[b] or cu[b + 1] > cu[B]
+
     for b in constrained:
         b = int(b)
-        if b < 0 or b >= B:
+        if b < 0 or b >= B or malformed(b):
             continue
         k = int(cu[b + 1] - cu[b])
         if b not in placed:

@@ -65,8 +65,8 @@ typedef struct {
                            * accepted through position j (j < a_b); row 3 [a] counts requests
                            * that accepted exactly a drafts. Skipped requests are not counted.
                            * ("vLLM tour part 2", section "Telemetry and tuning": per-position
-                           * draft / accepted counts and the acceptance histogram; "Speculative
-                           * decoding -- code walkthrough", section 7.2: the per-position count
+                           * draft / accepted counts and the acceptance histogram; "5.2 Draft
+                           * models and model-free methods", section 7.2: the per-position count
                            * is of drafts accepted all the way through that position.) */
 } specdec_ref_diag;
 

@@ -19,6 +19,7 @@ SPECDEC_ERR_TIMEOUT = 4
 SPECDEC_F32 = 0
 SPECDEC_BF16 = 1
 SPECDEC_KMAX = 32
+TELEMETRY_SHAPE = (4, SPECDEC_KMAX + 1)   # rows: drafts, eligible, accepted-through by position; histogram
 
 ST_BAD_DRAFT_ID = 1
 ST_EMPTY_MASK_ROW = 2
@@ -28,7 +29,9 @@ ST_BAD_OFFSETS = 16
 ST_DEVICE_TIMEOUT = 32
 
 EXPORTED = ("specdec_verify", "specdec_verify_noalloc", "specdec_wait", "specdec_status_string",
-            "specdec_launch_config", "specdec_workspace_size")
+            "specdec_launch_config", "specdec_workspace_size", "specdec_ngram_propose",
+            "specdec_bitmask_scatter")
+NGRAM_MAX_N = 64                        # SPECDEC_NGRAM_MAX_N
 NOALLOC_MAX_REQUESTS = 16384            # SPECDEC_NOALLOC_MAX_REQUESTS
 
 _lib = None
@@ -51,10 +54,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.specdec_verify.restype = ctypes.c_int
     lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
-                                   vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+                                   vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.specdec_verify_noalloc.restype = ctypes.c_int
     lib.specdec_verify_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
-                                           vp, vp, vp, vp, vp, vp, vp]
+                                           vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.specdec_ngram_propose.restype = ctypes.c_int
+    lib.specdec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.specdec_bitmask_scatter.restype = ctypes.c_int
+    lib.specdec_bitmask_scatter.argtypes = [vp, ctypes.c_int64, vp, i32, vp, i32, i32, vp, vp]
     lib.specdec_workspace_size.restype = ctypes.c_size_t
     lib.specdec_workspace_size.argtypes = [i32, i32]
     lib.specdec_wait.restype = ctypes.c_int
@@ -117,7 +124,7 @@ def _marshal(target_logits, logits_dtype, stream, tensors):
 def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
                    bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
                    status=None, diag_accept_prob=None, diag_row_stats=None, workspace=None, stream=None,
-                   logits_dtype=None) -> None:
+                   logits_dtype=None, telemetry=None) -> None:
     """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
     (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
     non-zero status."""
@@ -127,12 +134,12 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
         ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
         ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
         ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
-        ("workspace", workspace)))
+        ("telemetry", telemetry), ("workspace", workspace)))
     rc = load().specdec_verify(
         _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
         int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
-        _p(diag_row_stats), _p(workspace), 0 if workspace is None else _nbytes(workspace), stream)
+        _p(diag_row_stats), _p(telemetry), _p(workspace), 0 if workspace is None else _nbytes(workspace), stream)
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_verify")
 
@@ -140,19 +147,20 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
 def specdec_verify_noalloc(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int,
                            max_k: int, bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted,
                            counters, status=None, diag_accept_prob=None, diag_row_stats=None, stream=None,
-                           logits_dtype=None) -> None:
+                           logits_dtype=None, telemetry=None) -> None:
     """specdec_verify with the library's own schedule scratch (no workspace argument)."""
     dt, stream = _marshal(target_logits, logits_dtype, stream, (
         ("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
         ("has_q", has_q), ("cu_num_draft", cu_num_draft), ("bitmask", bitmask),
         ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
         ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
-        ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats)))
+        ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
+        ("telemetry", telemetry)))
     rc = load().specdec_verify_noalloc(
         _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
         int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
-        _p(diag_row_stats), stream)
+        _p(diag_row_stats), _p(telemetry), stream)
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_verify_noalloc")
 
@@ -171,3 +179,42 @@ def specdec_wait(stream=None, timeout_ms: int = -1) -> None:
     rc = load().specdec_wait(stream, int(timeout_ms))
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_wait")
+
+
+def ngram_propose(tokens, cu_hist, B: int, min_n: int, max_n: int, k: int, out_drafts, out_num, out_match,
+                  stream=None) -> None:
+    """Queue the n-gram proposer (specdec_ngram_propose) on `stream` (default: torch's current
+    stream); raises SpecdecError on a non-zero status."""
+    import torch
+
+    for name, t in (("tokens", tokens), ("cu_hist", cu_hist), ("out_drafts", out_drafts), ("out_num", out_num),
+                    ("out_match", out_match)):
+        if t is not None and hasattr(t, "is_cuda") and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load().specdec_ngram_propose(_p(tokens), _p(cu_hist), int(B), int(min_n), int(max_n), int(k),
+                                      _p(out_drafts), _p(out_num), _p(out_match), stream)
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_ngram_propose")
+
+
+def bitmask_scatter(compact, compact_rows: int, constrained, n: int, cu_num_draft, B: int, V: int, bitmask,
+                    stream=None) -> None:
+    """Queue specdec_bitmask_scatter on `stream` (default: torch's current stream)."""
+    import torch
+
+    for name, t in (("compact", compact), ("constrained", constrained), ("cu_num_draft", cu_num_draft),
+                    ("bitmask", bitmask)):
+        if t is not None and hasattr(t, "is_cuda") and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load().specdec_bitmask_scatter(_p(compact), int(compact_rows), _p(constrained), int(n), _p(cu_num_draft),
+                                        int(B), int(V), _p(bitmask), stream)
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_bitmask_scatter")

@@ -7,7 +7,7 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "specdec_verify.cu")]
+SOURCES = [os.path.join(PKG, "csrc", f) for f in ("specdec_verify.cu", "specdec_ngram.cu", "specdec_bitmask.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecdec.so")
 

@@ -99,6 +99,7 @@ struct Args {
     uint32_t* status;
     float* diag_alpha;
     float* diag_row;
+    unsigned long long* telemetry;   // [4][SPECDEC_KMAX + 1] or NULL (see specdec.h)
     int32_t B, V, max_k, W;
     int32_t slice_units;    // kUnit blocks per CTA slice
     int32_t G;              // CTAs per request (cluster size)
@@ -332,6 +333,28 @@ __device__ __forceinline__ Part cluster_reduce(Part p, float c, Shared& sh, int 
 // ---------------------------------------------------------------------------------------------
 // element access
 // ---------------------------------------------------------------------------------------------
+
+// Per-position telemetry of one verified request, one warp (lane j = position j): drafts,
+// grammar-eligible drafts and drafts accepted all the way through position j, and one count in
+// the histogram of accepted lengths ("vLLM tour part 2", section "Telemetry and tuning").
+__device__ __forceinline__ void add_telemetry(unsigned long long* tm, int lane, int k, int g, int acc)
+{
+    constexpr int kRow = SPECDEC_KMAX + 1;
+    if (lane < k) atomicAdd(tm + 0 * kRow + lane, 1ull);
+    if (lane < g) atomicAdd(tm + 1 * kRow + lane, 1ull);
+    if (lane < acc) atomicAdd(tm + 2 * kRow + lane, 1ull);
+    if (lane == 0) atomicAdd(tm + 3 * kRow + acc, 1ull);
+}
+
+// The same from one thread (the streaming kernel's writer, which holds little live state there).
+__device__ __noinline__ void add_telemetry_serial(unsigned long long* tm, int k, int g, int acc)
+{
+    constexpr int kRow = SPECDEC_KMAX + 1;
+    for (int j = 0; j < k; ++j) atomicAdd(tm + 0 * kRow + j, 1ull);
+    for (int j = 0; j < g; ++j) atomicAdd(tm + 1 * kRow + j, 1ull);
+    for (int j = 0; j < acc; ++j) atomicAdd(tm + 2 * kRow + j, 1ull);
+    atomicAdd(tm + 3 * kRow + acc, 1ull);
+}
 
 template <typename ET> struct Elem;
 
@@ -681,6 +704,7 @@ __global__ void __launch_bounds__(kThreads) specdec_verify_kernel(const Args a)
         }
         a.out_num_accepted[b] = skip == 0 ? acc_len : 0;
     }
+    if (a.telemetry && skip == 0 && rank == 0 && warp == 0) add_telemetry(a.telemetry, lane, k, g, acc_len);
     __syncthreads();
     if (sh.timed_out) {
         st |= SPECDEC_ST_DEVICE_TIMEOUT;
@@ -1798,6 +1822,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 atomicAdd(&a.counters[1], (unsigned long long)(k - g));
                 atomicAdd(&a.counters[2], (unsigned long long)g);
                 atomicAdd(&a.counters[3], (unsigned long long)acc_len);
+                if (a.telemetry) add_telemetry_serial(a.telemetry, k, g, acc_len);
             } else if (rs.skip == 2) {
                 for (int j = 0; j <= k; ++j) a.out_tokens[rs.row0 + j] = -1;
             }
@@ -2212,8 +2237,8 @@ extern "C" specdec_status_t specdec_verify(
     const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
     int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
     const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
-    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* workspace, size_t workspace_bytes,
-    void* stream)
+    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, unsigned long long* telemetry,
+    void* workspace, size_t workspace_bytes, void* stream)
 {
     if (logits_dtype != SPECDEC_F32 && logits_dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     if (B < 0 || V < 1 || max_k < 0 || max_k > SPECDEC_KMAX) return SPECDEC_ERR_INVALID_ARG;
@@ -2225,7 +2250,8 @@ extern "C" specdec_status_t specdec_verify(
         !aligned(cu_num_draft, 4) || (bitmask && !aligned(bitmask, 4)) || !aligned(temperature, 4) ||
         !aligned(uniforms, 4) || !aligned(exp_noise, 4) || !aligned(out_tokens, 4) ||
         !aligned(out_num_accepted, 4) || !aligned(counters, 8) || (status && !aligned(status, 4)) ||
-        (diag_accept_prob && !aligned(diag_accept_prob, 4)) || (diag_row_stats && !aligned(diag_row_stats, 4)))
+        (diag_accept_prob && !aligned(diag_accept_prob, 4)) || (diag_row_stats && !aligned(diag_row_stats, 4)) ||
+        (telemetry && !aligned(telemetry, 8)))
         return SPECDEC_ERR_INVALID_ARG;
     LaunchShape shape;
     const specdec_status_t rc = shape_for(V, logits_dtype, B, &shape);
@@ -2249,6 +2275,7 @@ extern "C" specdec_status_t specdec_verify(
     a.status = status;
     a.diag_alpha = diag_accept_prob;
     a.diag_row = diag_row_stats;
+    a.telemetry = telemetry;
     a.B = B;
     a.V = V;
     a.max_k = max_k;
@@ -2287,7 +2314,7 @@ extern "C" specdec_status_t specdec_verify_noalloc(
     const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
     int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
     const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
-    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, void* stream)
+    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, unsigned long long* telemetry, void* stream)
 {
     static_assert(kNoallocScratchBytes >= sizeof(int32_t) * SPECDEC_NOALLOC_MAX_REQUESTS + SPECDEC_NOALLOC_MAX_REQUESTS,
                   "scratch holds the order and the keys");
@@ -2304,7 +2331,7 @@ extern "C" specdec_status_t specdec_verify_noalloc(
     }
     return specdec_verify(target_logits, logits_dtype, draft_ids, draft_probs, has_q, cu_num_draft, B, V, max_k,
                           bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters, status,
-                          diag_accept_prob, diag_row_stats, scratch, scratch ? kNoallocScratchBytes : 0, stream);
+                          diag_accept_prob, diag_row_stats, telemetry, scratch, scratch ? kNoallocScratchBytes : 0, stream);
 }
 
 extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)

@@ -50,6 +50,7 @@ class Outputs:
     diag_accept_prob: Optional[object] = None
     diag_row_stats: Optional[object] = None
     workspace: Optional[object] = None
+    telemetry: Optional[object] = None
 
     def numpy(self) -> Dict[str, np.ndarray]:
         d = {"out_tokens": self.out_tokens, "out_num_accepted": self.out_num_accepted,
@@ -57,10 +58,12 @@ class Outputs:
         if self.diag_accept_prob is not None:
             d["diag_accept_prob"] = self.diag_accept_prob
             d["diag_row_stats"] = self.diag_row_stats
+        if self.telemetry is not None:
+            d["telemetry"] = self.telemetry
         res = {}
         for k, t in d.items():
             t = t.cpu()
-            if k == "counters":
+            if k in ("counters", "telemetry"):
                 res[k] = t.view(dtype=__import__("torch").int64).numpy().view(np.uint64).copy()
             elif k == "status":
                 res[k] = t.numpy().view(np.uint32).copy()
@@ -69,8 +72,10 @@ class Outputs:
         return res
 
 
-def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: bool = True) -> Outputs:
-    """Output tensors (and, with workspace=True, the verify's scratch: the request schedule)."""
+def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: bool = True,
+                  telemetry: Optional[bool] = None) -> Outputs:
+    """Output tensors (and, with workspace=True, the verify's scratch: the request schedule).
+    The per-position telemetry is allocated when asked for (default: with the diagnostics)."""
     import torch
 
     ws_bytes = _native.workspace_size(w.B, w.V) if workspace else 0
@@ -82,6 +87,8 @@ def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: boo
         diag_accept_prob=torch.full((max(w.N, 1),), float("nan"), dtype=torch.float32, device=device) if diag else None,
         diag_row_stats=torch.full((max(w.T, 1), 2), float("nan"), dtype=torch.float32, device=device) if diag else None,
         workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None,
+        telemetry=(torch.zeros(_native.TELEMETRY_SHAPE, dtype=torch.int64, device=device)
+                   if (diag if telemetry is None else telemetry) else None),
     )
 
 
@@ -91,7 +98,8 @@ def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> No
         dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
         w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
         out.out_tokens, out.out_num_accepted, out.counters, out.status,
-        out.diag_accept_prob, out.diag_row_stats, workspace=out.workspace, stream=stream)
+        out.diag_accept_prob, out.diag_row_stats, workspace=out.workspace, stream=stream,
+        telemetry=out.telemetry)
 
 
 def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True) -> Dict[str, np.ndarray]:

@@ -27,7 +27,7 @@ from __future__ import annotations
 import concurrent.futures
 import dataclasses
 import os
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -50,6 +50,7 @@ _TAGS = {
     "mask": 12,
     "uniforms": 13,
     "exp_noise": 14,
+    "ngram_histories": 15,
 }
 
 _ROW_BLOCK = 64  # rows generated per block (one substream each) for the [T, V] tensors
@@ -471,3 +472,48 @@ def config(i: int, seed: Optional[int] = None) -> Workload:
                           logit_sigma=3.0, temperature="half_greedy(0.5,1.2)", q_mode="half",
                           draft_sigma=0.5, mf_argmax_frac=0.4, mask="half", forced_invalid_frac=0.2)
     raise IndexError(i)
+
+
+# ----------------------------------------------------------------------------------------------
+# n-gram proposer inputs: token histories
+# ----------------------------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Histories:
+    """Token histories of a batch back to back: tokens int32 [total], cu_hist int64 [B+1]."""
+    name: str
+    tokens: np.ndarray
+    cu_hist: np.ndarray
+    V: int
+
+    @property
+    def B(self) -> int:
+        return int(self.cu_hist.size - 1)
+
+
+def ngram_histories(seed: int, B: int = 1024, L: Tuple[int, int] = (1024, 8192), V: int = 151936,
+                    copy_frac: float = 0.5, span: Tuple[int, int] = (8, 64), name: Optional[str] = None) -> Histories:
+    """Histories in which text repeats, as in the workloads the n-gram drafter is meant for (output
+    that quotes its prompt, code that repeats identifiers): each history grows in pieces, a piece
+    being either fresh uniform tokens or a copy of an earlier span (with probability copy_frac),
+    piece lengths uniform in `span`; lengths uniform in L. Inputs only."""
+    rng = substream(seed, "ngram_histories")
+    lens = rng.integers(L[0], L[1] + 1, size=B)
+    out = []
+    for b in range(B):
+        n = int(lens[b])
+        h = np.empty(n, dtype=np.int32)
+        pos = 0
+        while pos < n:
+            m = min(int(rng.integers(span[0], span[1] + 1)), n - pos)
+            if pos > m and rng.random() < copy_frac:
+                src = int(rng.integers(0, pos - m + 1))
+                h[pos:pos + m] = h[src:src + m]
+            else:
+                h[pos:pos + m] = rng.integers(0, V, size=m, dtype=np.int32)
+            pos += m
+        out.append(h)
+    cu = np.zeros(B + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lens)
+    tokens = np.concatenate(out) if B else np.zeros(0, dtype=np.int32)
+    return Histories(name=name or f"ngram_histories_B{B}_L{L[0]}to{L[1]}_V{V}", tokens=tokens, cu_hist=cu, V=V)

@@ -653,6 +653,9 @@ def check_bitmask_scatter(seed=91):
     assert out[:, 0].tolist() == [106, 107, 100, 101, 102]        # request 0 after 1's two listings
     out = bitmask_ref.bitmask_scatter(comp[:4], [1, 0], cu, 2, 20)
     assert out[:, 0].tolist() == [103, 0, 100, 101, 102]          # request 0's second row is past the end
+    cu_bad = np.array([0, 3, 2, 4], dtype=np.int32)               # request 1 has decreasing offsets:
+    out = bitmask_ref.bitmask_scatter(comp, [1, 0, 2], cu_bad, 3, 20)   # it owns no rows
+    assert out[:, 0].tolist() == [100, 101, 102, 103, 104, 105, 106]
 
 
 ALL_PINS = [

@@ -95,11 +95,11 @@ def _call(lib, **over):
     # CUDA call, so nothing is dereferenced
     a = dict(logits=4096, dtype=0, ids=4096, q=None, has_q=None, cu=4096, B=4, V=1000, max_k=3, mask=None,
              temp=4096, u=4096, noise=4096, out=4096, acc=4096, ctr=4096, status=None, da=None, dr=None,
-             ws=None, ws_bytes=0)
+             tm=None, ws=None, ws_bytes=0)
     a.update(over)
     return lib.specdec_verify(a["logits"], a["dtype"], a["ids"], a["q"], a["has_q"], a["cu"], a["B"], a["V"],
                               a["max_k"], a["mask"], a["temp"], a["u"], a["noise"], a["out"], a["acc"],
-                              a["ctr"], a["status"], a["da"], a["dr"], a["ws"], a["ws_bytes"], None)
+                              a["ctr"], a["status"], a["da"], a["dr"], a["tm"], a["ws"], a["ws_bytes"], None)
 
 
 def test_host_validation(lib, monkeypatch):
@@ -118,6 +118,7 @@ def test_host_validation(lib, monkeypatch):
     assert _call(lib, dtype=1, logits=4098, B=0) == E.SPECDEC_OK  # bf16 needs 2-byte alignment only
     assert _call(lib, ctr=4100) == E.SPECDEC_ERR_INVALID_ARG      # counters need 8-byte alignment
     assert _call(lib, mask=4097) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, tm=4100) == E.SPECDEC_ERR_INVALID_ARG        # telemetry needs 8-byte alignment
     assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
 
 
@@ -152,3 +153,36 @@ def test_missing_library_fails_loudly(tmp_path):
             _native.load(str(tmp_path / "nope.so"))
         finally:
             _native._lib = saved
+
+
+def test_ngram_host_validation(lib):
+    """specdec_ngram_propose rejects bad sizes before any CUDA call (fake aligned pointers)."""
+    E = _native
+    f = 4096
+    call = lambda **o: lib.specdec_ngram_propose(o.get("tok", f), o.get("cu", f), o.get("B", 4), o.get("min_n", 2),
+                                                 o.get("max_n", 4), o.get("k", 3), o.get("d", f), o.get("n", f),
+                                                 o.get("m", f), None)
+    assert call(B=0) == E.SPECDEC_OK
+    assert call(B=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(min_n=0) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(k=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(k=33) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(max_n=65) == E.SPECDEC_ERR_UNSUPPORTED
+    assert call(tok=None) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(cu=4100) == E.SPECDEC_ERR_INVALID_ARG          # int64 offsets need 8-byte alignment
+
+
+def test_bitmask_scatter_host_validation(lib):
+    """specdec_bitmask_scatter rejects bad sizes before any CUDA call (fake aligned pointers)."""
+    E = _native
+    f = 4096
+    call = lambda **o: lib.specdec_bitmask_scatter(o.get("c", f), o.get("rows", 10), o.get("ids", f), o.get("n", 3),
+                                                   o.get("cu", f), o.get("B", 4), o.get("V", 1000), o.get("out", f), None)
+    assert call(B=0) == E.SPECDEC_OK
+    assert call(B=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(V=0) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(n=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(rows=-1) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(out=None) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(ids=None) == E.SPECDEC_ERR_INVALID_ARG
+    assert call(c=4098) == E.SPECDEC_ERR_INVALID_ARG

@@ -262,6 +262,10 @@ def test_counters_accumulate_and_runs_are_deterministic(cuda, kernel):
     torch.cuda.synchronize()
     second = out.numpy()
     assert np.array_equal(second["counters"], 2 * first["counters"])
+    assert np.array_equal(second["telemetry"], 2 * first["telemetry"])
+    tm = first["telemetry"].astype(np.int64)
+    assert tm[0].sum() == first["counters"][0] and tm[1].sum() == first["counters"][2]
+    assert tm[2].sum() == first["counters"][3]
     for key in ("out_tokens", "out_num_accepted", "status"):
         assert np.array_equal(first[key], second[key])
     assert np.array_equal(first["diag_accept_prob"], second["diag_accept_prob"], equal_nan=True)

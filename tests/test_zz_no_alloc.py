@@ -23,10 +23,10 @@ def test_requests_beyond_the_scratch_are_refused(lib):
     f = 4096
     B = _native.NOALLOC_MAX_REQUESTS + 1
     rc = lib.specdec_verify_noalloc(f, 0, f, None, None, f, B, 1000, 3, None, f, f, f, f, f, f,
-                                    None, None, None, None)
+                                    None, None, None, None, None)
     assert rc == _native.SPECDEC_ERR_UNSUPPORTED
     rc0 = lib.specdec_verify_noalloc(f, 0, f, None, None, f, 0, 1000, 3, None, f, f, f, f, f, f,
-                                     None, None, None, None)
+                                     None, None, None, None, None)
     assert rc0 == _native.SPECDEC_OK                  # an empty batch needs no scratch
 
 
@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, monkeypatch):
             dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
             w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
             na_out.out_tokens, na_out.out_num_accepted, na_out.counters, na_out.status,
-            na_out.diag_accept_prob, na_out.diag_row_stats)
+            na_out.diag_accept_prob, na_out.diag_row_stats, telemetry=na_out.telemetry)
         torch.cuda.synchronize()
         na_calls.append(na_out.numpy())
 
@@ -73,7 +73,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, monkeypatch):
         for k in ("diag_accept_prob", "diag_row_stats"):
             assert np.array_equal(na_calls[i][k], ws_calls[i][k], equal_nan=True), (i, k)
         assert np.array_equal(na_calls[i]["counters"], ws_calls[i]["counters"]), i
+        assert np.array_equal(na_calls[i]["telemetry"], ws_calls[i]["telemetry"]), i
     assert np.array_equal(na_calls[1]["counters"], 2 * na_calls[0]["counters"])
+    assert np.array_equal(na_calls[1]["telemetry"], 2 * na_calls[0]["telemetry"])
 
     ref = oracle.verify(w)
     rep = parity.compare(w, na_calls[0], ref)
