@@ -49,6 +49,7 @@ class _Diag(ctypes.Structure):
         ("emit_top2", ctypes.c_void_p),
         ("emit_scores", ctypes.c_void_p),
         ("score_request", ctypes.c_int32),
+        ("top_p_margin", ctypes.c_void_p),
         ("telemetry", ctypes.c_void_p),
     ]
 
@@ -71,6 +72,7 @@ def load(path: str = _LIB):
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                    ctypes.POINTER(_Diag)]
     ng = lib.specdec_ngram_ref
@@ -88,7 +90,7 @@ def _ptr(a: Optional[np.ndarray]):
 class OracleResult(dict):
     """out_tokens [T], out_num_accepted [B], counters [4] (R, I, D, A), status [B],
     alpha [N], row_m [T], row_S [T], emit_top1 [B], emit_top2 [B], emit_scores [V],
-    telemetry [4, 33] (see specdec_ref.h)."""
+    telemetry [4, 33], top_p_margin [T] (see specdec_ref.h)."""
 
     def __getattr__(self, k):
         try:
@@ -113,22 +115,25 @@ def verify(w, *, score_request: int = -1, counters: Optional[np.ndarray] = None,
     top2 = np.empty(B, dtype=np.float64)
     scores = np.empty(V, dtype=np.float64)
     telemetry = np.zeros(TELEMETRY_SHAPE, dtype=np.uint64)
+    margin = np.empty(T, dtype=np.float64)
     diag = _Diag(alpha.ctypes.data, row_m.ctypes.data, row_S.ctypes.data, top1.ctypes.data,
-                 top2.ctypes.data, scores.ctypes.data, int(score_request), telemetry.ctypes.data)
+                 top2.ctypes.data, scores.ctypes.data, int(score_request), margin.ctypes.data,
+                 telemetry.ctypes.data)
     logits = np.ascontiguousarray(w.logits)
     dtype = 1 if w.logits_dtype == "bf16" else 0
     args = [np.ascontiguousarray(a) if a is not None else None for a in
             (w.draft_ids, w.draft_probs, w.has_q, w.cu_num_draft, w.bitmask, w.temperature,
-             w.uniforms, w.exp_noise)]
+             w.uniforms, w.exp_noise, getattr(w, "top_k", None), getattr(w, "top_p", None))]
     rc = lib.specdec_verify_ref(
         _ptr(logits), dtype, _ptr(args[0]), _ptr(args[1]), _ptr(args[2]), _ptr(args[3]),
         B, V, int(w.max_k), _ptr(args[4]), _ptr(args[5]), _ptr(args[6]), _ptr(args[7]),
+        _ptr(args[8]), _ptr(args[9]),
         _ptr(out_tokens), _ptr(out_num), _ptr(ctr), _ptr(status), ctypes.byref(diag))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (rc={rc})")
     return OracleResult(out_tokens=out_tokens, out_num_accepted=out_num, counters=ctr, status=status,
                         alpha=alpha, row_m=row_m, row_S=row_S, emit_top1=top1, emit_top2=top2,
-                        emit_scores=scores, telemetry=telemetry)
+                        emit_scores=scores, telemetry=telemetry, top_p_margin=margin)
 
 
 def ngram_propose(histories, *, min_n: int = 2, max_n: int = 4, k: int = 3, lib_path: str = _LIB):

@@ -22,6 +22,7 @@ import numpy as np
 
 U_BAND = 1e-6
 MARGIN_BAND = 1e-6
+TOPP_BAND = 1e-6      # top-p: |mass above the boundary - top_p| (the kernel sums in fixed point)
 P_RTOL = 1e-5
 
 
@@ -94,6 +95,13 @@ def compare(w, gpu: dict, ref: dict, counters_before=(0, 0, 0, 0)) -> ParityRepo
                 t1, t2 = ref["emit_top1"][b], ref["emit_top2"][b]
                 if np.isfinite(t1) and t1 > 0 and (t1 - t2) / t1 < MARGIN_BAND:
                     cut = a_ref
+        # a row whose top-p boundary sits within floating-point reach of top_p (oracle's view)
+        tpm = ref.get("top_p_margin")
+        if tpm is not None and not greedy[b] and not (int(ref["status"][b]) & (8 | 16)):
+            for j in range(min(a_ref, k) + 1):
+                if np.isfinite(tpm[row0 + j]) and tpm[row0 + j] < TOPP_BAND and (cut is None or j < cut):
+                    cut = j
+                    break
         if cut is not None:
             rep.excluded_requests += 1
             rep.excluded_positions += k + 1 - cut

@@ -27,6 +27,7 @@ typedef struct {
     const int32_t* cu; int32_t B, V, max_k;
     const int32_t* bitmask; int32_t W;
     const float* temperature; const float* uniforms; const float* noise;
+    const int32_t* top_k; const float* top_p;
     int32_t* out_tokens; int32_t* out_num_accepted; uint64_t* counters; uint32_t* status;
     specdec_ref_diag* diag;
     double* z; double* p; double* w;   /* per-row scratch, V doubles each */
@@ -106,6 +107,63 @@ static void temperature_softmax(const ref_call* c, double T, double* m_out, doub
     for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;
     *m_out = m;
     *S_out = S;
+}
+
+/* Top-k / top-p on the masked, temperature-scaled target distribution p of a sampled row ("vLLM
+ * tour part 2", section "Verification: rejection sampling on the GPU": apply_sampling_constraints
+ * applies temperature and top-k/top-p to the flattened target tensor before acceptance).
+ * Readings (the page gives no more): top-k keeps every allowed id whose logit is at least the k-th
+ * largest allowed logit (ties at the boundary kept), k <= 0 keeps all; top-p then works on the
+ * top-k distribution renormalised and keeps every id whose mass of strictly larger logits is below
+ * top_p (the smallest top set reaching top_p, ties kept), top_p >= 1 keeps all. p is renormalised
+ * over the kept ids. Returns the margin min |mass above - top_p| over the two tie groups at the
+ * top-p boundary (+inf when top-p keeps all), for the parity exclusion band. */
+typedef struct { double z, p; } zp_pair;
+
+static int cmp_desc(const void* a, const void* b)
+{
+    const double x = ((const zp_pair*)a)->z, y = ((const zp_pair*)b)->z;
+    return (x < y) - (x > y);
+}
+
+static double sampling_filter(const ref_call* c, int32_t k, double tp)
+{
+    /* the allowed ids' (logit, probability) pairs in decreasing logit order */
+    int32_t m = 0;
+    for (int32_t i = 0; i < c->V; ++i) if (c->z[i] > -INFINITY) ++m;
+    zp_pair* a = (zp_pair*)malloc(sizeof(zp_pair) * (size_t)(m > 0 ? m : 1));
+    m = 0;
+    for (int32_t i = 0; i < c->V; ++i)
+        if (c->z[i] > -INFINITY) { a[m].z = c->z[i]; a[m].p = c->p[i]; ++m; }
+    qsort(a, (size_t)m, sizeof(zp_pair), cmp_desc);
+    double zk = -INFINITY;                                   /* top-k: keep z >= zk */
+    if (k > 0 && k < m) zk = a[k - 1].z;
+    double Mk = 0.0;                                         /* mass of the top-k set */
+    for (int32_t i = 0; i < m && a[i].z >= zk; ++i) Mk += a[i].p;
+    double zp = zk, margin = INFINITY;                       /* top-p: keep z >= zp */
+    if (tp < 1.0) {
+        double above = 0.0;                                  /* renormalised mass of larger logits */
+        int32_t g0 = 0;
+        while (g0 < m && a[g0].z >= zk) {                    /* tie groups, decreasing logit */
+            int32_t g1 = g0;
+            double gm = 0.0;
+            while (g1 < m && a[g1].z == a[g0].z) gm += a[g1++].p;
+            const double dist = fabs(above - tp);
+            if (dist < margin) margin = dist;
+            if (!(above < tp)) break;                        /* this group and all below are dropped */
+            zp = a[g0].z;
+            above += gm / Mk;
+            g0 = g1;
+        }
+    }
+    double S = 0.0;
+    for (int32_t i = 0; i < c->V; ++i) {
+        if (!(c->z[i] >= zp) || c->z[i] == -INFINITY) c->p[i] = 0.0;
+        S += c->p[i];
+    }
+    for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;
+    free(a);
+    return margin;
 }
 
 /* a7: probability of accepting draft x at draft slot d.
@@ -230,6 +288,15 @@ static void verify_request(ref_call* c, int32_t b)
     const int greedy = !(Tf > 0.0f) || !temperature_is_valid(Tf);
     const int qmode = (c->q != NULL) && (c->has_q == NULL || c->has_q[b] != 0);
     const double T = (double)Tf;
+    /* top-k / top-p of this request: k <= 0 and top_p >= 1 keep all; a top_p that is not a
+     * number in (0, 1] is flagged and keeps all */
+    const int32_t filter_k = c->top_k ? c->top_k[b] : 0;
+    double filter_p = 1.0;
+    if (c->top_p) {
+        const float tpf = c->top_p[b];
+        if (tpf > 0.0f && tpf < 1.0f) filter_p = (double)tpf;
+        else if (!(tpf >= 1.0f)) st |= REF_ST_BAD_TOP_P;
+    }
 
     int32_t a = k;            /* accepted length */
     int32_t emitted = -1;     /* token at position a */
@@ -268,6 +335,10 @@ static void verify_request(ref_call* c, int32_t b)
         temperature_softmax(c, T, &m, &S);
         if (c->diag && c->diag->row_m) c->diag->row_m[t] = m;
         if (c->diag && c->diag->row_S) c->diag->row_S[t] = S;
+        if (filter_k > 0 || filter_p < 1.0) {
+            const double margin = sampling_filter(c, filter_k, filter_p);
+            if (c->diag && c->diag->top_p_margin) c->diag->top_p_margin[t] = margin;
+        }
         if (is_bonus) {
             /* a10: the bonus token is an ordinary sample from p ("the bonus position is
              * sampled ... with the request's own sampler settings") */
@@ -311,8 +382,8 @@ int specdec_verify_ref(
     const int32_t* draft_ids, const float* draft_probs, const uint8_t* has_q,
     const int32_t* cu_num_draft, int32_t B, int32_t V, int32_t max_k,
     const int32_t* bitmask, const float* temperature, const float* uniforms,
-    const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted,
-    uint64_t* counters, uint32_t* status, specdec_ref_diag* diag)
+    const float* exp_noise, const int32_t* top_k, const float* top_p, int32_t* out_tokens,
+    int32_t* out_num_accepted, uint64_t* counters, uint32_t* status, specdec_ref_diag* diag)
 {
     if (B < 0 || V <= 0 || max_k < 0 || max_k > 32) return 1;
     if (logits_dtype != REF_LOGITS_F32 && logits_dtype != REF_LOGITS_BF16) return 1;
@@ -328,6 +399,7 @@ int specdec_verify_ref(
     c.cu = cu_num_draft; c.B = B; c.V = V; c.max_k = max_k;
     c.bitmask = bitmask; c.W = (V + 31) / 32;
     c.temperature = temperature; c.uniforms = uniforms; c.noise = exp_noise;
+    c.top_k = top_k; c.top_p = top_p;
     c.out_tokens = out_tokens; c.out_num_accepted = out_num_accepted;
     c.counters = counters; c.status = status; c.diag = diag;
     c.z = (double*)malloc(sizeof(double) * (size_t)V);
@@ -345,6 +417,7 @@ int specdec_verify_ref(
         if (diag->emit_top1) for (int32_t i = 0; i < B; ++i) diag->emit_top1[i] = NAN;
         if (diag->emit_top2) for (int32_t i = 0; i < B; ++i) diag->emit_top2[i] = NAN;
         if (diag->emit_scores) for (int32_t i = 0; i < V; ++i) diag->emit_scores[i] = NAN;
+        if (diag->top_p_margin) for (int64_t i = 0; i < T; ++i) diag->top_p_margin[i] = INFINITY;
     }
 
     for (int32_t b = 0; b < B; ++b) verify_request(&c, b);

@@ -22,6 +22,8 @@
  *   - a draft with no probabilities (n-gram / suffix) is a one-hot q: accept with
  *     probability p(x); on rejection the residual is p with x removed, renormalised
  *     ("5.2 Draft models and model-free methods", infra-guide, section 4.3);
+ *   - optional top-k / top-p on the target distribution before acceptance ("vLLM tour
+ *     part 2", section "Verification: rejection sampling on the GPU");
  *   - counters R (raw drafts), I (grammar-invalidated), D = R - I (eligible),
  *     A (accepted) ("Structured output speculative decoding acceptance",
  *     fanout.sh, section "Name the three counters").
@@ -48,7 +50,8 @@ enum {
     REF_ST_EMPTY_MASK_ROW = 2u,   /* a row that was read allows no token (or only -inf logits) */
     REF_ST_BAD_TEMPERATURE = 4u,  /* temperature not 0 and not a positive normal finite float */
     REF_ST_K_TOO_LARGE = 8u,      /* k_b > max_k: request skipped */
-    REF_ST_BAD_OFFSETS = 16u      /* cu not non-decreasing within [0, cu[B]]: request skipped */
+    REF_ST_BAD_OFFSETS = 16u,     /* cu not non-decreasing within [0, cu[B]]: request skipped */
+    REF_ST_BAD_TOP_P = 64u        /* top_p not a number in (0, 1]: no top-p filter */
 };
 
 /* Optional fp64 diagnostics (any pointer may be NULL). */
@@ -60,6 +63,8 @@ typedef struct {
     double* emit_top2;    /* [B]   runner-up score of that race (0 when it had one candidate), else NaN */
     double* emit_scores;  /* [V]   all race scores of request score_request (0 where w_i = 0), else NaN */
     int32_t score_request;/*       request whose race scores fill emit_scores (-1: none) */
+    double* top_p_margin; /* [T] or NULL: for rows a top-p filter was applied to, the distance of
+                           * the boundary tie groups' mass above from top_p; else +inf */
     uint64_t* telemetry;  /* [4][33] ADDED to, or NULL: per position j, row 0 counts drafts
                            * (j < k_b), row 1 grammar-eligible drafts (j < g_b), row 2 drafts
                            * accepted through position j (j < a_b); row 3 [a] counts requests
@@ -83,6 +88,8 @@ int specdec_verify_ref(
     const float* temperature,                          /* [B] */
     const float* uniforms,                             /* [T] */
     const float* exp_noise,                            /* [T, V] */
+    const int32_t* top_k,                              /* [B] or NULL: top-k per request (<= 0: off) */
+    const float* top_p,                                /* [B] or NULL: top-p per request (>= 1: off) */
     int32_t* out_tokens,                               /* [T] */
     int32_t* out_num_accepted,                         /* [B] */
     uint64_t* counters,                                /* [4] */

@@ -51,6 +51,7 @@ _TAGS = {
     "uniforms": 13,
     "exp_noise": 14,
     "ngram_histories": 15,
+    "top_k_top_p": 16,
 }
 
 _ROW_BLOCK = 64  # rows generated per block (one substream each) for the [T, V] tensors
@@ -140,6 +141,8 @@ class Workload:
     uniforms: np.ndarray                 # [T] float32
     exp_noise: np.ndarray                # [T, V] float32
     description: str = ""
+    top_k: Optional[np.ndarray] = None   # [B] int32 or None (<= 0: no top-k)
+    top_p: Optional[np.ndarray] = None   # [B] float32 or None (>= 1: no top-p)
 
     @property
     def N(self) -> int:
@@ -199,6 +202,8 @@ class Workload:
             uniforms=np.ascontiguousarray(self.uniforms[rows]),
             exp_noise=np.ascontiguousarray(self.exp_noise[rows]),
             description=self.description,
+            top_k=None if self.top_k is None else np.ascontiguousarray(self.top_k[sel]),
+            top_p=None if self.top_p is None else np.ascontiguousarray(self.top_p[sel]),
         )
 
 
@@ -249,6 +254,8 @@ def make_batch(
     mask_run_frac: float = 0.8,
     forced_invalid_frac: float = 0.0,     # masked requests: share of drafts set to a disallowed id
     description: str = "",
+    top_k=None,                           # None, an int for every request, or an int array [B]
+    top_p=None,                           # None, a float for every request, or a float array [B]
 ) -> Workload:
     """Build one seeded batch. Parameters follow the workload recipes of the pages' configs."""
     # ---- ragged draft counts
@@ -415,11 +422,13 @@ def make_batch(
     has_q = None
     if q_any and not has_q_req.all():
         has_q = has_q_req.astype(np.uint8)
+    tk = None if top_k is None else np.broadcast_to(np.asarray(top_k, dtype=np.int32), (B,)).copy()
+    tp = None if top_p is None else np.broadcast_to(np.asarray(top_p, dtype=np.float32), (B,)).copy()
     return Workload(
         name=name, B=B, V=V, max_k=int(max_k), logits_dtype=logits_dtype, logits=logits,
         draft_ids=draft_ids, draft_probs=draft_probs, has_q=has_q,
         cu_num_draft=cu.astype(np.int32), bitmask=bitmask, temperature=temps,
-        uniforms=uniforms, exp_noise=exp_noise, description=description,
+        uniforms=uniforms, exp_noise=exp_noise, description=description, top_k=tk, top_p=tp,
     )
 
 
@@ -517,3 +526,16 @@ def ngram_histories(seed: int, B: int = 1024, L: Tuple[int, int] = (1024, 8192),
     cu[1:] = np.cumsum(lens)
     tokens = np.concatenate(out) if B else np.zeros(0, dtype=np.int32)
     return Histories(name=name or f"ngram_histories_B{B}_L{L[0]}to{L[1]}_V{V}", tokens=tokens, cu_hist=cu, V=V)
+
+
+def top_k_top_p_batch(seed: int = 5, B: int = 256, V: int = 128256) -> Workload:
+    """The random draft-model batch (B=256, k=4, V=128256, fp32, T ~ U[0.5, 1.2]) with per-request
+    top-k in {off, 20, 50, 200} and top-p in {off, 0.8, 0.9, 0.95}, drawn independently (the
+    drafter's q is not filtered). Inputs only."""
+    rng = substream(seed, "top_k_top_p")
+    tk = rng.choice(np.array([0, 20, 50, 200], dtype=np.int32), size=B)
+    tp = rng.choice(np.array([1.0, 0.8, 0.9, 0.95], dtype=np.float32), size=B)
+    return make_batch(seed, name=f"random_draft_model_topk_topp_B{B}_k4_V{V}_f32", B=B, V=V, k=4,
+                      logit_sigma=3.0, temperature="uniform(0.5,1.2)", q_mode="all", draft_sigma=0.5,
+                      top_k=tk, top_p=tp,
+                      description="random draft-model batch with per-request top-k / top-p")

@@ -658,10 +658,97 @@ def check_bitmask_scatter(seed=91):
     assert out[:, 0].tolist() == [100, 101, 102, 103, 104, 105, 106]
 
 
+# ---------------------------------------------------------------------------------------------
+# top-k / top-p on the target distribution ("vLLM tour part 2", section "Verification: rejection
+# sampling on the GPU": temperature and top-k/top-p are applied before acceptance)
+# ---------------------------------------------------------------------------------------------
+
+def _filtered_p(z, T, k, tp, allowed=None):
+    """The filtered target distribution by an all-pairs restatement (numpy broadcasting, no sort):
+    top-k keeps ids with at least k-1 ... fewer than k allowed ids strictly above; top-p keeps ids
+    whose (top-k renormalised) mass of strictly larger logits is below tp."""
+    s = z.astype(np.float64) / T
+    if allowed is not None:
+        s = np.where(allowed, s, -np.inf)
+    live = np.isfinite(s)
+    p = np.where(live, np.exp(s - s[live].max()), 0.0)
+    p /= p.sum()
+    above = (s[None, :] > s[:, None]) & live[None, :]          # above[i, j]: j strictly larger than i
+    keep = live.copy()
+    if k > 0:
+        keep &= above.sum(axis=1) < k                           # fewer than k allowed ids above
+    pk = np.where(keep, p, 0.0)
+    pk /= pk.sum()
+    if tp < 1.0:
+        keep &= (above * pk[None, :]).sum(axis=1) < tp
+    out = np.where(keep, p, 0.0)
+    return out / out.sum()
+
+
+def check_top_k_top_p(lib_path=None, n=400_000, seed=101):
+    kw = {} if lib_path is None else {"lib_path": lib_path}
+    rng = np.random.default_rng(seed)
+    # (1) acceptance probabilities of single-draft requests against the restatement, V <= 24,
+    #     every combination of top-k and top-p, with ties among the logits
+    for trial in range(300):
+        V = int(rng.integers(2, 25))
+        z = rng.integers(-3, 4, size=(2, V)).astype(np.float32) * 0.5        # many ties
+        T = float(rng.choice([0.6, 1.0, 1.7]))
+        k = int(rng.choice([0, 1, 2, 3, V, V + 5]))
+        tp = float(rng.choice([1.0, 0.95, 0.7, 0.4, 1e-4]))
+        q = rng.random(V) + 0.05
+        q /= q.sum()
+        x = int(rng.integers(0, V))
+        allowed = rng.random((2, V)) < 0.8
+        allowed[:, x] = True
+        w = batch(V=V, ks=[1], logits=z, draft_ids=[x], temperature=T, q=q[None, :].astype(np.float32),
+                  allowed=allowed, seed=trial)
+        w = dataclasses.replace(w, top_k=np.array([k], np.int32), top_p=np.array([tp], np.float32))
+        r = oracle.verify(w, **kw)
+        pf = _filtered_p(z[0], float(np.float32(T)), k, np.float32(tp), allowed[0])
+        qx = float(np.float32(q[x]))
+        want = 0.0 if pf[x] == 0 else min(1.0, pf[x] / qx)
+        assert abs(r.alpha[0] - want) <= 1e-12 * max(1.0, want), (trial, r.alpha[0], want, k, tp)
+    # (2) no filter when k covers every allowed id and top_p = 1: identical outputs
+    w0 = W.make_batch(seed, B=40, V=200, k=(0, 4), logit_sigma=2.0, temperature="half_greedy(0.5,1.2)",
+                      q_mode="half", draft_sigma=0.4, mask="half", mask_density=0.3, mask_run_len=4)
+    r0 = oracle.verify(w0, **kw)
+    for tk, tpv in ((200, 1.0), (0, 1.0), (10_000, 1.5)):
+        r1 = oracle.verify(dataclasses.replace(w0, top_k=np.full(40, tk, np.int32), top_p=np.full(40, tpv, np.float32)), **kw)
+        assert np.array_equal(r1.out_tokens, r0.out_tokens) and np.array_equal(r1.counters, r0.counters)
+    # (3) a top_p that is not a number in (0, 1]: flagged, no top-p filter
+    for bad in (0.0, -0.5, float("nan")):
+        r1 = oracle.verify(dataclasses.replace(w0, top_p=np.full(40, bad, np.float32)), **kw)
+        assert ((r1.status & 64) != 0).all()
+        assert np.array_equal(r1.out_tokens, r0.out_tokens)
+    # (4) losslessness on the filtered distribution: first emitted token ~ p' (chi-square, V = 8)
+    V = 8
+    z0 = np.array([1.5, -0.5, 0.3, 2.2, -1.0, 0.0, 1.1, -2.0])
+    z1 = np.array([-0.2, 0.9, 1.7, -1.3, 0.4, 2.0, -0.7, 0.1])
+    q0 = np.array([0.05, 0.20, 0.10, 0.05, 0.25, 0.05, 0.10, 0.20])
+    results = {}
+    for name, k, tp, mode, zz, T in (("topk3_q", 3, 1.0, "q", np.stack([z0, z1]), 1.0),
+                                      ("topp0.7_q", 0, 0.7, "q", np.stack([z0, z1]), 1.0),
+                                      ("topk4_topp0.8_model_free", 4, 0.8, "mf", np.stack([z0, z1]), 0.8),
+                                      ("topk5_bonus_only", 5, 1.0, "mf", z1[None, :], 1.3)):
+        w = _chi2_batch(n, zz, T, mode, q_rows=q0[None, :], x_fixed=[3] if zz.shape[0] > 1 else [], seed=seed + len(results))
+        w = dataclasses.replace(w, top_k=np.full(n, k, np.int32), top_p=np.full(n, tp, np.float32))
+        r = oracle.verify(w, **kw)
+        first = r.out_tokens[0::zz.shape[0]]
+        pf = _filtered_p(zz[0], float(np.float32(T)), k, np.float32(tp))
+        support = pf > 0
+        assert not np.bincount(first, minlength=V)[~support].any()      # nothing outside the kept set
+        results[name] = _chi2(np.bincount(first, minlength=V)[support], pf[support])
+    bad = {nm: v for nm, v in results.items() if not v[0] < stats.chi2.ppf(0.999, v[1])}
+    assert not bad, f"chi-square failures: {bad} (all: {results})"
+    return results
+
+
 ALL_PINS = [
     check_worked_counter_example,
     check_telemetry,
     check_ngram_proposer,
+    check_top_k_top_p,
     check_strict_accept_comparison,
     check_edge_cases,
     check_residual_excludes_draft,

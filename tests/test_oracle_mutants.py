@@ -35,7 +35,7 @@ MUTANTS = {
                                          "if (!ok || !grammar_allows(c, row0 + j, x)) g = j;"),
     "bonus_row_skipped": ("for (int32_t j = 0; j <= k; ++j) {\n        const int64_t t = row0 + j;",
                           "for (int32_t j = 0; j < k; ++j) {\n        const int64_t t = row0 + j;"),
-    "softmax_not_normalised": ("for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;", "(void)0;"),
+    "softmax_not_normalised": ("for (int32_t i = 0; i < c->V; ++i) c->p[i] /= S;\n    *m_out = m;", "*m_out = m;"),
     "empty_row_not_flagged": ("if (live == 0) {", "if (live < 0) {"),
     "model_free_alpha_is_one": ("if (!qmode) return px;", "if (!qmode) return 1.0;"),
     "telemetry_accepted_through_stop_row": ("for (int32_t j = 0; j < a; ++j) tm[2 * 33 + j] += 1;",
@@ -49,6 +49,10 @@ MUTANTS = {
                            "for (int64_t start = 0; start < L - n; ++start) {\n                int64_t i = 0;\n                while (i < n && h[start + i] == tail[i]) ++i;\n                if (i == n) { hit_n = (int32_t)n; hit_start = start; }"),
     "ngram_short_windows_first": ("for (int64_t n = n_hi; n >= min_n && hit_n == 0; --n) {",
                                   "for (int64_t n = min_n; n <= n_hi && hit_n == 0; ++n) {"),
+    "filter_drops_boundary_group": ("if (!(c->z[i] >= zp) || c->z[i] == -INFINITY) c->p[i] = 0.0;",
+                                    "if (!(c->z[i] > zp) || c->z[i] == -INFINITY) c->p[i] = 0.0;"),
+    "top_p_mass_not_renormalised": ("above += gm / Mk;", "above += gm;"),
+    "top_k_off_by_one": ("if (k > 0 && k < m) zk = a[k - 1].z;", "if (k > 0 && k < m) zk = a[k].z;"),
     "no_stop_at_rejection": ("        a = j;\n        emitted = exponential_race(c, t, b);\n        break;",
                              "        a = j;\n        emitted = exponential_race(c, t, b);\n        c->out_tokens[t] = emitted;\n        continue;"),
 }
@@ -72,6 +76,7 @@ def _run_pins(lib):
         ("worked_counter_example", lambda: _pins.check_worked_counter_example(lib)),
         ("telemetry", lambda: _pins.check_telemetry(lib)),
         ("ngram", lambda: _pins.check_ngram_proposer(lib)),
+        ("top_k_top_p", lambda: _pins.check_top_k_top_p(lib, n=100_000)),
         ("strict_accept_comparison", lambda: _pins.check_strict_accept_comparison(lib)),
         ("edge_cases", lambda: _pins.check_edge_cases(lib)),
         ("residual_excludes_draft", lambda: _pins.check_residual_excludes_draft(lib)),

@@ -52,3 +52,8 @@ def test_ngram_proposer():
 
 def test_bitmask_scatter():
     _pins.check_bitmask_scatter()
+
+
+def test_top_k_top_p():
+    res = _pins.check_top_k_top_p()
+    assert len(res) == 4
