@@ -59,6 +59,8 @@ def parse():
                     help="time the n-gram proposer (model-free drafter) instead of the verify")
     ap.add_argument("--scatter", action="store_true",
                     help="time the bitmask scatter (compact scheduler-order masks -> batch rows) instead")
+    ap.add_argument("--filters", action="store_true",
+                    help="verify the random draft-model batch with per-request top-k / top-p instead")
     ap.add_argument("--requests", type=int, default=0,
                     help="verify only the first N requests of the workload (profiler captures); 0 = all")
     return ap.parse_args()
@@ -86,10 +88,11 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload_for(cfg: int, rank: int, requests: int = 0) -> W.Workload:
+def workload_for(cfg: int, rank: int, requests: int = 0, filters: bool = False) -> W.Workload:
     # rank 0 verifies the recipe's own seeded batch; other ranks verify independent batches;
-    # requests > 0 keeps the first `requests` requests (smaller cases for profiler captures)
-    w = W.config(cfg, seed=cfg + 1000 * rank)
+    # requests > 0 keeps the first `requests` requests (smaller cases for profiler captures);
+    # filters: the random draft-model batch with per-request top-k / top-p
+    w = W.top_k_top_p_batch(5 + 1000 * rank) if filters else W.config(cfg, seed=cfg + 1000 * rank)
     if 0 < requests < w.B:
         w = w.subset(range(requests), name=f"{w.name}_first{requests}")
     return w
@@ -261,7 +264,7 @@ def run_reference(args, world, rank):
         return
     import oracle
 
-    w = workload_for(args.config, 0, args.requests)
+    w = workload_for(args.config, 0, args.requests, args.filters)
     oracle.load()
     budget_total = 150.0
     per_step = max(0.05, min(5.0, budget_total / max(1, args.steps + args.warmup)))
@@ -478,7 +481,7 @@ def main():
         pg.barrier()
     _native.load()
 
-    w = workload_for(args.config, rank, args.requests)
+    w = workload_for(args.config, rank, args.requests, args.filters)
     host = device.host_tensors(w)
     dev_in = device.device_tensors(w, dev, host)
     out = device.alloc_outputs(w, dev, diag=False, telemetry=True)   # per-position counts, every step
@@ -495,6 +498,8 @@ def main():
         device.verify(w, dev_in, out, stream=stream)
     torch.cuda.synchronize()
     out.counters.zero_()
+    if out.telemetry is not None:
+        out.telemetry.zero_()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if pg:

@@ -62,6 +62,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
 #define SPECDEC_ST_K_TOO_LARGE     8u   /* k_b > max_k: skipped, -1 in its rows, no counters */
 #define SPECDEC_ST_BAD_OFFSETS    16u   /* cu[0] != 0 or cu[b] > cu[b+1] or cu[b+1] > cu[B]: skipped */
 #define SPECDEC_ST_DEVICE_TIMEOUT 32u   /* an on-chip copy did not land within its time limit */
+#define SPECDEC_ST_BAD_TOP_P      64u   /* top_p not a number in (0, 1]: no top-p filter */
 
 /*
  * specdec_verify -- verify one batch (stream-ordered, asynchronous).
@@ -81,6 +82,20 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *   bitmask        [T, W] int32 or NULL (unconstrained). Bit (i & 31) of word i >> 5 is 1
  *                  when token i is allowed; bits at or above V are ignored.
  *   temperature    [B] fp32; 0 means greedy.
+ *   top_k          [B] int32 or NULL: top-k per request (<= 0: off). The target distribution of a
+ *                  sampled request keeps every allowed id whose logit is at least the k-th largest
+ *                  allowed logit (ties at the boundary kept) before acceptance, residual and bonus
+ *                  ("vLLM tour part 2", section "Verification: rejection sampling on the GPU":
+ *                  temperature and top-k/top-p are applied to the target tensor). Greedy requests
+ *                  ignore it (the argmax is always kept).
+ *   top_p          [B] fp32 or NULL: top-p per request (>= 1: off), applied after top-k: the kept
+ *                  ids are those whose (top-k renormalised) mass of strictly larger logits is
+ *                  below top_p (ties kept); p is renormalised over the kept ids. A value that is
+ *                  not a number in (0, 1] sets SPECDEC_ST_BAD_TOP_P and is ignored. With top_k or
+ *                  top_p given, the streaming kernel runs one CTA per request and each filtered
+ *                  row is streamed once more per 8-bit digit of the threshold search (2 digits per
+ *                  search for bf16 logits, 4 for fp32); the slice-resident cluster kernel
+ *                  (SPECDEC_KERNEL=cluster) does not support them (SPECDEC_ERR_UNSUPPORTED).
  *   uniforms       [T] fp32 in [0, 1); draft j of request b is accepted iff
  *                  uniforms[t(b,j)] < alpha (strict). Entries at bonus rows are unused.
  *   exp_noise      [T, V] fp32 Exp(1) samples > 0; the token drawn from weights w at row t
@@ -143,6 +158,8 @@ specdec_status_t specdec_verify(
     int32_t B, int32_t V, int32_t max_k,
     const int32_t* bitmask,
     const float* temperature,
+    const int32_t* top_k,
+    const float* top_p,
     const float* uniforms,
     const float* exp_noise,
     int32_t* out_tokens,
@@ -191,6 +208,8 @@ specdec_status_t specdec_verify_noalloc(
     int32_t B, int32_t V, int32_t max_k,
     const int32_t* bitmask,
     const float* temperature,
+    const int32_t* top_k,
+    const float* top_p,
     const float* uniforms,
     const float* exp_noise,
     int32_t* out_tokens,

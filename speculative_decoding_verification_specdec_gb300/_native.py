@@ -27,6 +27,7 @@ ST_BAD_TEMPERATURE = 4
 ST_K_TOO_LARGE = 8
 ST_BAD_OFFSETS = 16
 ST_DEVICE_TIMEOUT = 32
+ST_BAD_TOP_P = 64
 
 EXPORTED = ("specdec_verify", "specdec_verify_noalloc", "specdec_wait", "specdec_status_string",
             "specdec_launch_config", "specdec_workspace_size", "specdec_ngram_propose",
@@ -53,10 +54,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.specdec_verify.restype = ctypes.c_int
-    lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
+    lib.specdec_verify.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                    vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.specdec_verify_noalloc.restype = ctypes.c_int
-    lib.specdec_verify_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp,
+    lib.specdec_verify_noalloc.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp,
                                            vp, vp, vp, vp, vp, vp, vp, vp]
     lib.specdec_ngram_propose.restype = ctypes.c_int
     lib.specdec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
@@ -124,7 +125,7 @@ def _marshal(target_logits, logits_dtype, stream, tensors):
 def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int, max_k: int,
                    bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters,
                    status=None, diag_accept_prob=None, diag_row_stats=None, workspace=None, stream=None,
-                   logits_dtype=None, telemetry=None) -> None:
+                   logits_dtype=None, telemetry=None, top_k=None, top_p=None) -> None:
     """Queue one verify on `stream` (default: torch's current stream). Tensors are CUDA tensors
     (or raw device addresses as ints, with logits_dtype given); raises SpecdecError on a
     non-zero status."""
@@ -134,10 +135,10 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
         ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
         ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
         ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
-        ("telemetry", telemetry), ("workspace", workspace)))
+        ("telemetry", telemetry), ("workspace", workspace), ("top_k", top_k), ("top_p", top_p)))
     rc = load().specdec_verify(
         _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
-        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
+        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(top_k), _p(top_p), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
         _p(diag_row_stats), _p(telemetry), _p(workspace), 0 if workspace is None else _nbytes(workspace), stream)
     if rc != SPECDEC_OK:
@@ -147,7 +148,7 @@ def specdec_verify(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B
 def specdec_verify_noalloc(target_logits, draft_ids, draft_probs, has_q, cu_num_draft, B: int, V: int,
                            max_k: int, bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted,
                            counters, status=None, diag_accept_prob=None, diag_row_stats=None, stream=None,
-                           logits_dtype=None, telemetry=None) -> None:
+                           logits_dtype=None, telemetry=None, top_k=None, top_p=None) -> None:
     """specdec_verify with the library's own schedule scratch (no workspace argument)."""
     dt, stream = _marshal(target_logits, logits_dtype, stream, (
         ("target_logits", target_logits), ("draft_ids", draft_ids), ("draft_probs", draft_probs),
@@ -155,10 +156,10 @@ def specdec_verify_noalloc(target_logits, draft_ids, draft_probs, has_q, cu_num_
         ("temperature", temperature), ("uniforms", uniforms), ("exp_noise", exp_noise),
         ("out_tokens", out_tokens), ("out_num_accepted", out_num_accepted), ("counters", counters),
         ("status", status), ("diag_accept_prob", diag_accept_prob), ("diag_row_stats", diag_row_stats),
-        ("telemetry", telemetry)))
+        ("telemetry", telemetry), ("top_k", top_k), ("top_p", top_p)))
     rc = load().specdec_verify_noalloc(
         _p(target_logits), dt, _p(draft_ids), _p(draft_probs), _p(has_q), _p(cu_num_draft),
-        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(uniforms), _p(exp_noise),
+        int(B), int(V), int(max_k), _p(bitmask), _p(temperature), _p(top_k), _p(top_p), _p(uniforms), _p(exp_noise),
         _p(out_tokens), _p(out_num_accepted), _p(counters), _p(status), _p(diag_accept_prob),
         _p(diag_row_stats), _p(telemetry), stream)
     if rc != SPECDEC_OK:

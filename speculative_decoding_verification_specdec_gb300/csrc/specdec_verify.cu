@@ -91,6 +91,8 @@ struct Args {
     const int32_t* cu;
     const int32_t* bitmask;
     const float* temperature;
+    const int32_t* top_k;        // [B] or NULL: top-k per request (<= 0: off)
+    const float* top_p;          // [B] or NULL: top-p per request (>= 1: off)
     const float* uniforms;
     const float* noise;
     int32_t* out_tokens;
@@ -758,7 +760,8 @@ constexpr int kDataBytes = kRingBytes - kListBytes;
 constexpr int kGatherCap = kDataBytes / 16;    // logits groups per gather batch
 constexpr int kSegWords = 5120;                // mask words scanned per pass (20 per consumer thread)
 
-enum : int { kDecNextRow = 1, kDecDrawP = 2, kDecDrawQ = 3, kDecDrawOneHot = 4, kDecDone = 5 };
+enum : int { kDecNextRow = 1, kDecDrawP = 2, kDecDrawQ = 3, kDecDrawOneHot = 4, kDecDone = 5,
+              kDecRescan = 6 };   // stream the same row once more (a top-k / top-p digit pass)
 
 __host__ __device__ constexpr int ids_per_stage(int bytes_per_id)
 {
@@ -800,6 +803,16 @@ struct StreamShared {
     int32_t g, greedy, qmode, sparse, timed_out, dec_code;
     uint32_t st;
     float c;
+    // top-k / top-p threshold search: one 8-bit digit of the logit keys per pass
+    uint32_t fcnt[256];
+    unsigned long long fmass[256];       // fixed point, 2^40 = exp2(0)
+    uint32_t fkmin[256], fkmax[256];     // first pass: smallest / largest logit key per bin
+    uint32_t fsel_digit;                 // chosen digit (0xffffffff: none)
+    uint32_t fsel_pad;
+    unsigned long long fsel_cnt, fsel_mass;   // count / mass above the chosen digit (this level)
+    unsigned long long ftot_mass;             // mass of every element counted in this pass
+    int32_t fk;
+    float fp;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -880,6 +893,57 @@ __device__ __forceinline__ ReqShape request_shape(const Args& a, int b)
     r.row0 = (int64_t)d0 + b;
     r.skip = (a.cu[0] != 0 || d0 < 0 || d1 < d0 || d1 > ntot) ? 1 : (r.k > a.max_k ? 2 : 0);
     return r;
+}
+
+// Top-k / top-p of request b, read the same way by producer and consumers: k <= 0 and top_p >= 1
+// are off, a top_p that is not a number in (0, 1] is off (and flagged); greedy requests ignore both
+// (the argmax is always kept).
+struct Filter {
+    int k;
+    float p;
+    bool bad_p, on;
+};
+
+__device__ __forceinline__ bool request_greedy(const Args& a, int b)
+{
+    const float T = a.temperature[b];
+    const bool tvalid = (T == 0.f) || (T >= FLT_MIN && T <= FLT_MAX);
+    return !(T > 0.f) || !tvalid;
+}
+
+__device__ __forceinline__ Filter request_filter(const Args& a, int b)
+{
+    Filter f;
+    f.k = a.top_k ? a.top_k[b] : 0;
+    f.p = 1.f;
+    f.bad_p = false;
+    if (a.top_p) {
+        const float v = a.top_p[b];
+        if (v > 0.f && v < 1.f) f.p = v;
+        else if (!(v >= 1.f)) f.bad_p = true;
+    }
+    f.on = (f.k > 0 || f.p < 1.f) && !request_greedy(a, b);
+    return f;
+}
+
+// First-pass bin of an element by its mass e = exp2(z * c - MC) in (0, ~1]: 8 bins per halving
+// (exponent and 3 mantissa bits), from bin 8 (2^-30) to 255 (1); bin 0 holds everything below
+// 2^-30. Non-decreasing in e, hence in the logit: every element of a higher bin has a larger logit.
+__device__ __forceinline__ uint32_t mass_bin(float e)
+{
+    const uint32_t u = __float_as_uint(e);
+    const int ex = (int)(u >> 23);
+    if (ex < 97) return 0u;
+    const uint32_t d = (uint32_t)(ex - 97) * 8u + ((u >> 20) & 7u) + 8u;
+    return d > 255u ? 255u : d;
+}
+
+// Order-preserving 32-bit key of a logit (its fp32 bits): a larger logit has a larger key, and
+// equal logits have equal keys (-0 and +0 both map to the key of +0).
+__device__ __forceinline__ uint32_t logit_key(float z)
+{
+    const uint32_t u = z == 0.f ? 0u : __float_as_uint(z);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // Sparse or dense: a warp reads up to 32 mask words of the request's first row; the request
@@ -1206,7 +1270,9 @@ struct Producer {
     }
 };
 
-template <typename ET>
+// kFilt: the variant with the top-k / top-p threshold search (compiled separately so that the
+// search's code does not take registers from the variant every other batch runs)
+template <typename ET, bool kFilt>
 __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kernel(const Args a)
 {
     using G = Geom<ET>;
@@ -1255,6 +1321,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         }
         if (rs.skip == 0 && !sp) {
             Producer<ET> pr(a, sh, ring, lane, lo, hi);
+            // a filtered request streams its rows again for the threshold search, so nothing of
+            // the next row may sit in the ring before a row's decisions are all taken
+            const int spec_r = (kFilt && request_filter(a, b).on) ? 0 : spec;
             uint32_t dec_round = 0;
             int issued_next = 0;
             for (int j = 0; j <= rs.k; ++j) {
@@ -1262,12 +1331,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 for (int c = issued_next; c < nrow_chunks; ++c) pr.row_chunk(t, c);
                 issued_next = 0;
                 if (j < rs.k) {
-                    for (int c = 0; c < spec; ++c) pr.row_chunk(t + 1, c);
-                    issued_next = spec;
+                    for (int c = 0; c < spec_r; ++c) pr.row_chunk(t + 1, c);
+                    issued_next = spec_r;
                 }
                 if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
                 ++dec_round;
                 int code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                if constexpr (kFilt) {
+                    while (code == kDecRescan) {             // one more pass of a threshold search
+                        for (int c = 0; c < nrow_chunks; ++c) pr.row_chunk(t, c);
+                        if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
+                        ++dec_round;
+                        code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                    }
+                }
                 if (code == kDecNextRow) continue;
                 while (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot) {
                     const bool wq = (code == kDecDrawQ);
@@ -1316,6 +1393,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (!tvalid) st |= SPECDEC_ST_BAD_TEMPERATURE;
             }
             if (lane == 0) {
+                const Filter f = request_filter(a, b);
+                if (f.bad_p && rs.skip == 0) st |= SPECDEC_ST_BAD_TOP_P;
+                sh.fk = f.on ? f.k : 0;
+                sh.fp = f.on ? f.p : 1.f;
                 sh.g = g; sh.greedy = greedy; sh.qmode = qmode; sh.st = st; sh.sparse = sparse;
                 sh.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);   // log2(e) / T, once
             }
@@ -1326,6 +1407,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         const bool greedy = sh.greedy != 0, qmode = sh.qmode != 0, sparse = sh.sparse != 0;
         const float c = sh.c;
         const float T = a.temperature[b];
+        const int fk = sh.fk;
+        const float fp = sh.fp;
+        const bool filt = kFilt && (fk > 0 || fp < 1.f);          // a top-k / top-p request (sampled)
         uint32_t st = sh.st;
         const bool has_mask = a.bitmask != nullptr;
         uint32_t* list = reinterpret_cast<uint32_t*>(ring);
@@ -1506,7 +1590,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         };
         // Sparse draw pass over list[0, n) of row t: logits, noise and (q-mode) q of the listed
         // groups, gathered with cp.async in batches sized to the data region.
-        auto sparse_draw = [&](int64_t t, int64_t d, int x, int n, int code, Part& dp, float MC, float invS) {
+        auto sparse_draw = [&](int64_t t, int64_t d, int x, int n, int code, Part& dp, float MC, float invS, uint32_t kt) {
             const bool wq = (code == kDecDrawQ);
             const int per = 16 + 4 * VE + (wq ? 4 * VE : 0);
             const int cap = kDataBytes / per;
@@ -1552,6 +1636,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
                         for (int q = 0; q < VE; ++q) {
                             z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                            if (kt != 0u && logit_key(z[u * VE + q]) < kt) z[u * VE + q] = -INFINITY;
                             ids[u * VE + q] = in ? grp * VE + q : -1;
                         }
                     }
@@ -1566,9 +1651,243 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
 
+            // ---- top-k / top-p (sampled requests that ask for them): the threshold key kt of row t
+            // (kept ids: key >= kt) and the kept mass relative to MC, by an exact radix select over
+            // the allowed logits' order-preserving keys, one 8-bit digit per pass over the row
+            // (bf16 keys have 16 significant bits: 2 passes per search, fp32 4): element counts
+            // for top-k, masses exp2(z * c - MC) in 2^-40 fixed point (exact, order-independent
+            // sums) for top-p. Dense rows are streamed again through the ring; sparse rows reuse
+            // their gathered groups when the row's list fit one gather batch, else gather again.
+            constexpr int kLevels = (sizeof(ET) == 2) ? 2 : 4;
+            // The visitors call f(z, valid) for every element slot of the row in warp-converged
+            // code (all 32 lanes of a warp together; valid = an allowed id with a finite logit), so
+            // that f may use warp-wide intrinsics.
+            auto gather_and_visit = [&](int64_t t, int n, auto&& f) {
+                const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
+                const uint32_t dbase = smem_addr(ring + kDataOff);
+                const uint4* data = reinterpret_cast<const uint4*>(ring + kDataOff);
+                for (int b0 = 0; b0 < n; b0 += kGatherCap) {
+                    const int nb = min(kGatherCap, n - b0);
+                    for (int e = ct; e < nb; e += kConsumers)
+                        cp_async16(dbase + (uint32_t)e * 16u, lrow + (size_t)(list[b0 + e] >> 8) * 16u);
+                    cp_async_wait_all();
+                    consumer_sync();
+                    for (int e0 = ct - lane; e0 < nb; e0 += kConsumers) {      // warp-uniform trip count
+                        const int e = e0 + lane;
+                        const bool in = e < nb;
+                        float z[VE];
+                        unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
+                        const uint32_t bits = in ? (list[b0 + e] & 0xffu) : 0u;
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) f(z[q], ((bits >> q) & 1u) && z[q] > -INFINITY);
+                    }
+                    consumer_sync();
+                }
+            };
+            auto visit_row = [&](int64_t t, int j, auto&& f) {
+                if (!sparse) {
+                    post(kDecRescan);
+                    for (int ch = 0; ch < nrow_chunks; ++ch) {
+                        const int s = wait_full();
+                        const unsigned char* stg = ring + (size_t)s * kStageBytes;
+                        const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::kRowMaskOff);
+                        const int i0 = lo + ch * G::kRowIds;
+                        const int n = min(G::kRowIds, hi - i0);
+                        const int nvec = (n + VE - 1) / VE;
+                        for (int v0 = ct - lane; v0 < nvec; v0 += kConsumers) {     // warp-uniform trip count
+                            const int v = v0 + lane;
+                            const bool in = v < nvec;
+                            float z[VE];
+                            if (in) Elem<ET>::load(stg, v, z);
+                            else {
+#pragma unroll
+                                for (int e = 0; e < VE; ++e) z[e] = -INFINITY;
+                            }
+                            const uint32_t bits = in ? vec_bits<VE>(sm, has_mask, v) : 0u;
+#pragma unroll
+                            for (int e = 0; e < VE; ++e) f(z[e], ((bits >> e) & 1u) && z[e] > -INFINITY);
+                        }
+                        release(s);
+                    }
+                } else if (listed_row == j && listed_n <= kGatherCap) {
+                    // the row's groups are still in the data region, in list order
+                    const uint4* data = reinterpret_cast<const uint4*>(ring + kDataOff);
+                    for (int e0 = ct - lane; e0 < listed_n; e0 += kConsumers) {
+                        const int e = e0 + lane;
+                        const bool in = e < listed_n;
+                        float z[VE];
+                        unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
+                        const uint32_t bits = in ? (list[e] & 0xffu) : 0u;
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) f(z[q], ((bits >> q) & 1u) && z[q] > -INFINITY);
+                    }
+                } else if (listed_row == j) {
+                    gather_and_visit(t, listed_n, f);
+                } else {
+                    for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
+                        const int w1 = min(whi, w0 + kSegWords);
+                        const int n = build_list(t, w0, w1);
+                        if (n >= 0) {
+                            gather_and_visit(t, n, f);
+                        } else {
+                            for (int s0 = w0; s0 < w1; s0 += G::kSafeWords)
+                                gather_and_visit(t, build_list(t, s0, min(w1, s0 + G::kSafeWords)), f);
+                        }
+                    }
+                }
+            };
+            // one pass over the row. First pass (bin0 < 0): every element at or above floor_key, binned
+            // by its mass (mass_bin), with each bin's smallest and largest key. Later passes: the
+            // elements of first-pass bin bin0 whose key matches pval on the bits of pmask, binned by
+            // the key's bits [shift, shift + 8) (width bits). The lanes of a warp that fall into the
+            // same bin first combine their count, mass (as two 32-bit halves) and keys, so that one
+            // lane per bin and warp-step touches shared memory.
+            auto hist_pass = [&](int64_t t, int j, int bin0, uint32_t pmask, uint32_t pval, int shift, uint32_t width,
+                                 uint32_t floor_key, float MC) {
+                for (int i = ct; i < 256; i += kConsumers) {
+                    sh.fcnt[i] = 0u; sh.fmass[i] = 0ull; sh.fkmin[i] = 0xffffffffu; sh.fkmax[i] = 0u;
+                }
+                consumer_sync();
+                visit_row(t, j, [&](float z, bool valid) {
+                    const uint32_t key = logit_key(z);
+                    const float e = valid ? ex2(fmaf(z, c, -MC)) : 0.f;
+                    const uint32_t mb = mass_bin(e);
+                    uint32_t dg = 0xffffffffu;                          // not counted
+                    if (valid && key >= floor_key) {
+                        if (bin0 < 0) dg = mb;
+                        else if ((int)mb == bin0 && (key & pmask) == pval) dg = (key >> shift) & width;
+                    }
+                    const unsigned peers = __match_any_sync(0xffffffffu, dg);
+                    if (dg == 0xffffffffu) return;
+                    const unsigned long long m = __float2ull_rn(e * 1099511627776.f);   // < 2^41
+                    const uint32_t mhi = __reduce_add_sync(peers, (uint32_t)(m >> 20));
+                    const uint32_t mlo = __reduce_add_sync(peers, (uint32_t)(m & 0xfffffu));
+                    const uint32_t kmin = __reduce_min_sync(peers, key);
+                    const uint32_t kmax = __reduce_max_sync(peers, key);
+                    if (lane == __ffs(peers) - 1) {
+                        atomicAdd(&sh.fcnt[dg], (uint32_t)__popc(peers));
+                        atomicAdd(&sh.fmass[dg], ((unsigned long long)mhi << 20) + mlo);
+                        if (bin0 < 0) {
+                            atomicMin(&sh.fkmin[dg], kmin);
+                            atomicMax(&sh.fkmax[dg], kmax);
+                        }
+                    }
+                });
+                consumer_sync();
+            };
+            // digit choice by consumer warp 0: lane l holds digits 255 - 8l .. 248 - 8l (highest
+            // first); per-lane sums, an exclusive scan over lanes, then each lane walks its digits.
+            // mode 0 (top-k): the digit where the count from the top reaches `need`;
+            // mode 1 (top-p): the lowest non-empty digit whose mass above (plus `above`) is below P.
+            auto select_digit = [&](int mode, unsigned long long need, double P, unsigned long long above) {
+                if (cw == 0) {
+                    unsigned long long lc = 0ull, lm = 0ull;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) { lc += sh.fcnt[255 - 8 * lane - i]; lm += sh.fmass[255 - 8 * lane - i]; }
+                    unsigned long long ic = lc, im = lm;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, off);
+                        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
+                        if (lane >= off) { ic += yc; im += ym; }
+                    }
+                    const unsigned long long tot_m = __shfl_sync(0xffffffffu, im, 31);
+                    unsigned long long c0 = ic - lc, m0 = im - lm, fc = 0ull, fm = 0ull;
+                    int found = -1;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int dg = 255 - 8 * lane - i;
+                        const unsigned long long cn = sh.fcnt[dg], ms = sh.fmass[dg];
+                        if (mode == 0) {
+                            if (found < 0 && c0 + cn >= need) { found = dg; fc = c0; fm = m0; }
+                        } else if (cn != 0ull && (double)(above + m0) < P) {
+                            found = dg; fc = c0; fm = m0;
+                        }
+                        c0 += cn;
+                        m0 += ms;
+                    }
+                    const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
+                    // top-k: the first lane that reaches `need`; top-p: the last lane with a candidate
+                    const int src = who == 0u ? -1 : (mode == 0 ? __ffs(who) - 1 : 31 - __clz(who));
+                    if (lane == 0) { sh.fsel_digit = 0xffffffffu; sh.ftot_mass = tot_m; }
+                    __syncwarp();
+                    if (lane == src) { sh.fsel_digit = (uint32_t)found; sh.fsel_cnt = fc; sh.fsel_mass = fm; }
+                }
+                consumer_sync();
+            };
+            // the threshold key for one search: mode 0 (top-k: the `need`-th largest element) or
+            // mode 1 (top-p: the smallest key whose mass above is below P; P from the first pass when
+            // P < 0, as p_frac of the mass at or above floor_key). Returns the key, the count and
+            // mass above it (`cnt_above`, `mass_above`) and the mass of its own ties (`mass_at`);
+            // false when the search keeps every element (top-k with k >= the elements).
+            auto search = [&](int64_t t, int j, int mode, unsigned long long need, double p_frac, uint32_t floor_key,
+                              float MC, uint32_t& key_out, unsigned long long& mass_above, unsigned long long& mass_at) -> bool {
+                hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC);
+                double P = 0.0;
+                if (mode == 1) {
+                    select_digit(1, 0ull, -1.0, 0ull);               // totals only
+                    P = p_frac * (double)sh.ftot_mass;
+                }
+                select_digit(mode, need, P, 0ull);
+                const uint32_t b0 = sh.fsel_digit;
+                if (b0 == 0xffffffffu) {                             // top-k covers every element
+                    mass_above = sh.ftot_mass;
+                    mass_at = 0ull;
+                    return false;
+                }
+                unsigned long long above = sh.fsel_mass;
+                need -= sh.fsel_cnt;
+                uint32_t kmin = sh.fkmin[b0], kmax = sh.fkmax[b0];
+                unsigned long long at = sh.fmass[b0];
+                // resolve the keys of bin b0 from the highest bit where they differ, 8 bits a pass
+                uint32_t pmask = 0u, pval = 0u;
+                if (kmin != kmax) {
+                    const int hb = 31 - __clz(kmin ^ kmax);
+                    pmask = hb == 31 ? 0u : (0xffffffffu << (hb + 1));
+                    pval = kmin & pmask;
+                    for (int top = hb; top >= 0; top -= 8) {
+                        const int shift = max(0, top - 7);
+                        const uint32_t width = (top - shift == 7) ? 0xffu : ((1u << (top - shift + 1)) - 1u);
+                        hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC);
+                        select_digit(mode, need, P, above);
+                        const uint32_t dg = sh.fsel_digit;           // always found inside the bin
+                        above += sh.fsel_mass;
+                        need -= sh.fsel_cnt;
+                        pval |= dg << shift;
+                        pmask |= width << shift;
+                        at = sh.fmass[dg];
+                    }
+                    kmin = pval;
+                }
+                key_out = kmin;
+                mass_above = above;
+                mass_at = at;
+                return true;
+            };
+            auto filter_row = [&](int64_t t, int j, float MC, uint32_t& kt, float& S_keep) -> bool {
+                uint32_t floor_key = 0u;
+                unsigned long long keep = 0ull, above = 0ull, at = 0ull;
+                bool cut_k = false;
+                if (fk > 0) {
+                    uint32_t key;
+                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, key, above, at);
+                    if (cut_k) { floor_key = key; keep = above + at; }
+                }
+                bool cut_p = false;
+                if (fp < 1.f) {
+                    uint32_t key;
+                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, key, above, at);
+                    if (cut_p) { floor_key = key; keep = above + at; }
+                }
+                kt = floor_key;
+                S_keep = (float)((double)keep * (1.0 / 1099511627776.0));
+                return cut_k || cut_p;
+            };
+
             // ---- decision on row j from its reduced partial r (identical in every consumer thread
             // of every CTA of the request); returns the next code (a draw kind, next row, done)
-            auto decide = [&](int j, const Part& r, bool& stop, float& MC, float& S_mc) -> int {
+            auto decide = [&](int j, const Part& r, bool& stop, float& MC, float& S_mc, bool cut, uint32_t kt,
+                              float S_keep) -> int {
                 const int64_t t = rs.row0 + j;
                 const int64_t d = (int64_t)rs.d0 + j;
                 const bool bonus = (j == k);
@@ -1603,11 +1922,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     // S against MC = round(M*c), the reference the draw terms use
                     S_mc = fmaf(r.S, fmaf(r.m, c, -MC) * 0.69314718f, r.S);
                     if (writer && a.diag_row) { a.diag_row[2 * t] = r.m / T; a.diag_row[2 * t + 1] = r.S; }
+                    if (cut) S_mc = S_keep;                        // top-k / top-p: the kept ids' mass
                     code = kDecDrawP;
                     if (!bonus) {
                         float alpha = 0.f;
                         if (j < g) {
-                            const float px = (r.zx > -INFINITY) ? ex2_scaled(r.zx, c, MC) / S_mc : 0.f;
+                            const bool kept = r.zx > -INFINITY && (!cut || logit_key(r.zx) >= kt);
+                            const float px = kept ? ex2_scaled(r.zx, c, MC) / S_mc : 0.f;
                             if (qmode) {
                                 const float qx = sh.qxs[j];
                                 alpha = (px <= 0.f) ? 0.f : (qx <= px ? 1.f : px / qx);
@@ -1624,7 +1945,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             };
 
             // ---- a9/a10: draw pass(es) over the stop / bonus row j
-            auto draw_row = [&](int j, int code, float MC, float S_mc) {
+            auto draw_row = [&](int j, int code, float MC, float S_mc, uint32_t kt) {
                 const int64_t t = rs.row0 + j;
                 const int64_t d = (int64_t)rs.d0 + j;
                 const int x = (j == k) ? -1 : sh.xs[j];
@@ -1661,6 +1982,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 #pragma unroll
                                             for (int e = 0; e < VE; ++e) z[u * VE + e] = ((bits >> e) & 1u) ? z[u * VE + e] : -INFINITY;
                                         }
+                                        if (kt != 0u) {                  // top-k / top-p: ids below the threshold
+#pragma unroll
+                                            for (int e = 0; e < VE; ++e)
+                                                if (logit_key(z[u * VE + e]) < kt) z[u * VE + e] = -INFINITY;
+                                        }
 #pragma unroll
                                         for (int h = 0; h < VE / 4; ++h) {
                                             const float4 f = reinterpret_cast<const float4*>(se + e0)[h];
@@ -1684,16 +2010,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         }
                     } else {
                         if (listed_row == j) {
-                            sparse_draw(t, d, x, listed_n, code, dp, MC, invS);
+                            sparse_draw(t, d, x, listed_n, code, dp, MC, invS, kt);
                         } else {
                             for (int w0 = wlo; w0 < whi; w0 += kSegWords) {
                                 const int w1 = min(whi, w0 + kSegWords);
                                 const int n = build_list(t, w0, w1);
                                 if (n >= 0) {
-                                    sparse_draw(t, d, x, n, code, dp, MC, invS);
+                                    sparse_draw(t, d, x, n, code, dp, MC, invS, kt);
                                 } else {
                                     for (int s0 = w0; s0 < w1; s0 += G::kSafeWords)
-                                        sparse_draw(t, d, x, build_list(t, s0, min(w1, s0 + G::kSafeWords)), code, dp, MC, invS);
+                                        sparse_draw(t, d, x, build_list(t, s0, min(w1, s0 + G::kSafeWords)), code, dp, MC, invS, kt);
                                 }
                             }
                         }
@@ -1796,16 +2122,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 const Part r = reduce(p);
                 SPECDEC_STAMP(4);
 
+                uint32_t kt = 0u;
+                float S_keep = 0.f;
+                bool cut = false;
+                if constexpr (kFilt) cut = filt && r.m > -INFINITY && filter_row(t, j, r.m * c, kt, S_keep);
                 bool stop;
                 float MC, S_mc;
-                const int code = decide(j, r, stop, MC, S_mc);
+                const int code = decide(j, r, stop, MC, S_mc, cut, kt, S_keep);
                 post(code);
                 if (!stop) continue;
 
                 // drain the chunks of row j+1 the producer queued before this decision
-                if (!sparse && j < k)
+                if (!sparse && j < k && !filt)
                     for (int ch = 0; ch < spec; ++ch) release(wait_full());
-                draw_row(j, code, MC, S_mc);
+                draw_row(j, code, MC, S_mc, cut ? kt : 0u);
                 acc_len = j;
                 break;
             }
@@ -1888,6 +2218,9 @@ __device__ __forceinline__ int request_cost_key(const Args& a, int b)
     }
     constexpr float es = (float)sizeof(ET);
     float cost = (float)(rs.k + 1) * (greedy ? 0.6f : 0.35f);
+    // a top-k / top-p request streams each row once more per digit of each threshold search
+    const Filter f = request_filter(a, b);
+    if (f.on) cost *= 1.f + (float)(((f.k > 0) + (f.p < 1.f)) * (sizeof(ET) == 2 ? 2 : 4));
     if (!greedy) cost += 0.85f * (es + 4.f + (qmode ? 4.f : 0.f)) / es;
     if (sparse) cost *= 0.25f;
     return min(kSchedKeys - 1, (int)(cost * 16.f + 0.5f));
@@ -2057,10 +2390,15 @@ cudaError_t configure_kernel_once()
         if (err == cudaSuccess)
             err = cudaFuncSetAttribute(specdec_verify_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kRingBytes);
         if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kRingBytes);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(specdec_verify_stream_kernel<ET, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     });
     return err;
 }
@@ -2092,7 +2430,9 @@ template <typename ET>
 specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream, bool after_schedule)
 {
     if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
-    void (*kernel)(Args) = sh.stream ? specdec_verify_stream_kernel<ET> : specdec_verify_kernel<ET>;
+    void (*kernel)(Args) = !sh.stream ? specdec_verify_kernel<ET>
+                           : (args.top_k || args.top_p) ? specdec_verify_stream_kernel<ET, true>
+                                                        : specdec_verify_stream_kernel<ET, false>;
     if (sh.G > 1) {
         // the cluster size actually used, cached per (kernel, G, smem) request
         static std::mutex mu;
@@ -2235,10 +2575,10 @@ extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_
 extern "C" specdec_status_t specdec_verify(
     const void* target_logits, specdec_dtype_t logits_dtype, const int32_t* draft_ids,
     const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
-    int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
-    const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
-    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, unsigned long long* telemetry,
-    void* workspace, size_t workspace_bytes, void* stream)
+    int32_t max_k, const int32_t* bitmask, const float* temperature, const int32_t* top_k, const float* top_p,
+    const float* uniforms, const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted,
+    unsigned long long* counters, uint32_t* status, float* diag_accept_prob, float* diag_row_stats,
+    unsigned long long* telemetry, void* workspace, size_t workspace_bytes, void* stream)
 {
     if (logits_dtype != SPECDEC_F32 && logits_dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     if (B < 0 || V < 1 || max_k < 0 || max_k > SPECDEC_KMAX) return SPECDEC_ERR_INVALID_ARG;
@@ -2251,11 +2591,18 @@ extern "C" specdec_status_t specdec_verify(
         !aligned(uniforms, 4) || !aligned(exp_noise, 4) || !aligned(out_tokens, 4) ||
         !aligned(out_num_accepted, 4) || !aligned(counters, 8) || (status && !aligned(status, 4)) ||
         (diag_accept_prob && !aligned(diag_accept_prob, 4)) || (diag_row_stats && !aligned(diag_row_stats, 4)) ||
-        (telemetry && !aligned(telemetry, 8)))
+        (telemetry && !aligned(telemetry, 8)) || (top_k && !aligned(top_k, 4)) || (top_p && !aligned(top_p, 4)))
         return SPECDEC_ERR_INVALID_ARG;
     LaunchShape shape;
     const specdec_status_t rc = shape_for(V, logits_dtype, B, &shape);
     if (rc != SPECDEC_OK) return rc;
+    if (top_k || top_p) {
+        // the threshold search reduces within one CTA: one CTA per request, streaming kernel only
+        if (!shape.stream) return SPECDEC_ERR_UNSUPPORTED;
+        const long long units = ((long long)V + kUnit - 1) / kUnit;
+        shape.G = 1;
+        shape.slice_units = (int)units;
+    }
     if (B == 0) return SPECDEC_OK;
     if ((long long)B * shape.G > INT_MAX) return SPECDEC_ERR_UNSUPPORTED;
 
@@ -2267,6 +2614,8 @@ extern "C" specdec_status_t specdec_verify(
     a.cu = cu_num_draft;
     a.bitmask = bitmask;
     a.temperature = temperature;
+    a.top_k = top_k;
+    a.top_p = top_p;
     a.uniforms = uniforms;
     a.noise = exp_noise;
     a.out_tokens = out_tokens;
@@ -2312,9 +2661,10 @@ extern "C" specdec_status_t specdec_verify(
 extern "C" specdec_status_t specdec_verify_noalloc(
     const void* target_logits, specdec_dtype_t logits_dtype, const int32_t* draft_ids,
     const float* draft_probs, const uint8_t* has_q, const int32_t* cu_num_draft, int32_t B, int32_t V,
-    int32_t max_k, const int32_t* bitmask, const float* temperature, const float* uniforms,
-    const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted, unsigned long long* counters,
-    uint32_t* status, float* diag_accept_prob, float* diag_row_stats, unsigned long long* telemetry, void* stream)
+    int32_t max_k, const int32_t* bitmask, const float* temperature, const int32_t* top_k, const float* top_p,
+    const float* uniforms, const float* exp_noise, int32_t* out_tokens, int32_t* out_num_accepted,
+    unsigned long long* counters, uint32_t* status, float* diag_accept_prob, float* diag_row_stats,
+    unsigned long long* telemetry, void* stream)
 {
     static_assert(kNoallocScratchBytes >= sizeof(int32_t) * SPECDEC_NOALLOC_MAX_REQUESTS + SPECDEC_NOALLOC_MAX_REQUESTS,
                   "scratch holds the order and the keys");
@@ -2330,8 +2680,9 @@ extern "C" specdec_status_t specdec_verify_noalloc(
         if (scratch == nullptr) return SPECDEC_ERR_CUDA;
     }
     return specdec_verify(target_logits, logits_dtype, draft_ids, draft_probs, has_q, cu_num_draft, B, V, max_k,
-                          bitmask, temperature, uniforms, exp_noise, out_tokens, out_num_accepted, counters, status,
-                          diag_accept_prob, diag_row_stats, telemetry, scratch, scratch ? kNoallocScratchBytes : 0, stream);
+                          bitmask, temperature, top_k, top_p, uniforms, exp_noise, out_tokens, out_num_accepted,
+                          counters, status, diag_accept_prob, diag_row_stats, telemetry, scratch,
+                          scratch ? kNoallocScratchBytes : 0, stream);
 }
 
 extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)

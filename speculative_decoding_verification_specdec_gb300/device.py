@@ -11,7 +11,7 @@ from . import _native
 from .workloads import BF16, Workload
 
 INPUT_FIELDS = ("logits", "draft_ids", "draft_probs", "has_q", "cu_num_draft", "bitmask", "temperature",
-                "uniforms", "exp_noise")
+                "uniforms", "exp_noise", "top_k", "top_p")
 
 
 def _host_tensor(a: np.ndarray, bf16: bool = False):
@@ -99,7 +99,7 @@ def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> No
         w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
         out.out_tokens, out.out_num_accepted, out.counters, out.status,
         out.diag_accept_prob, out.diag_row_stats, workspace=out.workspace, stream=stream,
-        telemetry=out.telemetry)
+        telemetry=out.telemetry, top_k=dev.get("top_k"), top_p=dev.get("top_p"))
 
 
 def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True) -> Dict[str, np.ndarray]:

@@ -95,10 +95,10 @@ def _call(lib, **over):
     # CUDA call, so nothing is dereferenced
     a = dict(logits=4096, dtype=0, ids=4096, q=None, has_q=None, cu=4096, B=4, V=1000, max_k=3, mask=None,
              temp=4096, u=4096, noise=4096, out=4096, acc=4096, ctr=4096, status=None, da=None, dr=None,
-             tm=None, ws=None, ws_bytes=0)
+             tm=None, ws=None, ws_bytes=0, tk=None, tp=None)
     a.update(over)
     return lib.specdec_verify(a["logits"], a["dtype"], a["ids"], a["q"], a["has_q"], a["cu"], a["B"], a["V"],
-                              a["max_k"], a["mask"], a["temp"], a["u"], a["noise"], a["out"], a["acc"],
+                              a["max_k"], a["mask"], a["temp"], a["tk"], a["tp"], a["u"], a["noise"], a["out"], a["acc"],
                               a["ctr"], a["status"], a["da"], a["dr"], a["tm"], a["ws"], a["ws_bytes"], None)
 
 
@@ -119,6 +119,8 @@ def test_host_validation(lib, monkeypatch):
     assert _call(lib, ctr=4100) == E.SPECDEC_ERR_INVALID_ARG      # counters need 8-byte alignment
     assert _call(lib, mask=4097) == E.SPECDEC_ERR_INVALID_ARG
     assert _call(lib, tm=4100) == E.SPECDEC_ERR_INVALID_ARG        # telemetry needs 8-byte alignment
+    assert _call(lib, tk=4098) == E.SPECDEC_ERR_INVALID_ARG
+    assert _call(lib, tk=4096) == E.SPECDEC_ERR_UNSUPPORTED        # cluster kernel: no top-k / top-p
     assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
 
 

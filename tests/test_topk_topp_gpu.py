@@ -1,0 +1,98 @@
+"""Top-k / top-p on the GPU against the oracle: mixed batches (fp32 and bf16, dense and sparse
+rows, greedy and sampled, draft-model and model-free), ties at the top-k boundary, filters that
+keep everything, and the bad-top_p flag."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import parity
+from speculative_decoding_verification_specdec_gb300 import _native, build, device
+from speculative_decoding_verification_specdec_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    import torch
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    if build.needs_rebuild():
+        build.build_library()
+    _native.load()
+    torch.cuda.set_device(0)
+    return "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def stream_kernel(monkeypatch):
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+
+
+def _check(w, cuda, workspace=True):
+    got = device.run(w, device=cuda, diag=True, workspace=workspace)
+    ref = oracle.verify(w)
+    rep = parity.compare(w, got, ref)
+    assert not (got["status"] & _native.ST_DEVICE_TIMEOUT).any()
+    assert rep.ok, (f"{w.name}: {rep.summary()} tokens={rep.token_mismatches[:8]} acc={rep.accepted_mismatches[:8]} "
+                    f"status={rep.status_mismatches[:8]} alpha={rep.alpha_bad[:5]}")
+    return rep, got, ref
+
+
+def _filters(B, seed, ks=(0, 1, 3, 20, 200), ps=(1.0, 0.5, 0.8, 0.95, 0.999)):
+    rng = np.random.default_rng(seed)
+    return rng.choice(np.array(ks, np.int32), size=B), rng.choice(np.array(ps, np.float32), size=B)
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+@pytest.mark.parametrize("mask", ["none", "half"])
+def test_mixed_batches(cuda, dtype, mask):
+    B = 96
+    tk, tp = _filters(B, 7 if dtype == W.F32 else 8)
+    w = W.make_batch(61, name=f"topkp_{dtype}_{mask}", B=B, V=5000, k=(0, 5), logits_dtype=dtype, logit_sigma=2.5,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.4, mf_argmax_frac=0.5,
+                     mask=mask, mask_density=0.1, mask_run_len=16, forced_invalid_frac=0.1, top_k=tk, top_p=tp)
+    rep, got, ref = _check(w, cuda)
+    assert rep.compared_tokens > 300
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_ties_at_the_boundary(cuda, dtype):
+    """Logits on a coarse grid (many ties): every tie group at a top-k or top-p boundary is kept."""
+    B, V = 120, 64
+    rng = np.random.default_rng(3)
+    tk, tp = _filters(B, 4, ks=(0, 1, 2, 5, 9), ps=(1.0, 0.3, 0.6, 0.9))
+    w = W.make_batch(62, name=f"topkp_ties_{dtype}", B=B, V=V, k=(1, 4), logits_dtype=dtype, logit_sigma=1.0,
+                     temperature="uniform(0.7,1.3)", q_mode="half", draft_sigma=0.5, top_k=tk, top_p=tp)
+    grid = np.round(W.bf16_bits_to_f32(w.logits) if dtype == W.BF16 else w.logits)
+    logits = W.f32_to_bf16_bits(grid.astype(np.float32)) if dtype == W.BF16 else grid.astype(np.float32)
+    w = dataclasses.replace(w, logits=np.ascontiguousarray(logits))
+    _check(w, cuda)
+
+
+def test_random_draft_model_batch_with_filters(cuda):
+    """The benchmark's filtered batch: B=256, k=4, V=128256, fp32, per-request top-k / top-p."""
+    _check(W.top_k_top_p_batch(), cuda)
+
+
+def test_filters_that_keep_everything_change_nothing(cuda):
+    w0 = W.make_batch(63, name="topkp_noop", B=48, V=3000, k=(0, 4), logit_sigma=2.0,
+                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.4, mask="half",
+                      mask_density=0.2, mask_run_len=8)
+    base = device.run(w0, device=cuda, diag=False)
+    for tk, tpv in ((0, 1.0), (3000, 1.0), (100000, 2.0)):
+        w = dataclasses.replace(w0, top_k=np.full(48, tk, np.int32), top_p=np.full(48, tpv, np.float32))
+        got = device.run(w, device=cuda, diag=False)
+        assert np.array_equal(got["out_tokens"], base["out_tokens"]), (tk, tpv)
+        assert np.array_equal(got["counters"], base["counters"])
+
+
+def test_bad_top_p_is_flagged(cuda):
+    w0 = W.make_batch(64, name="topkp_bad", B=16, V=1000, k=2, logit_sigma=2.0, temperature=1.0, q_mode="all",
+                      draft_sigma=0.4)
+    w = dataclasses.replace(w0, top_p=np.array([0.0, -1.0, np.nan, 0.5] * 4, np.float32))
+    rep, got, ref = _check(w, cuda)
+    flagged = (got["status"] & _native.ST_BAD_TOP_P) != 0
+    assert flagged.tolist() == [True, True, True, False] * 4

@@ -22,10 +22,10 @@ def test_requests_beyond_the_scratch_are_refused(lib):
     nothing is dereferenced, no device is needed)."""
     f = 4096
     B = _native.NOALLOC_MAX_REQUESTS + 1
-    rc = lib.specdec_verify_noalloc(f, 0, f, None, None, f, B, 1000, 3, None, f, f, f, f, f, f,
+    rc = lib.specdec_verify_noalloc(f, 0, f, None, None, f, B, 1000, 3, None, f, None, None, f, f, f, f, f,
                                     None, None, None, None, None)
     assert rc == _native.SPECDEC_ERR_UNSUPPORTED
-    rc0 = lib.specdec_verify_noalloc(f, 0, f, None, None, f, 0, 1000, 3, None, f, f, f, f, f, f,
+    rc0 = lib.specdec_verify_noalloc(f, 0, f, None, None, f, 0, 1000, 3, None, f, None, None, f, f, f, f, f,
                                      None, None, None, None, None)
     assert rc0 == _native.SPECDEC_OK                  # an empty batch needs no scratch
 
