@@ -92,10 +92,11 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  ids are those whose (top-k renormalised) mass of strictly larger logits is
  *                  below top_p (ties kept); p is renormalised over the kept ids. A value that is
  *                  not a number in (0, 1] sets SPECDEC_ST_BAD_TOP_P and is ignored. With top_k or
- *                  top_p given, the streaming kernel runs one CTA per request and each filtered
- *                  row is streamed once more per 8-bit digit of the threshold search (2 digits per
- *                  search for bf16 logits, 4 for fp32); the slice-resident cluster kernel
- *                  (SPECDEC_KERNEL=cluster) does not support them (SPECDEC_ERR_UNSUPPORTED).
+ *                  top_p given, the streaming kernel runs one CTA per request and each search
+ *                  (top-k, then top-p) streams a filtered row once more to bin its logits by mass,
+ *                  then once per 8-bit digit of the keys inside the chosen bin (at most 2 for bf16
+ *                  logits, 4 for fp32). V > 2^20, or the slice-resident cluster kernel
+ *                  (SPECDEC_KERNEL=cluster), with either of them: SPECDEC_ERR_UNSUPPORTED.
  *   uniforms       [T] fp32 in [0, 1); draft j of request b is accepted iff
  *                  uniforms[t(b,j)] < alpha (strict). Entries at bonus rows are unused.
  *   exp_noise      [T, V] fp32 Exp(1) samples > 0; the token drawn from weights w at row t
@@ -138,8 +139,9 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
  * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
  * pointer (draft_ids may be NULL), B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
- * element (telemetry: 8 bytes); SPECDEC_ERR_UNSUPPORTED for an unknown dtype (or, with the cluster kernel that
- * keeps each row slice on chip, a row wider than 3 MiB); SPECDEC_ERR_CUDA if the launch fails.
+ * element (telemetry: 8 bytes); SPECDEC_ERR_UNSUPPORTED for an unknown dtype, for top_k or top_p with V > 2^20
+ * (or with the cluster kernel), or, with the cluster kernel that keeps each row slice on chip, a row wider than
+ * 3 MiB; SPECDEC_ERR_CUDA if the launch fails.
  *
  * Kernels: by default each request is verified by a cluster of G CTAs (G = 1 for large
  * batches, up to 4 for small ones), each streaming its slice of every row through a ring of

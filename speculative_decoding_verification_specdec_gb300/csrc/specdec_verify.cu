@@ -803,14 +803,21 @@ struct StreamShared {
     int32_t g, greedy, qmode, sparse, timed_out, dec_code;
     uint32_t st;
     float c;
-    // top-k / top-p threshold search: one 8-bit digit of the logit keys per pass
+    // top-k / top-p threshold search: the 256 bins of one pass. Masses are sums of 24-bit
+    // integers kept as the sums of their low and high 12 bits (exact in 32 bits for V <= 2^20).
     uint32_t fcnt[256];
-    unsigned long long fmass[256];       // fixed point, 2^40 = exp2(0)
+    uint32_t flo[256], fhi[256];
     uint32_t fkmin[256], fkmax[256];     // first pass: smallest / largest logit key per bin
+    uint32_t ft_cnt[kConsumerWarps], ft_kmin[kConsumerWarps], ft_kmax[kConsumerWarps];   // tail, per warp
+    unsigned long long ft_m[kConsumerWarps];
+    unsigned long long ftail_m;          // first pass: tail mass in units of 2^-54
     uint32_t fsel_digit;                 // chosen digit (0xffffffff: none)
     uint32_t fsel_pad;
-    unsigned long long fsel_cnt, fsel_mass;   // count / mass above the chosen digit (this level)
-    unsigned long long ftot_mass;             // mass of every element counted in this pass
+    unsigned long long fsel_cnt;         // count above the chosen digit (this level)
+    double fsel_mass, fsel_at;           // mass above the chosen digit / of the digit itself
+    double ftot_mass;                    // mass of every element counted in this pass
+    double fsel_P;                       // the top-p target mass the choice used
+    uint32_t fsel_kmin, fsel_kmax;       // first pass: the chosen bin's smallest / largest key
     int32_t fk;
     float fp;
 };
@@ -927,8 +934,10 @@ __device__ __forceinline__ Filter request_filter(const Args& a, int b)
 }
 
 // First-pass bin of an element by its mass e = exp2(z * c - MC) in (0, ~1]: 8 bins per halving
-// (exponent and 3 mantissa bits), from bin 8 (2^-30) to 255 (1); bin 0 holds everything below
-// 2^-30. Non-decreasing in e, hence in the logit: every element of a higher bin has a larger logit.
+// (exponent and 3 mantissa bits), from bin 8 (2^-30) to 255 (1); bin 0 (the tail) holds
+// everything below 2^-30. Non-decreasing in e, hence in the logit: every element of a higher bin
+// has a larger logit. All elements of a bin from 8 up share e's binary exponent, so the bin's mass
+// is its elements' 24-bit significands summed exactly, times 2^(exponent - 23).
 __device__ __forceinline__ uint32_t mass_bin(float e)
 {
     const uint32_t u = __float_as_uint(e);
@@ -936,6 +945,20 @@ __device__ __forceinline__ uint32_t mass_bin(float e)
     if (ex < 97) return 0u;
     const uint32_t d = (uint32_t)(ex - 97) * 8u + ((u >> 20) & 7u) + 8u;
     return d > 255u ? 255u : d;
+}
+
+// The 24-bit significand of e (bins 8..255) or e in units of 2^-54 (the tail, e < 2^-30): an
+// integer below 2^24 whose sum over a bin, times bin_scale, is the bin's mass.
+__device__ __forceinline__ uint32_t mass_units(float e, bool tail)
+{
+    return tail ? __float2uint_rn(e * 0x1p54f) : ((__float_as_uint(e) & 0x7fffffu) | 0x800000u);
+}
+
+// 2^(exponent - 23) for the elements of mass bin mb (2^-54 for the tail)
+__device__ __forceinline__ double bin_scale(uint32_t mb)
+{
+    const int ex = mb == 0u ? -54 : (int)((mb - 8u) >> 3) + 97 - 150;
+    return __longlong_as_double((long long)(ex + 1023) << 52);
 }
 
 // Order-preserving 32-bit key of a logit (its fp32 bits): a larger logit has a larger key, and
@@ -1652,13 +1675,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
 
             // ---- top-k / top-p (sampled requests that ask for them): the threshold key kt of row t
-            // (kept ids: key >= kt) and the kept mass relative to MC, by an exact radix select over
-            // the allowed logits' order-preserving keys, one 8-bit digit per pass over the row
-            // (bf16 keys have 16 significant bits: 2 passes per search, fp32 4): element counts
-            // for top-k, masses exp2(z * c - MC) in 2^-40 fixed point (exact, order-independent
-            // sums) for top-p. Dense rows are streamed again through the ring; sparse rows reuse
-            // their gathered groups when the row's list fit one gather batch, else gather again.
-            constexpr int kLevels = (sizeof(ET) == 2) ? 2 : 4;
+            // (kept ids: key >= kt) and the kept mass relative to MC, by an exact radix select:
+            // a first pass bins the allowed logits by their mass exp2(z * c - MC), then passes over
+            // the elements of the chosen bin resolve their order-preserving keys 8 bits at a time
+            // (bf16 keys have 16 significant bits). Counts for top-k; masses for top-p as exact
+            // integer sums (the result does not depend on the order of the additions). Dense rows
+            // are streamed again through the ring; sparse rows reuse their gathered groups when the
+            // row's list fit one gather batch, else gather again.
             // The visitors call f(z, valid) for every element slot of the row in warp-converged
             // code (all 32 lanes of a warp together; valid = an allowed id with a finite logit), so
             // that f may use warp-wide intrinsics.
@@ -1736,127 +1759,177 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     }
                 }
             };
-            // one pass over the row. First pass (bin0 < 0): every element at or above floor_key, binned
-            // by its mass (mass_bin), with each bin's smallest and largest key. Later passes: the
-            // elements of first-pass bin bin0 whose key matches pval on the bits of pmask, binned by
-            // the key's bits [shift, shift + 8) (width bits). The lanes of a warp that fall into the
-            // same bin first combine their count, mass (as two 32-bit halves) and keys, so that one
-            // lane per bin and warp-step touches shared memory.
+            // one pass over the row into the 256 bins. First pass (bin0 < 0): every element at or above
+            // floor_key, by mass_bin, with each bin's smallest and largest key; the tail (bin 0), where
+            // most elements of a peaked row fall, is summed in registers and folded afterwards, so the
+            // shared-memory additions spread over the other bins. Later passes: the elements of mass
+            // bin bin0 whose key matches pval on the bits of pmask, by the key's bits [shift, shift +
+            // 8) (width). Integer sums only: the result does not depend on the order of the additions.
             auto hist_pass = [&](int64_t t, int j, int bin0, uint32_t pmask, uint32_t pval, int shift, uint32_t width,
-                                 uint32_t floor_key, float MC) {
+                                 uint32_t floor_key, float MC, uint32_t klo, uint32_t khi) {
                 for (int i = ct; i < 256; i += kConsumers) {
-                    sh.fcnt[i] = 0u; sh.fmass[i] = 0ull; sh.fkmin[i] = 0xffffffffu; sh.fkmax[i] = 0u;
+                    sh.fcnt[i] = 0u; sh.flo[i] = 0u; sh.fhi[i] = 0u; sh.fkmin[i] = 0xffffffffu; sh.fkmax[i] = 0u;
                 }
                 consumer_sync();
+                SPECDEC_STAMP(13);
+                uint32_t tcnt = 0u, tkmin = 0xffffffffu, tkmax = 0u;
+                unsigned long long tm = 0ull;
                 visit_row(t, j, [&](float z, bool valid) {
+                    if (!valid) return;
                     const uint32_t key = logit_key(z);
-                    const float e = valid ? ex2(fmaf(z, c, -MC)) : 0.f;
+                    if (key < floor_key || key < klo || key > khi || (key & pmask) != pval) return;
+                    const float e = ex2(fmaf(z, c, -MC));
                     const uint32_t mb = mass_bin(e);
-                    uint32_t dg = 0xffffffffu;                          // not counted
-                    if (valid && key >= floor_key) {
-                        if (bin0 < 0) dg = mb;
-                        else if ((int)mb == bin0 && (key & pmask) == pval) dg = (key >> shift) & width;
-                    }
-                    const unsigned peers = __match_any_sync(0xffffffffu, dg);
-                    if (dg == 0xffffffffu) return;
-                    const unsigned long long m = __float2ull_rn(e * 1099511627776.f);   // < 2^41
-                    const uint32_t mhi = __reduce_add_sync(peers, (uint32_t)(m >> 20));
-                    const uint32_t mlo = __reduce_add_sync(peers, (uint32_t)(m & 0xfffffu));
-                    const uint32_t kmin = __reduce_min_sync(peers, key);
-                    const uint32_t kmax = __reduce_max_sync(peers, key);
-                    if (lane == __ffs(peers) - 1) {
-                        atomicAdd(&sh.fcnt[dg], (uint32_t)__popc(peers));
-                        atomicAdd(&sh.fmass[dg], ((unsigned long long)mhi << 20) + mlo);
-                        if (bin0 < 0) {
-                            atomicMin(&sh.fkmin[dg], kmin);
-                            atomicMax(&sh.fkmax[dg], kmax);
+                    if (bin0 < 0) {
+                        if (mb == 0u) {
+                            tcnt += 1u;
+                            tm += mass_units(e, true);
+                            tkmin = min(tkmin, key);
+                            tkmax = max(tkmax, key);
+                        } else {
+                            const uint32_t m = mass_units(e, false);
+                            atomicAdd(&sh.fcnt[mb], 1u);
+                            atomicAdd(&sh.flo[mb], m & 0xfffu);
+                            atomicAdd(&sh.fhi[mb], m >> 12);
+                            atomicMin(&sh.fkmin[mb], key);
+                            atomicMax(&sh.fkmax[mb], key);
                         }
+                    } else if ((int)mb == bin0) {
+                        const uint32_t m = mass_units(e, bin0 == 0);
+                        const uint32_t dg = (key >> shift) & width;
+                        atomicAdd(&sh.fcnt[dg], 1u);
+                        atomicAdd(&sh.flo[dg], m & 0xfffu);
+                        atomicAdd(&sh.fhi[dg], m >> 12);
                     }
                 });
+                SPECDEC_STAMP(14);
+                if (bin0 < 0) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        tcnt += __shfl_xor_sync(0xffffffffu, tcnt, off);
+                        tm += __shfl_xor_sync(0xffffffffu, tm, off);
+                        tkmin = min(tkmin, __shfl_xor_sync(0xffffffffu, tkmin, off));
+                        tkmax = max(tkmax, __shfl_xor_sync(0xffffffffu, tkmax, off));
+                    }
+                    if (lane == 0) { sh.ft_cnt[cw] = tcnt; sh.ft_m[cw] = tm; sh.ft_kmin[cw] = tkmin; sh.ft_kmax[cw] = tkmax; }
+                    consumer_sync();
+                    if (ct == 0) {
+                        uint32_t c0 = 0u, k0 = 0xffffffffu, k1 = 0u;
+                        unsigned long long m0 = 0ull;
+                        for (int w = 0; w < kConsumerWarps; ++w) {
+                            c0 += sh.ft_cnt[w]; m0 += sh.ft_m[w];
+                            k0 = min(k0, sh.ft_kmin[w]); k1 = max(k1, sh.ft_kmax[w]);
+                        }
+                        sh.fcnt[0] = c0; sh.ftail_m = m0; sh.fkmin[0] = k0; sh.fkmax[0] = k1;
+                    }
+                }
                 consumer_sync();
             };
             // digit choice by consumer warp 0: lane l holds digits 255 - 8l .. 248 - 8l (highest
             // first); per-lane sums, an exclusive scan over lanes, then each lane walks its digits.
+            // Bin masses in fp64 from the exact integer sums: bin_scale per bin in the first pass
+            // (bin0 < 0), the scale of mass bin bin0 in the later ones.
             // mode 0 (top-k): the digit where the count from the top reaches `need`;
-            // mode 1 (top-p): the lowest non-empty digit whose mass above (plus `above`) is below P.
-            auto select_digit = [&](int mode, unsigned long long need, double P, unsigned long long above) {
+            // mode 1 (top-p): the lowest non-empty digit whose mass above (plus `above`) is below P
+            // (P = p_frac of this pass's total when p_frac >= 0).
+            // Everything the caller needs is copied to the fsel_ fields before the closing barrier:
+            // the next pass clears the bins as soon as a thread reaches it.
+            auto select_digit = [&](int mode, unsigned long long need, double P, double above, int bin0,
+                                    double p_frac) {
                 if (cw == 0) {
-                    unsigned long long lc = 0ull, lm = 0ull;
+                    const double pscale = bin0 < 0 ? 0.0 : bin_scale((uint32_t)bin0);
+                    unsigned long long bc[8], lc = 0ull;
+                    double bm[8], lm = 0.0;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) { lc += sh.fcnt[255 - 8 * lane - i]; lm += sh.fmass[255 - 8 * lane - i]; }
-                    unsigned long long ic = lc, im = lm;
+                    for (int i = 0; i < 8; ++i) {
+                        const int dg = 255 - 8 * lane - i;
+                        bc[i] = sh.fcnt[dg];
+                        if (bin0 < 0 && dg == 0) bm[i] = (double)sh.ftail_m * 0x1p-54;
+                        else bm[i] = ((double)sh.fhi[dg] * 4096.0 + (double)sh.flo[dg]) *
+                                     (bin0 < 0 ? (dg >= 8 ? bin_scale((uint32_t)dg) : 0.0) : pscale);
+                        lc += bc[i];
+                        lm += bm[i];
+                    }
+                    unsigned long long ic = lc;
+                    double im = lm;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, off);
-                        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
+                        const double ym = __shfl_up_sync(0xffffffffu, im, off);
                         if (lane >= off) { ic += yc; im += ym; }
                     }
-                    const unsigned long long tot_m = __shfl_sync(0xffffffffu, im, 31);
-                    unsigned long long c0 = ic - lc, m0 = im - lm, fc = 0ull, fm = 0ull;
+                    const double tot_m = __shfl_sync(0xffffffffu, im, 31);
+                    if (p_frac >= 0.0) P = p_frac * tot_m;
+                    unsigned long long c0 = __shfl_up_sync(0xffffffffu, ic, 1);
+                    double m0 = __shfl_up_sync(0xffffffffu, im, 1);
+                    if (lane == 0) { c0 = 0ull; m0 = 0.0; }
+                    unsigned long long fc = 0ull;
+                    double fm = 0.0, fa = 0.0;
                     int found = -1;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int dg = 255 - 8 * lane - i;
-                        const unsigned long long cn = sh.fcnt[dg], ms = sh.fmass[dg];
                         if (mode == 0) {
-                            if (found < 0 && c0 + cn >= need) { found = dg; fc = c0; fm = m0; }
-                        } else if (cn != 0ull && (double)(above + m0) < P) {
-                            found = dg; fc = c0; fm = m0;
+                            if (found < 0 && c0 + bc[i] >= need) { found = dg; fc = c0; fm = m0; fa = bm[i]; }
+                        } else if (bc[i] != 0ull && above + m0 < P) {
+                            found = dg; fc = c0; fm = m0; fa = bm[i];
                         }
-                        c0 += cn;
-                        m0 += ms;
+                        c0 += bc[i];
+                        m0 += bm[i];
                     }
                     const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
                     // top-k: the first lane that reaches `need`; top-p: the last lane with a candidate
                     const int src = who == 0u ? -1 : (mode == 0 ? __ffs(who) - 1 : 31 - __clz(who));
-                    if (lane == 0) { sh.fsel_digit = 0xffffffffu; sh.ftot_mass = tot_m; }
+                    if (lane == 0) { sh.fsel_digit = 0xffffffffu; sh.ftot_mass = tot_m; sh.fsel_P = P; }
                     __syncwarp();
-                    if (lane == src) { sh.fsel_digit = (uint32_t)found; sh.fsel_cnt = fc; sh.fsel_mass = fm; }
+                    if (lane == src) {
+                        sh.fsel_digit = (uint32_t)found; sh.fsel_cnt = fc; sh.fsel_mass = fm; sh.fsel_at = fa;
+                        sh.fsel_kmin = sh.fkmin[found]; sh.fsel_kmax = sh.fkmax[found];
+                    }
                 }
                 consumer_sync();
             };
             // the threshold key for one search: mode 0 (top-k: the `need`-th largest element) or
-            // mode 1 (top-p: the smallest key whose mass above is below P; P from the first pass when
-            // P < 0, as p_frac of the mass at or above floor_key). Returns the key, the count and
-            // mass above it (`cnt_above`, `mass_above`) and the mass of its own ties (`mass_at`);
-            // false when the search keeps every element (top-k with k >= the elements).
+            // mode 1 (top-p: the smallest key whose mass above is below P = p_frac of the mass at or
+            // above floor_key). Returns the key, the mass above it (`mass_above`) and the mass of its
+            // own ties (`mass_at`); false when the search keeps every element (top-k with k >= the
+            // elements). The digit passes stop at bit 16 for bf16 logits: below it a key's bits
+            // follow from its sign bit (all zero for z >= 0, all one below).
             auto search = [&](int64_t t, int j, int mode, unsigned long long need, double p_frac, uint32_t floor_key,
-                              float MC, uint32_t& key_out, unsigned long long& mass_above, unsigned long long& mass_at) -> bool {
-                hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC);
-                double P = 0.0;
-                if (mode == 1) {
-                    select_digit(1, 0ull, -1.0, 0ull);               // totals only
-                    P = p_frac * (double)sh.ftot_mass;
-                }
-                select_digit(mode, need, P, 0ull);
+                              float MC, uint32_t& key_out, double& mass_above, double& mass_at) -> bool {
+                constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
+                hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu);
+                select_digit(mode, need, 0.0, 0.0, -1, mode == 1 ? p_frac : -1.0);
+                const double P = sh.fsel_P;
                 const uint32_t b0 = sh.fsel_digit;
                 if (b0 == 0xffffffffu) {                             // top-k covers every element
                     mass_above = sh.ftot_mass;
-                    mass_at = 0ull;
+                    mass_at = 0.0;
                     return false;
                 }
-                unsigned long long above = sh.fsel_mass;
+                double above = sh.fsel_mass;
+                double at = sh.fsel_at;
                 need -= sh.fsel_cnt;
-                uint32_t kmin = sh.fkmin[b0], kmax = sh.fkmax[b0];
-                unsigned long long at = sh.fmass[b0];
+                uint32_t kmin = sh.fsel_kmin;
+                const uint32_t kmax = sh.fsel_kmax;
                 // resolve the keys of bin b0 from the highest bit where they differ, 8 bits a pass
-                uint32_t pmask = 0u, pval = 0u;
                 if (kmin != kmax) {
                     const int hb = 31 - __clz(kmin ^ kmax);
-                    pmask = hb == 31 ? 0u : (0xffffffffu << (hb + 1));
-                    pval = kmin & pmask;
-                    for (int top = hb; top >= 0; top -= 8) {
-                        const int shift = max(0, top - 7);
-                        const uint32_t width = (top - shift == 7) ? 0xffu : ((1u << (top - shift + 1)) - 1u);
-                        hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC);
-                        select_digit(mode, need, P, above);
+                    uint32_t pmask = hb == 31 ? 0u : (0xffffffffu << (hb + 1));
+                    uint32_t pval = kmin & pmask;
+                    for (int top = hb; top >= kLowBit; top -= 8) {
+                        const int shift = max(kLowBit, top - 7);
+                        const uint32_t width = (1u << (top - shift + 1)) - 1u;
+                        hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC, kmin, kmax);
+                        select_digit(mode, need, P, above, (int)b0, -1.0);
                         const uint32_t dg = sh.fsel_digit;           // always found inside the bin
                         above += sh.fsel_mass;
+                        at = sh.fsel_at;
                         need -= sh.fsel_cnt;
                         pval |= dg << shift;
                         pmask |= width << shift;
-                        at = sh.fmass[dg];
                     }
+                    if (kLowBit > 0) pval |= (pval & 0x80000000u) ? 0u : ((1u << kLowBit) - 1u);
                     kmin = pval;
                 }
                 key_out = kmin;
@@ -1866,7 +1939,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             };
             auto filter_row = [&](int64_t t, int j, float MC, uint32_t& kt, float& S_keep) -> bool {
                 uint32_t floor_key = 0u;
-                unsigned long long keep = 0ull, above = 0ull, at = 0ull;
+                double keep = 0.0, above = 0.0, at = 0.0;
                 bool cut_k = false;
                 if (fk > 0) {
                     uint32_t key;
@@ -1880,7 +1953,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     if (cut_p) { floor_key = key; keep = above + at; }
                 }
                 kt = floor_key;
-                S_keep = (float)((double)keep * (1.0 / 1099511627776.0));
+                SPECDEC_STAMP(12);
+                S_keep = (float)keep;
                 return cut_k || cut_p;
             };
 
@@ -2597,8 +2671,9 @@ extern "C" specdec_status_t specdec_verify(
     const specdec_status_t rc = shape_for(V, logits_dtype, B, &shape);
     if (rc != SPECDEC_OK) return rc;
     if (top_k || top_p) {
-        // the threshold search reduces within one CTA: one CTA per request, streaming kernel only
-        if (!shape.stream) return SPECDEC_ERR_UNSUPPORTED;
+        // the threshold search reduces within one CTA: one CTA per request, streaming kernel only;
+        // its 32-bit bin sums of 12-bit mass parts are exact up to 2^20 elements per row
+        if (!shape.stream || V > (1 << 20)) return SPECDEC_ERR_UNSUPPORTED;
         const long long units = ((long long)V + kUnit - 1) / kUnit;
         shape.G = 1;
         shape.slice_units = (int)units;

@@ -124,6 +124,16 @@ def test_host_validation(lib, monkeypatch):
     assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
 
 
+def test_filter_vocabulary_limit(lib, monkeypatch):
+    # top-k / top-p sum 12-bit mass parts in 32-bit bins: exact up to 2^20 elements per row
+    monkeypatch.delenv("SPECDEC_KERNEL", raising=False)
+    E = _native
+    assert _call(lib, tp=4096, V=(1 << 20) + 1) == E.SPECDEC_ERR_UNSUPPORTED
+    assert _call(lib, tk=4096, V=(1 << 20) + 1) == E.SPECDEC_ERR_UNSUPPORTED
+    assert _call(lib, tk=4096, V=1 << 20, B=0) == E.SPECDEC_OK       # at the limit (empty batch: no launch)
+    assert _call(lib, V=(1 << 20) + 1, B=0) == E.SPECDEC_OK          # no filter: no limit
+
+
 def test_workspace_size_and_validation(lib, monkeypatch):
     E = _native
     assert _native.workspace_size(0, 1000) == 0 and _native.workspace_size(4, 0) == 0
