@@ -760,6 +760,8 @@ constexpr int kDataBytes = kRingBytes - kListBytes;
 constexpr int kGatherCap = kDataBytes / 16;    // logits groups per gather batch
 constexpr int kSegWords = 5120;                // mask words scanned per pass (20 per consumer thread)
 
+constexpr int kCandCap = 2048;                 // top-k / top-p: candidate keys held on chip
+
 enum : int { kDecNextRow = 1, kDecDrawP = 2, kDecDrawQ = 3, kDecDrawOneHot = 4, kDecDone = 5,
               kDecRescan = 6 };   // stream the same row once more (a top-k / top-p digit pass)
 
@@ -807,9 +809,8 @@ struct StreamShared {
     // integers kept as the sums of their low and high 12 bits (exact in 32 bits for V <= 2^20).
     uint32_t fcnt[256];
     uint32_t flo[256], fhi[256];
-    uint32_t fkmin[256], fkmax[256];     // first pass: smallest / largest logit key per bin
-    uint32_t ft_cnt[kConsumerWarps], ft_kmin[kConsumerWarps], ft_kmax[kConsumerWarps];   // tail, per warp
-    unsigned long long ft_m[kConsumerWarps];
+    uint32_t fw_cnt[kConsumerWarps], fw_kmin[kConsumerWarps], fw_kmax[kConsumerWarps];  // per-warp partials
+    unsigned long long fw_m[kConsumerWarps], fw_m2[kConsumerWarps];
     unsigned long long ftail_m;          // first pass: tail mass in units of 2^-54
     uint32_t fsel_digit;                 // chosen digit (0xffffffff: none)
     uint32_t fsel_pad;
@@ -817,7 +818,12 @@ struct StreamShared {
     double fsel_mass, fsel_at;           // mass above the chosen digit / of the digit itself
     double ftot_mass;                    // mass of every element counted in this pass
     double fsel_P;                       // the top-p target mass the choice used
-    uint32_t fsel_kmin, fsel_kmax;       // first pass: the chosen bin's smallest / largest key
+    unsigned long long fsel_n;           // elements in the chosen digit (first top-p pass: a bound)
+    uint32_t fc_kmin, fc_kmax;           // collection pass: the chosen bin's smallest / largest key
+    unsigned long long fc_mbin;          // collection pass: the chosen bin's mass (its units)
+    unsigned long long fc_mabove;        // collection pass: mass above the bin, units of 2^-40
+    uint32_t fncand;                     // candidates appended by the last collection pass
+    uint32_t fcand[kCandCap];            // candidate keys (in no particular order)
     int32_t fk;
     float fp;
 };
@@ -933,6 +939,22 @@ __device__ __forceinline__ Filter request_filter(const Args& a, int b)
     return f;
 }
 
+// Bit e set when z[e] is above -inf (a NaN never is)
+template <int N>
+__device__ __forceinline__ uint32_t finite_bits(const float* z)
+{
+    uint32_t b = 0u;
+#pragma unroll
+    for (int e = 0; e < N; ++e) b |= (z[e] > -INFINITY ? 1u : 0u) << e;
+    return b;
+}
+
+// The logit whose logit_key is `key` (zero comes back as +0)
+__device__ __forceinline__ float key_logit(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // First-pass bin of an element by its mass e = exp2(z * c - MC) in (0, ~1]: 8 bins per halving
 // (exponent and 3 mantissa bits), from bin 8 (2^-30) to 255 (1); bin 0 (the tail) holds
 // everything below 2^-30. Non-decreasing in e, hence in the logit: every element of a higher bin
@@ -940,11 +962,9 @@ __device__ __forceinline__ Filter request_filter(const Args& a, int b)
 // is its elements' 24-bit significands summed exactly, times 2^(exponent - 23).
 __device__ __forceinline__ uint32_t mass_bin(float e)
 {
-    const uint32_t u = __float_as_uint(e);
-    const int ex = (int)(u >> 23);
-    if (ex < 97) return 0u;
-    const uint32_t d = (uint32_t)(ex - 97) * 8u + ((u >> 20) & 7u) + 8u;
-    return d > 255u ? 255u : d;
+    // bits 30..20 of e are its exponent and top 3 mantissa bits: 8 * exponent + those 3 bits
+    const int d = (int)(__float_as_uint(e) >> 20) - (97 * 8 - 8);
+    return d < 8 ? 0u : (uint32_t)min(d, 255);
 }
 
 // The 24-bit significand of e (bins 8..255) or e in units of 2^-54 (the tail, e < 2^-30): an
@@ -1682,9 +1702,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // integer sums (the result does not depend on the order of the additions). Dense rows
             // are streamed again through the ring; sparse rows reuse their gathered groups when the
             // row's list fit one gather batch, else gather again.
-            // The visitors call f(z, valid) for every element slot of the row in warp-converged
-            // code (all 32 lanes of a warp together; valid = an allowed id with a finite logit), so
-            // that f may use warp-wide intrinsics.
+            // The visitors call f(z, valid) for every vector of element slots of the row (z: VE
+            // logits; bit e of valid: slot e holds an allowed id with a finite logit).
             auto gather_and_visit = [&](int64_t t, int n, auto&& f) {
                 const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
                 const uint32_t dbase = smem_addr(ring + kDataOff);
@@ -1701,8 +1720,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         float z[VE];
                         unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
                         const uint32_t bits = in ? (list[b0 + e] & 0xffu) : 0u;
-#pragma unroll
-                        for (int q = 0; q < VE; ++q) f(z[q], ((bits >> q) & 1u) && z[q] > -INFINITY);
+                        f(z, bits & finite_bits<VE>(z));
                     }
                     consumer_sync();
                 }
@@ -1710,6 +1728,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             auto visit_row = [&](int64_t t, int j, auto&& f) {
                 if (!sparse) {
                     post(kDecRescan);
+                    constexpr int NB = 4;                       // vectors loaded together (latency)
                     for (int ch = 0; ch < nrow_chunks; ++ch) {
                         const int s = wait_full();
                         const unsigned char* stg = ring + (size_t)s * kStageBytes;
@@ -1717,18 +1736,23 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         const int i0 = lo + ch * G::kRowIds;
                         const int n = min(G::kRowIds, hi - i0);
                         const int nvec = (n + VE - 1) / VE;
-                        for (int v0 = ct - lane; v0 < nvec; v0 += kConsumers) {     // warp-uniform trip count
-                            const int v = v0 + lane;
-                            const bool in = v < nvec;
-                            float z[VE];
-                            if (in) Elem<ET>::load(stg, v, z);
-                            else {
+                        for (int vb = ct - lane; vb < nvec; vb += kConsumers * NB) {   // warp-uniform trip count
+                            uint4 raw[NB];
+                            uint32_t bits[NB];
 #pragma unroll
-                                for (int e = 0; e < VE; ++e) z[e] = -INFINITY;
+                            for (int u = 0; u < NB; ++u) {
+                                const int v = vb + lane + u * kConsumers;
+                                const bool in = v < nvec;
+                                const uint32_t ni = Raw<ET>::kNegInf;
+                                raw[u] = in ? reinterpret_cast<const uint4*>(stg)[v] : make_uint4(ni, ni, ni, ni);
+                                bits[u] = in ? vec_bits<VE>(sm, has_mask, v) : 0u;
                             }
-                            const uint32_t bits = in ? vec_bits<VE>(sm, has_mask, v) : 0u;
 #pragma unroll
-                            for (int e = 0; e < VE; ++e) f(z[e], ((bits >> e) & 1u) && z[e] > -INFINITY);
+                            for (int u = 0; u < NB; ++u) {
+                                float z[VE];
+                                unpack_raw<ET>(raw[u], z);
+                                f(z, bits[u] & finite_bits<VE>(z));
+                            }
                         }
                         release(s);
                     }
@@ -1741,8 +1765,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         float z[VE];
                         unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
                         const uint32_t bits = in ? (list[e] & 0xffu) : 0u;
-#pragma unroll
-                        for (int q = 0; q < VE; ++q) f(z[q], ((bits >> q) & 1u) && z[q] > -INFINITY);
+                        f(z, bits & finite_bits<VE>(z));
                     }
                 } else if (listed_row == j) {
                     gather_and_visit(t, listed_n, f);
@@ -1759,69 +1782,82 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     }
                 }
             };
-            // one pass over the row into the 256 bins. First pass (bin0 < 0): every element at or above
-            // floor_key, by mass_bin, with each bin's smallest and largest key; the tail (bin 0), where
-            // most elements of a peaked row fall, is summed in registers and folded afterwards, so the
-            // shared-memory additions spread over the other bins. Later passes: the elements of mass
-            // bin bin0 whose key matches pval on the bits of pmask, by the key's bits [shift, shift +
-            // 8) (width). Integer sums only: the result does not depend on the order of the additions.
+            // Sum of v over the consumer threads, in a fixed order (shuffles, then the warps in
+            // order): every consumer thread gets the same value.
+            auto fold_u64 = [&](unsigned long long v, unsigned long long* slots) -> unsigned long long {
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) slots[cw] = v;
+                consumer_sync();
+                unsigned long long r = 0ull;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) r += slots[w];
+                return r;
+            };
+            // One pass into the 256 bins. First pass (bin0 < 0): every element at or above floor_key,
+            // by mass_bin, counting elements (want & 1: top-k) or summing masses (want & 2: top-p);
+            // the tail (bin 0), where most elements of a peaked row fall, is counted and summed in
+            // registers and folded afterwards, so the shared-memory additions spread over the other
+            // bins. Later passes: the elements of mass bin bin0 whose key lies in [klo, khi] and
+            // matches pval on the bits of pmask, counted and summed by the key's bits [shift, shift
+            // + 8) (width). Integer sums only: the result does not depend on the order of the
+            // additions. The elements come from the row (ncand < 0) or the first ncand candidates.
             auto hist_pass = [&](int64_t t, int j, int bin0, uint32_t pmask, uint32_t pval, int shift, uint32_t width,
-                                 uint32_t floor_key, float MC, uint32_t klo, uint32_t khi) {
-                for (int i = ct; i < 256; i += kConsumers) {
-                    sh.fcnt[i] = 0u; sh.flo[i] = 0u; sh.fhi[i] = 0u; sh.fkmin[i] = 0xffffffffu; sh.fkmax[i] = 0u;
-                }
+                                 uint32_t floor_key, float MC, uint32_t klo, uint32_t khi, int ncand, int want) {
+                for (int i = ct; i < 256; i += kConsumers) { sh.fcnt[i] = 0u; sh.flo[i] = 0u; sh.fhi[i] = 0u; }
                 consumer_sync();
                 SPECDEC_STAMP(13);
-                uint32_t tcnt = 0u, tkmin = 0xffffffffu, tkmax = 0u;
+                const bool wcnt = bin0 >= 0 || (want & 1), wmass = bin0 >= 0 || (want & 2);
+                uint32_t tcnt = 0u;
                 unsigned long long tm = 0ull;
-                visit_row(t, j, [&](float z, bool valid) {
-                    if (!valid) return;
-                    const uint32_t key = logit_key(z);
-                    if (key < floor_key || key < klo || key > khi || (key & pmask) != pval) return;
-                    const float e = ex2(fmaf(z, c, -MC));
-                    const uint32_t mb = mass_bin(e);
-                    if (bin0 < 0) {
-                        if (mb == 0u) {
-                            tcnt += 1u;
-                            tm += mass_units(e, true);
-                            tkmin = min(tkmin, key);
-                            tkmax = max(tkmax, key);
-                        } else {
-                            const uint32_t m = mass_units(e, false);
-                            atomicAdd(&sh.fcnt[mb], 1u);
-                            atomicAdd(&sh.flo[mb], m & 0xfffu);
-                            atomicAdd(&sh.fhi[mb], m >> 12);
-                            atomicMin(&sh.fkmin[mb], key);
-                            atomicMax(&sh.fkmax[mb], key);
-                        }
-                    } else if ((int)mb == bin0) {
-                        const uint32_t m = mass_units(e, bin0 == 0);
-                        const uint32_t dg = (key >> shift) & width;
-                        atomicAdd(&sh.fcnt[dg], 1u);
-                        atomicAdd(&sh.flo[dg], m & 0xfffu);
-                        atomicAdd(&sh.fhi[dg], m >> 12);
+                const uint32_t kfloor = max(floor_key, klo);
+                auto bin = [&](const auto& z, uint32_t valid) {
+                    constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
+                    uint32_t key[N];
+                    uint32_t in = 0u;
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        key[i] = logit_key(z[i]);
+                        in |= (((valid >> i) & 1u) && key[i] >= kfloor && key[i] <= khi && (key[i] & pmask) == pval ? 1u : 0u) << i;
                     }
-                });
+                    if (in == 0u) return;
+                    float e[N];
+                    uint32_t mb[N];
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        e[i] = ex2(fmaf(z[i], c, -MC));
+                        mb[i] = mass_bin(e[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        if (!((in >> i) & 1u)) continue;
+                        uint32_t dg;
+                        if (bin0 < 0) {
+                            if (mb[i] == 0u) { tcnt += 1u; tm += mass_units(e[i], true); continue; }
+                            dg = mb[i];
+                        } else {
+                            if ((int)mb[i] != bin0) continue;
+                            dg = (key[i] >> shift) & width;
+                        }
+                        if (wcnt) atomicAdd(&sh.fcnt[dg], 1u);
+                        if (wmass) {
+                            const uint32_t m = mass_units(e[i], bin0 == 0);
+                            atomicAdd(&sh.flo[dg], m & 0xfffu);
+                            atomicAdd(&sh.fhi[dg], m >> 12);
+                        }
+                    }
+                };
+                if (ncand < 0) visit_row(t, j, bin);
+                else
+                    for (int i = ct; i < ncand; i += kConsumers) {
+                        const float z1[1] = {key_logit(sh.fcand[i])};
+                        bin(z1, 1u);
+                    }
                 SPECDEC_STAMP(14);
                 if (bin0 < 0) {
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) {
-                        tcnt += __shfl_xor_sync(0xffffffffu, tcnt, off);
-                        tm += __shfl_xor_sync(0xffffffffu, tm, off);
-                        tkmin = min(tkmin, __shfl_xor_sync(0xffffffffu, tkmin, off));
-                        tkmax = max(tkmax, __shfl_xor_sync(0xffffffffu, tkmax, off));
-                    }
-                    if (lane == 0) { sh.ft_cnt[cw] = tcnt; sh.ft_m[cw] = tm; sh.ft_kmin[cw] = tkmin; sh.ft_kmax[cw] = tkmax; }
-                    consumer_sync();
-                    if (ct == 0) {
-                        uint32_t c0 = 0u, k0 = 0xffffffffu, k1 = 0u;
-                        unsigned long long m0 = 0ull;
-                        for (int w = 0; w < kConsumerWarps; ++w) {
-                            c0 += sh.ft_cnt[w]; m0 += sh.ft_m[w];
-                            k0 = min(k0, sh.ft_kmin[w]); k1 = max(k1, sh.ft_kmax[w]);
-                        }
-                        sh.fcnt[0] = c0; sh.ftail_m = m0; sh.fkmin[0] = k0; sh.fkmax[0] = k1;
-                    }
+                    const unsigned long long c0 = fold_u64(tcnt, sh.fw_m);
+                    const unsigned long long m0 = fold_u64(tm, sh.fw_m2);
+                    if (ct == 0) { sh.fcnt[0] = (uint32_t)c0; sh.ftail_m = m0; }
                 }
                 consumer_sync();
             };
@@ -1863,16 +1899,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     unsigned long long c0 = __shfl_up_sync(0xffffffffu, ic, 1);
                     double m0 = __shfl_up_sync(0xffffffffu, im, 1);
                     if (lane == 0) { c0 = 0ull; m0 = 0.0; }
-                    unsigned long long fc = 0ull;
+                    unsigned long long fc = 0ull, fn = 0ull;
                     double fm = 0.0, fa = 0.0;
                     int found = -1;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int dg = 255 - 8 * lane - i;
+                        // elements in the digit: counted, or (first top-p pass, bins from 8 up) at
+                        // most the mass units over 2^23, the smallest significand
+                        const unsigned long long n = (bin0 < 0 && mode == 1 && dg >= 8)
+                            ? (((unsigned long long)sh.fhi[dg] << 12) + sh.flo[dg]) >> 23 : bc[i];
                         if (mode == 0) {
-                            if (found < 0 && c0 + bc[i] >= need) { found = dg; fc = c0; fm = m0; fa = bm[i]; }
-                        } else if (bc[i] != 0ull && above + m0 < P) {
-                            found = dg; fc = c0; fm = m0; fa = bm[i];
+                            if (found < 0 && c0 + bc[i] >= need) { found = dg; fc = c0; fm = m0; fa = bm[i]; fn = n; }
+                        } else if ((bc[i] != 0ull || bm[i] > 0.0) && above + m0 < P) {
+                            found = dg; fc = c0; fm = m0; fa = bm[i]; fn = n;
                         }
                         c0 += bc[i];
                         m0 += bm[i];
@@ -1884,10 +1924,79 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     __syncwarp();
                     if (lane == src) {
                         sh.fsel_digit = (uint32_t)found; sh.fsel_cnt = fc; sh.fsel_mass = fm; sh.fsel_at = fa;
-                        sh.fsel_kmin = sh.fkmin[found]; sh.fsel_kmax = sh.fkmax[found];
+                        sh.fsel_n = fn;
                     }
                 }
                 consumer_sync();
+            };
+            // One more pass for mass bin bc: the smallest and largest key and the mass of its
+            // elements (at or above floor_key), the mass above it (units of 2^-40), and, over the
+            // row (ncand < 0), the keys of its elements (all = false) or of every element from bin
+            // bc up (all = true) appended to the candidates. Returns the number of such elements
+            // (above kCandCap: only the first kCandCap kept). Over the first ncand candidates
+            // (ncand >= 0) nothing is appended and ncand comes back.
+            auto collect_pass = [&](int64_t t, int j, uint32_t bc, bool all, uint32_t floor_key, float MC,
+                                    int ncand) -> int {
+                if (ct == 0 && ncand < 0) sh.fncand = 0u;
+                consumer_sync();
+                SPECDEC_STAMP(10);
+                uint32_t kmn = 0xffffffffu, kmx = 0u;
+                unsigned long long mbin = 0ull, mab = 0ull;
+                auto take = [&](const auto& z, uint32_t valid) {
+                    constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
+                    uint32_t key[N];
+                    uint32_t in = 0u;
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        key[i] = logit_key(z[i]);
+                        in |= (((valid >> i) & 1u) && key[i] >= floor_key ? 1u : 0u) << i;
+                    }
+                    if (in == 0u) return;
+                    float e[N];
+                    uint32_t mb[N];
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        e[i] = ex2(fmaf(z[i], c, -MC));
+                        mb[i] = mass_bin(e[i]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        if (!((in >> i) & 1u) || mb[i] < bc) continue;
+                        if (mb[i] == bc) {
+                            kmn = min(kmn, key[i]);
+                            kmx = max(kmx, key[i]);
+                            mbin += mass_units(e[i], bc == 0u);
+                        } else {
+                            mab += __float2ull_rn(e[i] * 0x1p40f);
+                        }
+                        if (ncand < 0 && (all || mb[i] == bc)) {
+                            const uint32_t pos = atomicAdd(&sh.fncand, 1u);
+                            if (pos < (uint32_t)kCandCap) sh.fcand[pos] = key[i];
+                        }
+                    }
+                };
+                if (ncand < 0) visit_row(t, j, take);
+                else
+                    for (int i = ct; i < ncand; i += kConsumers) {
+                        const float z1[1] = {key_logit(sh.fcand[i])};
+                        take(z1, 1u);
+                    }
+                SPECDEC_STAMP(11);
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, off));
+                    kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, off));
+                }
+                if (lane == 0) { sh.fw_kmin[cw] = kmn; sh.fw_kmax[cw] = kmx; }
+                const unsigned long long m_bin = fold_u64(mbin, sh.fw_m);       // (its barrier covers the keys)
+                const unsigned long long m_above = fold_u64(mab, sh.fw_m2);
+                if (ct == 0) {
+                    uint32_t k0 = 0xffffffffu, k1 = 0u;
+                    for (int w = 0; w < kConsumerWarps; ++w) { k0 = min(k0, sh.fw_kmin[w]); k1 = max(k1, sh.fw_kmax[w]); }
+                    sh.fc_kmin = k0; sh.fc_kmax = k1; sh.fc_mbin = m_bin; sh.fc_mabove = m_above;
+                }
+                consumer_sync();
+                return ncand < 0 ? (int)sh.fncand : ncand;
             };
             // the threshold key for one search: mode 0 (top-k: the `need`-th largest element) or
             // mode 1 (top-p: the smallest key whose mass above is below P = p_frac of the mass at or
@@ -1895,10 +2004,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // own ties (`mass_at`); false when the search keeps every element (top-k with k >= the
             // elements). The digit passes stop at bit 16 for bf16 logits: below it a key's bits
             // follow from its sign bit (all zero for z >= 0, all one below).
+            // After the first pass chooses a mass bin, a collection pass takes its key range and
+            // mass and, when they fit on chip, the keys of its elements (of every element from that
+            // bin up when `keep_above` and they fit, for a search that follows); the digit passes
+            // then run over those candidates instead of the row. `ncand` >= 0 on entry means the
+            // candidates already hold every element at or above floor_key, so the whole search
+            // runs on chip; on return it is >= 0 when that holds for this search's kept elements.
             auto search = [&](int64_t t, int j, int mode, unsigned long long need, double p_frac, uint32_t floor_key,
-                              float MC, uint32_t& key_out, double& mass_above, double& mass_at) -> bool {
+                              float MC, bool keep_above, int& ncand, uint32_t& key_out, double& mass_above,
+                              double& mass_at) -> bool {
                 constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
-                hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu);
+                const int src0 = ncand;
+                // on chip, the first pass takes counts and masses (the candidates are few)
+                hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu, src0,
+                          src0 >= 0 ? 3 : (mode == 0 ? 1 : 2));
                 select_digit(mode, need, 0.0, 0.0, -1, mode == 1 ? p_frac : -1.0);
                 const double P = sh.fsel_P;
                 const uint32_t b0 = sh.fsel_digit;
@@ -1907,11 +2026,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     mass_at = 0.0;
                     return false;
                 }
-                double above = sh.fsel_mass;
-                double at = sh.fsel_at;
-                need -= sh.fsel_cnt;
-                uint32_t kmin = sh.fsel_kmin;
-                const uint32_t kmax = sh.fsel_kmax;
+                const unsigned long long n_above = sh.fsel_cnt, n_bin = sh.fsel_n;
+                double above = sh.fsel_mass;                      // (first top-k pass: not summed)
+                need -= n_above;
+                int src = src0;
+                if (src0 < 0) ncand = -1;
+                const bool all = src0 < 0 && keep_above && n_above + n_bin <= (unsigned long long)kCandCap;
+                const int n = collect_pass(t, j, b0, all, floor_key, MC, src0);
+                if (src0 < 0 && n <= kCandCap) {
+                    src = n;
+                    if (all) ncand = n;
+                }
+                const double bscale = bin_scale(b0);
+                if (mode == 0) above = (double)sh.fc_mabove * 0x1p-40;
+                double at = (double)sh.fc_mbin * bscale;
+                uint32_t kmin = sh.fc_kmin;
+                const uint32_t kmax = sh.fc_kmax;
                 // resolve the keys of bin b0 from the highest bit where they differ, 8 bits a pass
                 if (kmin != kmax) {
                     const int hb = 31 - __clz(kmin ^ kmax);
@@ -1920,7 +2050,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     for (int top = hb; top >= kLowBit; top -= 8) {
                         const int shift = max(kLowBit, top - 7);
                         const uint32_t width = (1u << (top - shift + 1)) - 1u;
-                        hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC, kmin, kmax);
+                        hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC, kmin, kmax, src, 3);
                         select_digit(mode, need, P, above, (int)b0, -1.0);
                         const uint32_t dg = sh.fsel_digit;           // always found inside the bin
                         above += sh.fsel_mass;
@@ -1940,16 +2070,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             auto filter_row = [&](int64_t t, int j, float MC, uint32_t& kt, float& S_keep) -> bool {
                 uint32_t floor_key = 0u;
                 double keep = 0.0, above = 0.0, at = 0.0;
+                int ncand = -1;                                  // candidates hold every kept element
                 bool cut_k = false;
                 if (fk > 0) {
                     uint32_t key;
-                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, key, above, at);
+                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, fp < 1.f, ncand, key, above, at);
                     if (cut_k) { floor_key = key; keep = above + at; }
                 }
                 bool cut_p = false;
                 if (fp < 1.f) {
                     uint32_t key;
-                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, key, above, at);
+                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, false, ncand, key, above, at);
                     if (cut_p) { floor_key = key; keep = above + at; }
                 }
                 kt = floor_key;
