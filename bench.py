@@ -19,6 +19,7 @@ cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the same w
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -41,7 +42,10 @@ METRIC = "verified draft tokens/s (HBM GB/s and fraction of GB300 peak in roofli
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 2 * 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_verification_specdec_gb300", "csrc", "specdec_verify.cu")
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_specdec_gb300", "csrc")
+KERNEL_SRC = os.path.join(CSRC, "specdec_verify.cu")
+NGRAM_SRC = os.path.join(CSRC, "specdec_ngram.cu")
+SCATTER_SRC = os.path.join(CSRC, "specdec_bitmask.cu")
 
 
 def parse():
@@ -61,6 +65,10 @@ def parse():
                     help="time the bitmask scatter (compact scheduler-order masks -> batch rows) instead")
     ap.add_argument("--filters", action="store_true",
                     help="verify the random draft-model batch with per-request top-k / top-p instead")
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="with --filters: this top-k on every request instead of the drawn mix (top-p off unless given)")
+    ap.add_argument("--top-p", type=float, default=None,
+                    help="with --filters: this top-p on every request instead of the drawn mix (top-k off unless given)")
     ap.add_argument("--requests", type=int, default=0,
                     help="verify only the first N requests of the workload (profiler captures); 0 = all")
     return ap.parse_args()
@@ -73,9 +81,9 @@ def dist_env():
     return world, rank, local
 
 
-def kernel_hash() -> str:
-    """Hash of the verify kernels' source: profiler counters are tied to the code they measured."""
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_hash(src: str = KERNEL_SRC) -> str:
+    """Hash of a kernel's source file: profiler counters are tied to the code they measured."""
+    with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
@@ -88,11 +96,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload_for(cfg: int, rank: int, requests: int = 0, filters: bool = False) -> W.Workload:
+def workload_for(cfg: int, rank: int, requests: int = 0, filters: bool = False, top_k=None, top_p=None) -> W.Workload:
     # rank 0 verifies the recipe's own seeded batch; other ranks verify independent batches;
     # requests > 0 keeps the first `requests` requests (smaller cases for profiler captures);
-    # filters: the random draft-model batch with per-request top-k / top-p
+    # filters: the random draft-model batch with per-request top-k / top-p (top_k / top_p: one
+    # setting on every request)
     w = W.top_k_top_p_batch(5 + 1000 * rank) if filters else W.config(cfg, seed=cfg + 1000 * rank)
+    if filters and (top_k is not None or top_p is not None):
+        tk = np.full(w.B, 0 if top_k is None else top_k, np.int32)            # the other one off
+        tp = np.full(w.B, 1.0 if top_p is None else top_p, np.float32)
+        name = w.name + (f"_topk{top_k}" if top_k is not None else "") + (f"_topp{top_p:g}" if top_p is not None else "")
+        w = dataclasses.replace(w, top_k=tk, top_p=tp, name=name)
     if 0 < requests < w.B:
         w = w.subset(range(requests), name=f"{w.name}_first{requests}")
     return w
@@ -264,7 +278,7 @@ def run_reference(args, world, rank):
         return
     import oracle
 
-    w = workload_for(args.config, 0, args.requests, args.filters)
+    w = workload_for(args.config, 0, args.requests, args.filters, args.top_k, args.top_p)
     oracle.load()
     budget_total = 150.0
     per_step = max(0.05, min(5.0, budget_total / max(1, args.steps + args.warmup)))
@@ -305,15 +319,15 @@ def run_reference(args, world, rank):
 # our arm
 # ------------------------------------------------------------------------------------------
 
-def traffic_from_profiles(config_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+def traffic_from_profiles(config_name: str, src: str = KERNEL_SRC):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(config_name)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    if not e or e.get("kernel_hash") != kernel_hash(src):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -379,8 +393,8 @@ def run_ngram(args, world, rank, local):
         "config": {"workload": hs.name, "B": B, "tokens": int(hs.tokens.size), "min_n": min_n, "max_n": max_n, "k": k,
                    "hit_rate": hits, "l2": "flushed between timed steps (268 MB write)"},
         "roofline": {"bound": "hbm", "achieved": alg / mean_s / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": alg / mean_s / 1e9 / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "specdec_ngram_kernel", "algorithmic_bytes_per_launch": alg},
+                     "frac": alg / mean_s / 1e9 / peak, "traffic": traffic_from_profiles(hs.name, NGRAM_SRC),
+                     "peak_kind": peak_kind, "kernel": "specdec_ngram_kernel", "algorithmic_bytes_per_launch": alg},
         "gpu_launches": args.steps, "clocks": clocks,
         "kernel_ms": {"median": statistics.median(ms), "min": min(ms), "max": max(ms)},
     }
@@ -445,7 +459,8 @@ def run_scatter(args, world, rank, local):
                    "constrained_requests": int(ids.numel()), "compact_rows": int(rows.size),
                    "l2": "flushed between timed steps (268 MB write)"},
         "roofline": {"bound": "hbm", "achieved": alg / mean_s / 1e9, "peak": peak, "unit": "GB/s",
-                     "frac": alg / mean_s / 1e9 / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": alg / mean_s / 1e9 / peak,
+                     "traffic": traffic_from_profiles(f"{w.name}_bitmask_scatter", SCATTER_SRC), "peak_kind": peak_kind,
                      "kernel": "specdec_bitmask_scatter_kernel", "algorithmic_bytes_per_launch": alg},
         "gpu_launches": args.steps, "clocks": clocks,
         "kernel_ms": {"median": statistics.median(ms), "min": min(ms), "max": max(ms)},
@@ -481,7 +496,7 @@ def main():
         pg.barrier()
     _native.load()
 
-    w = workload_for(args.config, rank, args.requests, args.filters)
+    w = workload_for(args.config, rank, args.requests, args.filters, args.top_k, args.top_p)
     host = device.host_tensors(w)
     dev_in = device.device_tensors(w, dev, host)
     out = device.alloc_outputs(w, dev, diag=False, telemetry=True)   # per-position counts, every step
