@@ -1690,6 +1690,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         };
 
         int acc_len = 0, emitted = -1;
+        bool try_slice = true;          // top-k: try the top-slice pass first (off after a miss)
         if (rs.skip == 0) {
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
@@ -1998,6 +1999,30 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 consumer_sync();
                 return ncand < 0 ? (int)sh.fncand : ncand;
             };
+            // One pass over the row appending the key of every allowed element whose logit is at least
+            // zt (a top slice of the row). Returns their number (above kCandCap: only the first
+            // kCandCap kept).
+            auto slice_pass = [&](int64_t t, int j, float zt) -> int {
+                if (ct == 0) sh.fncand = 0u;
+                consumer_sync();
+                SPECDEC_STAMP(10);
+                visit_row(t, j, [&](const auto& z, uint32_t valid) {
+                    constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
+                    uint32_t take = 0u;
+#pragma unroll
+                    for (int i = 0; i < N; ++i) take |= (((valid >> i) & 1u) && z[i] >= zt ? 1u : 0u) << i;
+                    if (take == 0u) return;
+#pragma unroll
+                    for (int i = 0; i < N; ++i)
+                        if ((take >> i) & 1u) {
+                            const uint32_t pos = atomicAdd(&sh.fncand, 1u);
+                            if (pos < (uint32_t)kCandCap) sh.fcand[pos] = logit_key(z[i]);
+                        }
+                });
+                SPECDEC_STAMP(11);
+                consumer_sync();
+                return (int)sh.fncand;
+            };
             // the threshold key for one search: mode 0 (top-k: the `need`-th largest element) or
             // mode 1 (top-p: the smallest key whose mass above is below P = p_frac of the mass at or
             // above floor_key). Returns the key, the mass above it (`mass_above`) and the mass of its
@@ -2011,10 +2036,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // candidates already hold every element at or above floor_key, so the whole search
             // runs on chip; on return it is >= 0 when that holds for this search's kept elements.
             auto search = [&](int64_t t, int j, int mode, unsigned long long need, double p_frac, uint32_t floor_key,
-                              float MC, bool keep_above, int& ncand, uint32_t& key_out, double& mass_above,
-                              double& mass_at) -> bool {
+                              float MC, float S, bool keep_above, bool& try_slice, int& ncand, uint32_t& key_out,
+                              double& mass_above, double& mass_at) -> bool {
                 constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
-                const int src0 = ncand;
+                int src0 = ncand;
+                // Top-k: first try the top slice of logits whose mass exp2(z*c - MC) is at least
+                // 1.0625 S / kCandCap (at most about kCandCap of them, S the row's softmax sum): when it
+                // holds k elements it holds the k-th largest and everything above it, and the whole
+                // search (and a top-p search after it) runs on chip. Else (too few, or too many) the
+                // row is searched as below, and the request stops trying.
+                bool top_slice = false;
+                if (src0 < 0 && mode == 0 && try_slice && need * 17 <= (unsigned long long)kCandCap * 16) {
+                    const float zt = (__log2f(S * (1.0625f / (float)kCandCap)) + MC) / c;
+                    const int n = slice_pass(t, j, zt);
+                    if (n <= kCandCap && (unsigned long long)n >= need) { src0 = n; top_slice = true; }
+                    else try_slice = false;
+                }
                 // on chip, the first pass takes counts and masses (the candidates are few)
                 hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu, src0,
                           src0 >= 0 ? 3 : (mode == 0 ? 1 : 2));
@@ -2030,7 +2067,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 double above = sh.fsel_mass;                      // (first top-k pass: not summed)
                 need -= n_above;
                 int src = src0;
-                if (src0 < 0) ncand = -1;
+                if (top_slice) ncand = src0;             // every element at or above this search's key
+                else if (src0 < 0) ncand = -1;
                 const bool all = src0 < 0 && keep_above && n_above + n_bin <= (unsigned long long)kCandCap;
                 const int n = collect_pass(t, j, b0, all, floor_key, MC, src0);
                 if (src0 < 0 && n <= kCandCap) {
@@ -2067,20 +2105,23 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 mass_at = at;
                 return true;
             };
-            auto filter_row = [&](int64_t t, int j, float MC, uint32_t& kt, float& S_keep) -> bool {
+            auto filter_row = [&](int64_t t, int j, float MC, float S, uint32_t& kt, float& S_keep) -> bool {
                 uint32_t floor_key = 0u;
                 double keep = 0.0, above = 0.0, at = 0.0;
                 int ncand = -1;                                  // candidates hold every kept element
                 bool cut_k = false;
                 if (fk > 0) {
                     uint32_t key;
-                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, fp < 1.f, ncand, key, above, at);
+                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, S, fp < 1.f, try_slice, ncand, key,
+                                   above, at);
                     if (cut_k) { floor_key = key; keep = above + at; }
                 }
                 bool cut_p = false;
                 if (fp < 1.f) {
                     uint32_t key;
-                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, false, ncand, key, above, at);
+                    bool no_slice = false;
+                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, S, false, no_slice, ncand, key, above,
+                                   at);
                     if (cut_p) { floor_key = key; keep = above + at; }
                 }
                 kt = floor_key;
@@ -2330,7 +2371,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 uint32_t kt = 0u;
                 float S_keep = 0.f;
                 bool cut = false;
-                if constexpr (kFilt) cut = filt && r.m > -INFINITY && filter_row(t, j, r.m * c, kt, S_keep);
+                if constexpr (kFilt) cut = filt && r.m > -INFINITY && filter_row(t, j, r.m * c, r.S, kt, S_keep);
                 bool stop;
                 float MC, S_mc;
                 const int code = decide(j, r, stop, MC, S_mc, cut, kt, S_keep);

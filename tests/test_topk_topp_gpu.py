@@ -99,24 +99,31 @@ def test_bad_top_p_is_flagged(cuda):
 
 
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
-@pytest.mark.parametrize("route", ["streamed_digits", "bin_on_chip", "all_kept_on_chip"])
+@pytest.mark.parametrize("route", ["streamed_digits", "bin_on_chip", "all_kept_on_chip", "top_p_peaked"])
 def test_threshold_search_routes(cuda, dtype, route):
     """Rows of 65536 logits that drive each route of the threshold search: a near-flat row whose
     chosen mass bin holds far more elements than fit on chip (every digit pass streams the row), a
-    top-k of 3000 (the chosen bin fits on chip, the elements above it do not), and a small top-k
-    followed by top-p (every kept element fits on chip, so the top-p search streams nothing)."""
+    top-k of 3000 (above the top-slice limit; the chosen bin fits on chip, the elements above it do
+    not), a small top-k followed by top-p (the top slice of logits holds every kept element, so the
+    top-p search streams nothing), and top-p alone on peaked rows (a small chosen bin, its digits on
+    chip)."""
     B, V = 24, 65536
-    rng = np.random.default_rng({"streamed_digits": 11, "bin_on_chip": 12, "all_kept_on_chip": 13}[route])
+    rng = np.random.default_rng({"streamed_digits": 11, "bin_on_chip": 12, "all_kept_on_chip": 13,
+                                 "top_p_peaked": 14}[route])
+    temperature = "uniform(0.5,1.2)"
     if route == "streamed_digits":
         sigma, tk, tp = 0.02, rng.choice(np.array([0, 5000, 20000], np.int32), B), \
             rng.choice(np.array([1.0, 0.3, 0.5, 0.7], np.float32), B)
     elif route == "bin_on_chip":
         sigma, tk, tp = 3.0, np.full(B, 3000, np.int32), rng.choice(np.array([1.0, 0.9, 0.97], np.float32), B)
-    else:
+    elif route == "all_kept_on_chip":
         sigma, tk, tp = 3.0, rng.choice(np.array([10, 50, 300], np.int32), B), \
             rng.choice(np.array([1.0, 0.5, 0.8, 0.95], np.float32), B)
+    else:
+        sigma, tk, tp = 3.0, np.zeros(B, np.int32), rng.choice(np.array([0.5, 0.8, 0.9], np.float32), B)
+        temperature = "uniform(0.4,0.6)"
     w = W.make_batch(65, name=f"topkp_route_{route}_{dtype}", B=B, V=V, k=(1, 4), logits_dtype=dtype,
-                     logit_sigma=sigma, temperature="uniform(0.5,1.2)", q_mode="half", draft_sigma=0.4,
+                     logit_sigma=sigma, temperature=temperature, q_mode="half", draft_sigma=0.4,
                      top_k=tk, top_p=tp)
     rep, got, ref = _check(w, cuda)
     assert rep.compared_tokens > 40
