@@ -127,3 +127,16 @@ def test_threshold_search_routes(cuda, dtype, route):
                      top_k=tk, top_p=tp)
     rep, got, ref = _check(w, cuda)
     assert rep.compared_tokens > 40
+
+
+def test_largest_filtered_vocabulary(cuda):
+    """V = 2^20, the widest row a filtered launch takes, with near-flat logits: about 2^20 elements
+    share one mass bin, where the 32-bit sums of 12-bit mass halves reach their bound (the top-k
+    request's digit passes sum the masses of that bin). The top-p request runs too, but every
+    element there carries about 1e-6 of the mass, so its boundary lies inside the excluded band."""
+    B, V = 2, 1 << 20
+    w = W.make_batch(66, name="topkp_V2p20", B=B, V=V, k=2, logit_sigma=0.001, temperature=1.0, q_mode="all",
+                     draft_sigma=0.0005, top_k=np.array([0, 300000], np.int32),
+                     top_p=np.array([0.5, 1.0], np.float32))
+    rep, got, ref = _check(w, cuda)
+    assert rep.compared_tokens >= 1

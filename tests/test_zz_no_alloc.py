@@ -80,3 +80,41 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, monkeypatch):
     ref = oracle.verify(w)
     rep = parity.compare(w, na_calls[0], ref)
     assert rep.ok, rep.summary()
+
+
+@pytest.mark.gpu
+def test_noalloc_with_top_k_top_p_matches_workspace_entry_point(lib, monkeypatch):
+    """A filtered batch of 400 requests (scheduled: one CTA per filtered request) through both
+    entry points: identical outputs, and equal to the oracle."""
+    import torch
+
+    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)
+    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    torch.cuda.set_device(0)
+    cuda = "cuda:0"
+    rng = np.random.default_rng(42)
+    B = 400
+    w = W.make_batch(42, name="noalloc_filters_B400", B=B, V=4096, k=(0, 5), logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
+                     mask_density=0.1, mask_run_len=16,
+                     top_k=rng.choice(np.array([0, 1, 20, 200], np.int32), B),
+                     top_p=rng.choice(np.array([1.0, 0.5, 0.9], np.float32), B))
+    assert _native.launch_config(w.V, 0, B=w.B)["kernels_with_workspace"] == 2
+    dev = device.device_tensors(w, cuda)
+    ws_out = _outputs(w, cuda, workspace=True)
+    na_out = _outputs(w, cuda, workspace=False)
+    device.verify(w, dev, ws_out)
+    _native.specdec_verify_noalloc(
+        dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
+        w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
+        na_out.out_tokens, na_out.out_num_accepted, na_out.counters, na_out.status,
+        na_out.diag_accept_prob, na_out.diag_row_stats, telemetry=na_out.telemetry,
+        top_k=dev["top_k"], top_p=dev["top_p"])
+    torch.cuda.synchronize()
+    ws, na = ws_out.numpy(), na_out.numpy()
+    for k in ("out_tokens", "out_num_accepted", "status", "counters", "telemetry"):
+        assert np.array_equal(na[k], ws[k]), k
+    for k in ("diag_accept_prob", "diag_row_stats"):
+        assert np.array_equal(na[k], ws[k], equal_nan=True), k
+    rep = parity.compare(w, na, oracle.verify(w))
+    assert rep.ok, rep.summary()
