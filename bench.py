@@ -23,6 +23,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -270,6 +271,41 @@ def cpu_oracle_sample(w: W.Workload, budget_s: float):
     oracle.verify(sub)
     dt = time.perf_counter() - t0
     return sub, dt
+
+
+def cpu_oracle_threads(sub: W.Workload, threads: int) -> float:
+    """The same oracle sample split into `threads` request ranges, one host thread each (the oracle's
+    C call releases the interpreter lock); returns the wall time of the parallel pass."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    parts = [sub.subset(c) for c in np.array_split(np.arange(sub.B), threads) if len(c)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(len(parts)) as ex:
+        list(ex.map(oracle.verify, parts))
+    return time.perf_counter() - t0
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+def nominal_bytes(w: W.Workload) -> int:
+    """The tensors' full sizes: logits + draft probs + bitmask + noise (every row, every id)."""
+    es = 2 if w.logits_dtype == W.BF16 else 4
+    n = w.T * w.V * es + w.T * w.V * 4
+    if w.draft_probs is not None:
+        n += w.N * w.V * 4
+    if w.bitmask is not None:
+        n += w.T * ((w.V + 31) // 32) * 4
+    return int(n)
 
 
 def run_reference(args, world, rank):
@@ -595,11 +631,16 @@ def main():
         e2e = {"value": R_all * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.e2e_steps}
 
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sub, dt = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": sub.N / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"first {sub.B} of {w.B} requests ({sub.N} drafts), one pass, {dt:.1f} s"}
+               "sample": f"first {sub.B} of {w.B} requests ({sub.N} drafts), one pass, {dt:.1f} s",
+               "cpu": cpu_model()}
+        nthreads = os.cpu_count() or 1
+        dtp = cpu_oracle_threads(sub, nthreads)
+        cpu_all = {"value": sub.N / dtp, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                   "sample": f"the same sample split over {nthreads} host threads, {dtp:.2f} s", "cpu": cpu_model()}
 
     if rank == 0:
         shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0, B=w.B)
@@ -620,6 +661,11 @@ def main():
                          "whole_row_gbs": achieved_rows, "whole_row_frac": achieved_rows / peak},
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
+            "emitted_tokens_per_s": int((res["out_tokens"] >= 0).sum()) / mean_s,
+            "mean_acceptance_length": 1.0 + (int(ctr[3]) / args.steps) / max(w.B, 1),
+            "nominal": {"bytes_per_launch": nominal_bytes(w), "effective_gbs": nominal_bytes(w) / mean_s / 1e9,
+                        "note": "full logits + draft probs + bitmask + noise tensors over the kernel time"},
             "gpu_launches": args.steps * shape["kernels_with_workspace"],
             "clocks": clocks,
             "kernel_ms": {"median": statistics.median(kernel_ms), "min": min(kernel_ms), "max": max(kernel_ms)},
