@@ -26,7 +26,7 @@
 namespace {
 
 constexpr int kNgramThreads = 256;
-constexpr int kTile = 8192;                    // window ends per shared-memory tile
+constexpr int kTile = 4096;                    // window ends per shared-memory tile (16 KB: 8 CTAs per SM)
 constexpr int kHalo = SPECDEC_NGRAM_MAX_N;     // tokens before a tile that its windows may reach
 constexpr int kSmemBytes = (kHalo + kTile) * 4;
 
