@@ -38,6 +38,7 @@
 #include <cstring>
 #include <ctime>
 #include <mutex>
+#include <type_traits>
 
 #include "specdec.h"
 
@@ -1208,6 +1209,126 @@ __device__ __forceinline__ void draw_lazy(Part& p, const float* z, const float* 
     }
 }
 
+// ---- one-pass race over a row that needs no acceptance ratio first: the bonus row of a sampled
+// request, or a row of a sampled model-free request. The bonus token is argmax_i p_i / E_i and
+// a model-free recovered token argmax_{i != x} p_i / E_i; both only compare ratios of
+// exp2(z * c) terms, so they need no normaliser and fold in the same pass as the softmax
+// statistics (which still give p(x) for the acceptance test). The terms are kept against a
+// running reference mc that is a whole number, so raising it rescales the sum and the best score
+// by an exact power of two (Part.flag carries mc's bits through the reductions).
+
+// 2^d for a whole number d <= 0 (0 below 2^-126)
+__device__ __forceinline__ float pow2_int(float d)
+{
+    return d < -126.f ? 0.f : __int_as_float(((int)d + 127) << 23);
+}
+
+// Raise a race partial's reference to cover a new maximum bm (finite, above p.m).
+__device__ __forceinline__ void race_raise(Part& p, float& mc, float bm, float c)
+{
+    const float nmc = ceilf(bm * c);
+    if (p.m == -INFINITY) {
+        mc = nmc;
+    } else if (nmc > mc) {
+        const float f = pow2_int(mc - nmc);
+        p.S *= f;
+        if (p.best > 0.f) {
+            p.best *= f;
+            if (!(p.best > 0.f)) { p.best = -INFINITY; p.idx = INT_MAX; }
+        }
+        mc = nmc;
+    }
+    p.m = bm;
+}
+
+// Race fold of NB groups (ids base + u * stride + e, increasing) whose max is bm; xslot = the
+// excluded draft token's position or -1.
+template <int NB, int VE>
+__device__ __forceinline__ void race_lazy(Part& p, float& mc, const float* z, const float* E, float bm, int base,
+                                          int stride, int xslot, float c)
+{
+    constexpr int N = NB * VE;
+    if (!(bm > -INFINITY)) return;
+    if (bm > p.m) race_raise(p, mc, bm, c);
+    float e[N], sc[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = ex2(fmaf(z[i], c, -mc));             // z = -inf gives 0
+    p.S += tree_sum<N>(e);
+#pragma unroll
+    for (int i = 0; i < N; ++i) sc[i] = (e[i] > 0.f && i != xslot) ? e[i] * fast_rcp(E[i]) : -1.f;
+    const float bs = tree_max<N>(sc);
+    if (bs > 0.f && bs > p.best) {               // strict: an equal earlier best keeps its lower id
+        int id = INT_MAX;
+#pragma unroll
+        for (int u = NB - 1; u >= 0; --u)
+#pragma unroll
+            for (int e2 = VE - 1; e2 >= 0; --e2) id = (sc[u * VE + e2] == bs) ? base + u * stride + e2 : id;
+        p.best = bs;
+        p.idx = id;
+    }
+}
+
+// Race fold of N candidates with ids ids[i] (in any order, -1 = unused slot); id x is excluded.
+template <int N>
+__device__ __forceinline__ void race_batch(Part& p, float& mc, const float* z, const float* E, const int* ids, int x,
+                                           float c)
+{
+    const float bm = tree_max<N>(z);
+    if (!(bm > -INFINITY)) return;
+    if (bm > p.m) race_raise(p, mc, bm, c);
+    float e[N], sc[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = ex2(fmaf(z[i], c, -mc));
+    p.S += tree_sum<N>(e);
+#pragma unroll
+    for (int i = 0; i < N; ++i) sc[i] = (e[i] > 0.f && ids[i] != x) ? e[i] * fast_rcp(E[i]) : -1.f;
+    const float bs = tree_max<N>(sc);
+    if (bs > 0.f && bs >= p.best) {
+        int id = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < N; ++i) id = (sc[i] == bs) ? min(id, ids[i]) : id;
+        if (bs > p.best || id < p.idx) { p.best = bs; p.idx = id; }
+    }
+}
+
+// Combine race partial b into a: both rescaled to the larger reference (exact powers of two).
+__device__ __forceinline__ void combine_race(Part& a, const Part& b)
+{
+    a.zx = fmaxf(a.zx, b.zx);
+    if (!(b.m > -INFINITY)) return;
+    if (!(a.m > -INFINITY)) { a.m = b.m; a.S = b.S; a.best = b.best; a.idx = b.idx; a.flag = b.flag; return; }
+    const float ma = __int_as_float(a.flag), mb = __int_as_float(b.flag), M = fmaxf(ma, mb);
+    const float fa = pow2_int(ma - M), fb = pow2_int(mb - M);
+    a.S = a.S * fa + b.S * fb;
+    float ba = a.best > 0.f ? a.best * fa : -INFINITY, bb = b.best > 0.f ? b.best * fb : -INFINITY;
+    int ia = a.idx, ib = b.idx;
+    if (!(ba > 0.f)) { ba = -INFINITY; ia = INT_MAX; }
+    if (!(bb > 0.f)) { bb = -INFINITY; ib = INT_MAX; }
+    if (bb > ba || (bb == ba && ib < ia)) { ba = bb; ia = ib; }
+    a.best = ba;
+    a.idx = ia;
+    a.m = fmaxf(a.m, b.m);
+    a.flag = __float_as_int(M);
+}
+
+template <bool kRace>
+__device__ __forceinline__ void combine_any(Part& a, const Part& b, float c)
+{
+    if constexpr (kRace) combine_race(a, b);
+    else combine(a, b, c);
+}
+
+template <bool kRace>
+__device__ __forceinline__ Part warp_reduce_any(Part p, float c)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Part o = shfl_part(p, off);
+        combine_any<kRace>(p, o, c);
+    }
+    return p;
+}
+
 template <typename ET>
 struct Producer {
     const Args& a;
@@ -1366,15 +1487,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             Producer<ET> pr(a, sh, ring, lane, lo, hi);
             // a filtered request streams its rows again for the threshold search, so nothing of
             // the next row may sit in the ring before a row's decisions are all taken
-            const int spec_r = (kFilt && request_filter(a, b).on) ? 0 : spec;
+            const bool filt_on = kFilt && request_filter(a, b).on;
+            const int spec_r = filt_on ? 0 : spec;
+            // race rows (one pass over logits + noise, the consumers' test): the bonus row of an
+            // unfiltered sampled request and every row of an unfiltered sampled model-free one
+            const bool race_req = !request_greedy(a, b) && !filt_on;
+            const bool qm = a.q != nullptr && (a.has_q == nullptr || a.has_q[b] != 0);
+            const int nrace_chunks = (hi - lo + G::draw_ids(false) - 1) / G::draw_ids(false);
+            auto race_row = [&](int j) { return race_req && (j == rs.k || !qm); };
+            auto issue = [&](int j, int c) {
+                if (race_row(j)) pr.draw_chunk(rs.row0 + j, (int64_t)rs.d0 + j, c, false);
+                else pr.row_chunk(rs.row0 + j, c);
+            };
             uint32_t dec_round = 0;
             int issued_next = 0;
             for (int j = 0; j <= rs.k; ++j) {
                 const int64_t t = rs.row0 + j;
-                for (int c = issued_next; c < nrow_chunks; ++c) pr.row_chunk(t, c);
+                const int nch = race_row(j) ? nrace_chunks : nrow_chunks;
+                for (int c = issued_next; c < nch; ++c) issue(j, c);
                 issued_next = 0;
                 if (j < rs.k) {
-                    for (int c = 0; c < spec_r; ++c) pr.row_chunk(t + 1, c);
+                    // (a race row has at least as many chunks as a plain one: spec_r < either)
+                    for (int c = 0; c < spec_r; ++c) issue(j + 1, c);
                     issued_next = spec_r;
                 }
                 if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
@@ -1480,18 +1614,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // with the other CTAs of the request: consumer thread i stores this CTA's partial into
         // CTA i's slot and arrives on CTA i's barrier; every CTA folds the NC partials in rank
         // order, so all of them hold bit-identical results.
-        auto reduce_cta = [&](Part p) -> Part {
-            p = warp_reduce(p, c);
+        // (race partials -- see race_raise -- combine by their own rule: `race` is a
+        // std::integral_constant<bool, ...>)
+        auto reduce_cta = [&](Part p, auto race) -> Part {
+            constexpr bool kR = decltype(race)::value;
+            p = warp_reduce_any<kR>(p, c);
             if (lane == 0) sh.wpart[par][cw] = p;
             consumer_sync();
             Part r = part_identity();
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) combine(r, sh.wpart[par][w], c);
+            for (int w = 0; w < kConsumerWarps; ++w) combine_any<kR>(r, sh.wpart[par][w], c);
             par ^= 1;
             return r;
         };
-        auto reduce = [&](Part p) -> Part {
-            const Part r = reduce_cta(p);
+        auto reduce_any = [&](Part p, auto race) -> Part {
+            constexpr bool kR = decltype(race)::value;
+            const Part r = reduce_cta(p, race);
             if (NC == 1) return r;
             const int slot = (int)(xround & 1u);
             if (ct < NC) {
@@ -1507,9 +1645,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             if (!mbar_wait_cluster_bounded(smem_addr(&sh.pbar[slot]), (xround >> 1) & 1u)) sh.timed_out = 1;
             ++xround;
             Part q = part_identity();
-            for (int i = 0; i < NC; ++i) combine(q, sh.parts[slot][i], c);
+            for (int i = 0; i < NC; ++i) combine_any<kR>(q, sh.parts[slot][i], c);
             return q;
         };
+        auto reduce = [&](Part p) -> Part { return reduce_any(p, std::false_type{}); };
         auto post = [&](int code) {
             if (leader && !sparse) {
                 *reinterpret_cast<volatile int*>(&sh.dec_code) = code;
@@ -1684,6 +1823,61 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         }
                     }
                     draw_batch<U * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
+                }
+                consumer_sync();
+            }
+        };
+        // Sparse race pass over list[0, n) of row t (race rows, see race_raise): logits and noise of
+        // the listed groups, gathered with cp.async in batches sized to the data region, folded into
+        // the softmax statistics and the race that excludes id x (x < 0: none).
+        auto sparse_race = [&](int64_t t, int x, int n, Part& p, float& mc) {
+            constexpr int per = 16 + 4 * VE;
+            constexpr int cap = kDataBytes / per;
+            unsigned char* dl = ring + kDataOff;
+            unsigned char* dn = dl + cap * 16;
+            const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
+            const unsigned char* erow = reinterpret_cast<const unsigned char*>(a.noise + t * (int64_t)a.V);
+            for (int b0 = 0; b0 < n; b0 += cap) {
+                const int nb = min(cap, n - b0);
+                for (int e = ct; e < nb; e += kConsumers) {
+                    const size_t grp = list[b0 + e] >> 8;
+                    cp_async16(smem_addr(dl + e * 16), lrow + grp * 16u);
+#pragma unroll
+                    for (int h = 0; h < VE / 4; ++h)
+                        cp_async16(smem_addr(dn + e * 4 * VE + 16 * h), erow + grp * (4u * VE) + 16u * h);
+                }
+                cp_async_wait_all();
+                consumer_sync();
+                constexpr int U = (VE == 8) ? 1 : 2;
+                for (int e0 = ct; e0 < nb; e0 += kConsumers * U) {
+                    float z[U * VE], ev[U * VE];
+                    int ids[U * VE];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int e = e0 + u * kConsumers;
+                        const bool in = e < nb;
+                        const uint32_t ent = in ? list[b0 + e] : 0u;
+                        const uint32_t bits = ent & 0xffu;
+                        const int grp = (int)(ent >> 8);
+                        const uint32_t ni = Raw<ET>::kNegInf;
+                        unpack_raw<ET>(in ? reinterpret_cast<const uint4*>(dl)[e] : make_uint4(ni, ni, ni, ni), z + u * VE);
+#pragma unroll
+                        for (int h = 0; h < VE / 4; ++h) {
+                            const float4 f = in ? reinterpret_cast<const float4*>(dn + e * 4 * VE)[h] : make_float4(1.f, 1.f, 1.f, 1.f);
+                            ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
+                        }
+#pragma unroll
+                        for (int q = 0; q < VE; ++q) {
+                            z[u * VE + q] = ((bits >> q) & 1u) ? z[u * VE + q] : -INFINITY;
+                            ids[u * VE + q] = in ? grp * VE + q : -1;
+                        }
+                    }
+                    if (x >= 0) {
+#pragma unroll
+                        for (int q = 0; q < U * VE; ++q)
+                            if (ids[q] == x) p.zx = z[q];
+                    }
+                    race_batch<U * VE>(p, mc, z, ev, ids, x, c);
                 }
                 consumer_sync();
             }
@@ -2190,6 +2384,34 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 return code;
             };
 
+            // ---- decision on race row j (see race_raise): the bonus token, or the acceptance test
+            // of model-free draft j with p(x) from the same pass and, on a rejection, the race's
+            // winner (p without the draft token) as the recovered token
+            auto decide_race = [&](int j, const Part& r, bool& stop) -> int {
+                const int64_t t = rs.row0 + j;
+                const int64_t d = (int64_t)rs.d0 + j;
+                const bool bonus = (j == k);
+                stop = true;
+                if (!(r.m > -INFINITY)) {
+                    st |= SPECDEC_ST_EMPTY_MASK_ROW;
+                    if (writer && a.diag_row) { a.diag_row[2 * t] = -INFINITY; a.diag_row[2 * t + 1] = 0.f; }
+                    acc_len = j; emitted = -1;
+                    return kDecDone;
+                }
+                const float mcr = __int_as_float(r.flag);      // the reference of r.S and r.best
+                if (writer && a.diag_row) {
+                    a.diag_row[2 * t] = r.m / T;
+                    a.diag_row[2 * t + 1] = r.S * ex2(fmaf(-r.m, c, mcr));   // S against exp2(m * c)
+                }
+                const int tok = r.idx == INT_MAX ? -1 : r.idx;
+                if (bonus) { emitted = tok; return kDecDone; }
+                const float alpha = (j < g && r.zx > -INFINITY) ? ex2(fmaf(r.zx, c, -mcr)) / r.S : 0.f;
+                if (writer && a.diag_alpha) a.diag_alpha[d] = alpha;
+                if (sh.us[j] < alpha) { if (writer) a.out_tokens[t] = sh.xs[j]; stop = false; return kDecNextRow; }
+                acc_len = j; emitted = tok;
+                return kDecDone;
+            };
+
             // ---- a9/a10: draw pass(es) over the stop / bonus row j
             auto draw_row = [&](int j, int code, float MC, float S_mc, uint32_t kt) {
                 const int64_t t = rs.row0 + j;
@@ -2279,14 +2501,81 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 }
             };
 
+            // race rows (see race_raise; the producer applies the same test): the bonus row of an
+            // unfiltered sampled request and every row of an unfiltered sampled model-free one
+            const bool race_req = !greedy && !filt;
             for (int j = 0; j <= k; ++j) {
                 const int64_t t = rs.row0 + j;
                 const bool bonus = (j == k);
                 const int x = bonus ? -1 : sh.xs[j];
+                const bool race = race_req && (bonus || !qmode);
                 Part p = part_identity();
-                float mc = 0.f;                            // running round(m * c)
+                float mc = 0.f;                            // running round(m * c) (race rows: a whole number)
 
-                if (!sparse) {
+                if (!sparse && race) {
+                    // ---- a2/a3/a5 + a9/a10 dense, one pass: logits, noise and mask words of the slice
+                    const int ids = G::draw_ids(false);
+                    const int nd = (hi - lo + ids - 1) / ids;
+                    for (int ch = 0; ch < nd; ++ch) {
+                        const int s = wait_full();
+                        if (ch == 0) SPECDEC_STAMP(2);
+                        const unsigned char* stg = ring + (size_t)s * kStageBytes;
+                        const uint32_t* sm = reinterpret_cast<const uint32_t*>(stg + G::dmask_off(false));
+                        const float* se = reinterpret_cast<const float*>(stg + G::noise_off(false));
+                        const int i0 = lo + ch * ids;
+                        const int n = min(ids, hi - i0);
+                        const int nvec = (n + VE - 1) / VE;
+                        const int vx = (x >= i0 && x < i0 + n) ? (x - i0) / VE : -1;
+                        constexpr int NB = (VE == 4) ? 4 : 2;
+                        constexpr uint32_t kFull = (1u << VE) - 1u;
+                        for (int vb = ct; vb < nvec; vb += kConsumers * NB) {
+                            uint4 raw[NB];
+                            uint32_t bits[NB];
+                            float ev[NB * VE];
+                            bool full = true;
+                            int xslot = -1;
+#pragma unroll
+                            for (int u = 0; u < NB; ++u) {
+                                const int v = vb + u * kConsumers;
+                                const bool in = v < nvec;
+                                const uint32_t ni = Raw<ET>::kNegInf;
+                                raw[u] = in ? reinterpret_cast<const uint4*>(stg)[v] : make_uint4(ni, ni, ni, ni);
+                                bits[u] = (in && has_mask) ? vec_bits<VE>(sm, true, v) : kFull;
+                                full = full && (bits[u] == kFull);
+#pragma unroll
+                                for (int h = 0; h < VE / 4; ++h) {
+                                    const float4 f = in ? reinterpret_cast<const float4*>(se + v * VE)[h] : make_float4(1.f, 1.f, 1.f, 1.f);
+                                    ev[u * VE + 4 * h] = f.x; ev[u * VE + 4 * h + 1] = f.y; ev[u * VE + 4 * h + 2] = f.z; ev[u * VE + 4 * h + 3] = f.w;
+                                }
+                                if (v == vx) xslot = u * VE + (x - i0) % VE;
+                            }
+                            float z[NB * VE];
+#pragma unroll
+                            for (int u = 0; u < NB; ++u) unpack_raw<ET>(raw[u], z + u * VE);
+                            float bm;
+                            if (full) {
+                                bm = raw_max<ET, NB>(raw, z);
+                            } else {
+#pragma unroll
+                                for (int u = 0; u < NB; ++u)
+#pragma unroll
+                                    for (int e = 0; e < VE; ++e)
+                                        z[u * VE + e] = ((bits[u] >> e) & 1u) ? z[u * VE + e] : -INFINITY;
+                                bm = tree_max<NB * VE>(z);
+                            }
+                            race_lazy<NB, VE>(p, mc, z, ev, bm, i0 + vb * VE, kConsumers * VE, xslot, c);
+                        }
+                        // the draft token's logit, read once by the thread that owns its group
+                        if (vx >= 0 && ct == vx % kConsumers) {
+                            float zz[VE];
+                            Elem<ET>::load(stg, vx, zz);
+#pragma unroll
+                            for (int e = 0; e < VE; ++e)
+                                if (e == (x - i0) % VE) p.zx = zz[e];
+                        }
+                        release(s);
+                    }
+                } else if (!sparse) {
                     // ---- a2/a3/a5/a6 dense: stream the slice chunk by chunk
                     for (int ch = 0; ch < nrow_chunks; ++ch) {
                         const int s = wait_full();
@@ -2348,17 +2637,32 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         const int n = build_list(t, w0, w1);
                         if (w0 == wlo) SPECDEC_STAMP(2);
                         if (n >= 0) {
-                            sparse_stats(t, greedy ? -1 : x, n, p, mc);
-                            if (w1 - w0 == whi - wlo) { listed_row = j; listed_n = n; }   // the whole slice in one list
+                            if (race) sparse_race(t, x, n, p, mc);
+                            else sparse_stats(t, greedy ? -1 : x, n, p, mc);
+                            if (!race && w1 - w0 == whi - wlo) { listed_row = j; listed_n = n; }   // the whole slice in one list
                         } else {
                             for (int s0 = w0; s0 < w1; s0 += G::kSafeWords) {
                                 const int n2 = build_list(t, s0, min(w1, s0 + G::kSafeWords));
-                                sparse_stats(t, greedy ? -1 : x, n2, p, mc);
+                                if (race) sparse_race(t, x, n2, p, mc);
+                                else sparse_stats(t, greedy ? -1 : x, n2, p, mc);
                             }
                         }
                     }
                 }
                 SPECDEC_STAMP(3);
+                if (race) {
+                    p.flag = __float_as_int(p.m > -INFINITY ? mc : -INFINITY);
+                    const Part r = reduce_any(p, std::true_type{});
+                    SPECDEC_STAMP(4);
+                    bool stop;
+                    post(decide_race(j, r, stop));
+                    if (!stop) continue;
+                    // drain the chunks of row j+1 the producer queued before this decision
+                    if (!sparse && j < k)
+                        for (int ch = 0; ch < spec; ++ch) release(wait_full());
+                    acc_len = j;
+                    break;
+                }
                 // each thread's terms were taken against mc = round(m*c); rebase its sum on the
                 // exact m*c (combine() rescales partials by exp2((m_a - m_b) * c))
                 if (!greedy && p.m > -INFINITY) {
@@ -2783,19 +3087,51 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 namespace {
 
-// Device address of g_noalloc_scratch on device `dev`, looked up once per device and cached.
+// The unique id of the calling thread's current context (0: none, or the driver entry points are
+// unavailable). Ids are never reused within a process, unlike context handles, so a context
+// created after cudaDeviceReset (or by the driver API) on the same ordinal has a new one.
+unsigned long long current_context_id()
+{
+    using GetCurrent = int (*)(void**);
+    using GetId = int (*)(void*, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+        (void)cudaGetLastError();
+    });
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == 0 && ctx != nullptr && get_id(ctx, &id) == 0) return id;
+    return 0;
+}
+
+// Device address of g_noalloc_scratch on device `dev` (current), looked up with
+// cudaGetSymbolAddress on the first call in each context and cached with that context's id.
 void* noalloc_scratch(int dev)
 {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    const unsigned long long ctx = current_context_id();
+    if (addr[dev] == nullptr || ctx == 0 || ctx != ctx_of[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
             (void)cudaGetLastError();
             return nullptr;
         }
         addr[dev] = p;
+        ctx_of[dev] = current_context_id();          // the lookup made the primary context current
     }
     return addr[dev];
 }
