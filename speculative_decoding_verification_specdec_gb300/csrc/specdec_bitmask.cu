@@ -88,39 +88,39 @@ specdec_bitmask_scatter_kernel(const int32_t* __restrict__ compact, int64_t comp
     }
 
     // the request's rows as one flat range of (row, 16-byte group) items, kUnroll loads in flight
-    // per thread before their stores (a load-then-store loop waits out one DRAM latency per item)
-    const int64_t rows_left = off < 0 ? 0 : compact_rows - off;        // compact rows it can copy
+    // per thread before their stores (a load-then-store loop waits out one DRAM latency per item).
+    // Item counts are 64-bit: k comes from the caller's offsets and is not bounded. The first
+    // copy_items items are copied, the rest of a listed request's items (rows past the end of the
+    // compact array) are zeroed; an unlisted request's rows are all ones.
+    const int64_t rows_left = off < 0 ? 0 : max((int64_t)0, min(compact_rows - off, (int64_t)k + 1));
     if (vec) {
-        const int n4 = W >> 2;
-        const int items = (k + 1) * n4;                                  // < 2^31: V is bounded on the host
+        const int64_t n4 = W >> 2;
+        const int64_t items = ((int64_t)k + 1) * n4;
+        const int64_t copy_items = rows_left * n4;
         int4* d4 = reinterpret_cast<int4*>(bitmask + t0 * (int64_t)W);
         const int4* s4 = off >= 0 ? reinterpret_cast<const int4*>(compact + off * (int64_t)W) : nullptr;
         constexpr int kUnroll = 8;
-        for (int base = tid; base < items; base += kScatterThreads * kUnroll) {
+        for (int64_t base = tid; base < items; base += (int64_t)kScatterThreads * kUnroll) {
             int4 v[kUnroll];
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int it = base + u * kScatterThreads;
-                const int row = it / n4;
-                // 0: all ones (not constrained), 1: copy, 2: zeros (past the end of the compact rows)
-                const int mode = off < 0 ? 0 : (row < rows_left ? 1 : 2);
-                if (it < items && mode == 1) v[u] = __ldcs(s4 + it);
-                else v[u] = mode == 0 ? make_int4(-1, -1, -1, -1) : make_int4(0, 0, 0, 0);
+                const int64_t it = base + (int64_t)u * kScatterThreads;
+                if (it < items && off >= 0 && it < copy_items) v[u] = __ldcs(s4 + it);
+                else v[u] = off < 0 ? make_int4(-1, -1, -1, -1) : make_int4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
-                const int it = base + u * kScatterThreads;
+                const int64_t it = base + (int64_t)u * kScatterThreads;
                 if (it < items) __stcs(d4 + it, v[u]);
             }
         }
     } else {
-        const int items = (k + 1) * W;
+        const int64_t items = ((int64_t)k + 1) * W;
+        const int64_t copy_items = rows_left * W;
         int32_t* dst = bitmask + t0 * (int64_t)W;
         const int32_t* src = off >= 0 ? compact + off * (int64_t)W : nullptr;
-        for (int it = tid; it < items; it += kScatterThreads) {
-            const int row = it / W;
-            dst[it] = off < 0 ? -1 : (row < rows_left ? src[it] : 0);
-        }
+        for (int64_t it = tid; it < items; it += kScatterThreads)
+            dst[it] = off < 0 ? -1 : (it < copy_items ? src[it] : 0);
     }
 }
 
@@ -132,7 +132,7 @@ extern "C" specdec_status_t specdec_bitmask_scatter(const int32_t* compact, int6
                                                     int32_t* bitmask, void* stream)
 {
     if (B < 0 || V < 1 || n < 0 || compact_rows < 0) return SPECDEC_ERR_INVALID_ARG;
-    if (V > (1 << 26)) return SPECDEC_ERR_UNSUPPORTED;               // (k + 1) * W stays below 2^31
+    if (V > (1 << 26)) return SPECDEC_ERR_UNSUPPORTED;
     if (B == 0) return SPECDEC_OK;
     if (!cu_num_draft || !bitmask || (n > 0 && !constrained) || (compact_rows > 0 && !compact))
         return SPECDEC_ERR_INVALID_ARG;
