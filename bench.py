@@ -12,9 +12,14 @@ value      verified draft tokens / s (R per step / kernel time), inputs resident
            batch: requests are independent, no collective in the data path).
 e2e        the same metric through the public API with page-locked HOST buffers: every step
            copies the step's inputs host->device, verifies, and reads the outputs back.
-roofline   algorithmic bytes per launch / mean kernel time, against the measured HBM copy
-           bandwidth.
-cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the same workload.
+roofline   algorithmic bytes per launch / mean step time, against the measured HBM copy
+           bandwidth. The bytes are whole rows (logits and mask words of rows 0..a_b, the draw
+           row's noise, a rejected draft-model row's q row); the stricter sector-exact count
+           (only the 32-byte sectors holding an allowed id on a masked row) is reported beside it.
+cpu_baseline  the CPU oracle, single-threaded, on a bounded sample of the same workload; when
+           the sample is the whole batch, `parity` compares the last timed step's outputs with
+           the oracle's.
+per_config the smaller recipes (C0-C3) timed the same way, each with its own parity check.
 """
 from __future__ import annotations
 
@@ -60,6 +65,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-recipe lines (C0-C3) of the default large-mixed-batch run")
     ap.add_argument("--ngram", action="store_true",
                     help="time the n-gram proposer (model-free drafter) instead of the verify")
     ap.add_argument("--scatter", action="store_true",
@@ -507,6 +514,96 @@ def run_scatter(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def time_verify(w, dev_in, out, flush, stream, steps, warmup, pg=None, sampler=None):
+    """W untimed warm-up verifies, then `steps` timed ones, each after an L2 flush (outside the
+    events), bracketed by a barrier and a synchronize. Returns the per-step kernel times (ms) and
+    the outputs of the last step; counters and telemetry are those of the timed steps, summed."""
+    import torch
+
+    from speculative_decoding_verification_specdec_gb300 import device
+
+    for _ in range(max(3, warmup)):
+        flush.zero_()
+        device.verify(w, dev_in, out, stream=stream)
+    torch.cuda.synchronize()
+    out.counters.zero_()
+    if out.telemetry is not None:
+        out.telemetry.zero_()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t0")
+    for i in range(steps):
+        flush.zero_()                      # L2 flush between timed steps (outside the events)
+        starts[i].record(stream)
+        device.verify(w, dev_in, out, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("t1")
+    if pg:
+        pg.barrier()
+    return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], out.numpy()
+
+
+def roofline_fracs(w, res, mean_s, peak):
+    """Algorithmic bytes of one launch over the mean step time: whole rows (the headline) and the
+    sector-exact count (only the 32-byte sectors holding an allowed id on a masked row)."""
+    ab = algorithmic_bytes(w, res["out_num_accepted"], res["status"])
+    return ab, ab["row_total"] / mean_s / 1e9, ab["total"] / mean_s / 1e9
+
+
+def step_outputs(res, steps):
+    """The last timed step's outputs with the counters and telemetry of one step."""
+    one = {k: res[k] for k in ("out_tokens", "out_num_accepted", "status")}
+    one["counters"] = np.asarray(res["counters"], dtype=np.uint64) // np.uint64(steps)
+    if res.get("telemetry") is not None:
+        one["telemetry"] = np.asarray(res["telemetry"], dtype=np.uint64) // np.uint64(steps)
+    return one
+
+
+def oracle_parity(w, gpu_step):
+    """The oracle's outputs for the whole batch against one timed step's outputs (the CPU-baseline
+    leg's own oracle run; element by element, with the near-tie exclusions of the parity rules)."""
+    import oracle
+    from oracle import parity
+
+    rep = parity.compare(w, gpu_step, oracle.verify(w))
+    return {"ok": bool(rep.ok), "requests": rep.requests, "excluded_requests": rep.excluded_requests,
+            "compared_tokens": rep.compared_tokens, "token_mismatches": len(rep.token_mismatches),
+            "accepted_mismatches": len(rep.accepted_mismatches), "counters": rep.counter_mismatch or "exact",
+            "telemetry": rep.telemetry_mismatch or "exact"}
+
+
+def per_config_lines(args, dev, flush, stream, peak, check_parity):
+    """The smaller recipes (C0-C3), each timed like the headline workload (fewer steps), with its
+    value, kernel median, roofline fractions and, with the CPU leg, parity of its timed outputs."""
+    from speculative_decoding_verification_specdec_gb300 import _native, device
+
+    steps = max(1, min(args.steps, 200))
+    out_lines = {}
+    for cfg in (0, 1, 2, 3):
+        w = W.config(cfg)
+        dev_in = device.device_tensors(w, dev)
+        out = device.alloc_outputs(w, dev, diag=False, telemetry=True)
+        ms, res = time_verify(w, dev_in, out, flush, stream, steps, args.warmup)
+        mean_s = sum(ms) / len(ms) / 1e3
+        ab, rows_gbs, sect_gbs = roofline_fracs(w, res, mean_s, peak)
+        shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0, B=w.B)
+        e = {"value": w.N / mean_s, "unit": UNIT, "steps": steps, "kernel_ms_median": statistics.median(ms),
+             "ms_per_step": mean_s * 1e3, "frac": rows_gbs / peak, "achieved_gbs": rows_gbs,
+             "sector_exact_frac": sect_gbs / peak, "bytes_per_launch": ab["row_total"],
+             "kernels_per_step": shape["kernels_with_workspace"]}
+        if check_parity:
+            e["parity"] = oracle_parity(w, step_outputs(res, steps))
+        out_lines[w.name] = e
+        del dev_in, out
+    return out_lines
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -546,32 +643,8 @@ def main():
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
-    # warm-up
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        device.verify(w, dev_in, out, stream=stream)
-    torch.cuda.synchronize()
-    out.counters.zero_()
-    if out.telemetry is not None:
-        out.telemetry.zero_()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    sampler.mark("t0")
-    for i in range(args.steps):
-        flush.zero_()                      # L2 flush between timed steps (outside the events)
-        starts[i].record(stream)
-        device.verify(w, dev_in, out, stream=stream)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    sampler.mark("t1")
-    if pg:
-        pg.barrier()
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms, res = time_verify(w, dev_in, out, flush, stream, args.steps, args.warmup, pg=pg, sampler=sampler)
     tot_ms = float(sum(kernel_ms))
-    res = out.numpy()
     ctr = res["counters"]
     R_per_step = int(ctr[0]) // args.steps
     assert R_per_step == w.N, (R_per_step, w.N)
@@ -587,12 +660,10 @@ def main():
     value = R_all * args.steps / (max_ms / 1e3)
     clocks = sampler.stop() if rank == 0 else None
 
-    # roofline of the (single) kernel
-    ab = algorithmic_bytes(w, res["out_num_accepted"], res["status"])
+    # roofline of the step (schedule + verify kernel)
     mean_s = (tot_ms / args.steps) / 1e3
     peak, peak_kind = measured_peaks()
-    achieved = ab["total"] / mean_s / 1e9
-    achieved_rows = ab["row_total"] / mean_s / 1e9
+    ab, achieved_rows, achieved_sect = roofline_fracs(w, res, mean_s, peak)
     traffic = traffic_from_profiles(w.name)
 
     # e2e through the public API with host buffers
@@ -634,7 +705,7 @@ def main():
         e2e = {"value": R_all * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.e2e_steps}
 
-    cpu = cpu_all = None
+    cpu = cpu_all = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sub, dt, reps = cpu_oracle_sample(w, args.cpu_seconds)
         cpu = {"value": sub.N / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -645,6 +716,12 @@ def main():
         dtp = cpu_oracle_threads(sub, nthreads)
         cpu_all = {"value": sub.N / dtp, "unit": UNIT, "cores": nthreads, "kind": "oracle",
                    "sample": f"the same sample split over {nthreads} host threads, {dtp:.2f} s", "cpu": cpu_model()}
+        # the oracle's outputs for the whole batch against the last timed step's
+        parity = oracle_parity(w, step_outputs(res, args.steps))
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config and not args.filters and args.requests == 0 \
+            and args.config == 4:
+        per_config = per_config_lines(args, dev, flush, stream, peak, check_parity=not args.no_cpu_baseline)
 
     if rank == 0:
         shape = _native.launch_config(w.V, 1 if w.logits_dtype == W.BF16 else 0, B=w.B)
@@ -656,13 +733,21 @@ def main():
                        "l2": "flushed between timed steps (268 MB write)",
                        "launch": {"grid_ctas": w.B * shape["ctas_per_request"], **shape},
                        "per_rank": "independent batch per rank (requests shard with no exchange)"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+            "roofline": {"bound": "hbm", "achieved": achieved_rows, "peak": peak, "unit": "GB/s",
+                         "frac": achieved_rows / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "kernel": "specdec_verify_stream_kernel",
                          "time": ("whole step: request-schedule kernel + verify kernel"
                                   if shape["kernels_with_workspace"] == 2 else "verify kernel"),
-                         "algorithmic_bytes_per_launch": ab,
-                         "whole_row_gbs": achieved_rows, "whole_row_frac": achieved_rows / peak},
+                         "bytes": ("algorithmic, whole rows: logits and mask words of rows 0..a_b, the draw "
+                                   "row's noise, a rejected draft-model row's q row, q(x) of the tested "
+                                   "drafts, the per-request arrays and outputs"),
+                         "algorithmic_bytes_per_launch": ab["row_total"],
+                         "sector_exact_gbs": achieved_sect, "sector_exact_frac": achieved_sect / peak,
+                         "sector_exact_bytes": ab,
+                         "sector_exact_note": ("stricter count: on a masked row only the 32-byte sectors "
+                                               "holding an allowed id")},
+            "parity": parity,
+            "per_config": per_config,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
