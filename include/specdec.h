@@ -100,7 +100,7 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  collect the chosen bin (on chip when it holds at most 2048 elements, else one
  *                  more pass per 8-bit digit of its keys: at most 2 for bf16 logits, 4 for fp32).
  *                  The result does not depend on the route. V > 2^20, or the slice-resident
- *                  cluster kernel (SPECDEC_KERNEL=cluster), with either of them:
+ *                  cluster kernel (specdec_set_launch_options), with either of them:
  *                  SPECDEC_ERR_UNSUPPORTED.
  *   uniforms       [T] fp32 in [0, 1); draft j of request b is accepted iff
  *                  uniforms[t(b,j)] < alpha (strict). Entries at bonus rows are unused.
@@ -140,7 +140,11 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *   workspace_bytes its size in bytes.
  *   stream         a cudaStream_t (NULL = legacy default stream).
  *
- * Rows after a request's first rejection are never read.
+ * Rows after a request's stop row a_b (its first rejection, or the bonus row) are never used: no
+ * output depends on them. At the byte level, a request whose bitmask is absent or dense may read
+ * the first two ring chunks (at most 2 x 32 KB) of row a_b + 1, queued before the decision on
+ * row a_b and discarded unused; a request with a sparse bitmask prefetches the mask words of all
+ * its rows into L2 when it starts. Nothing else of a later row is read.
  * Returns SPECDEC_OK once the kernel is queued; data errors land in status[].
  * Errors: SPECDEC_ERR_INVALID_ARG (nothing launched, nothing written) for a NULL required
  * pointer (draft_ids may be NULL), B < 0, V < 1, max_k outside [0, SPECDEC_KMAX], or a pointer not aligned to its
@@ -151,10 +155,9 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  * Kernels: by default each request is verified by a cluster of G CTAs (G = 1 for large
  * batches, up to 4 for small ones), each streaming its slice of every row through a ring of
  * 32 KB shared-memory stages filled by bulk async copies; requests whose bitmask allows few ids
- * gather only the allowed 16-byte groups instead. Setting the environment variable
- * SPECDEC_KERNEL=cluster selects the alternative kernel that keeps a slice of every row resident
- * in shared memory; SPECDEC_CTAS_PER_REQUEST=G forces G; SPECDEC_SCHEDULE=1 (0) forces the request
- * schedule on (off) whenever a workspace is given. All shapes compute identical results.
+ * gather only the allowed 16-byte groups instead. specdec_set_launch_options (below) selects the
+ * alternative kernel that keeps a slice of every row resident in shared memory, forces G, or
+ * forces the request schedule on or off. All shapes compute identical results.
  */
 specdec_status_t specdec_verify(
     const void* target_logits, specdec_dtype_t logits_dtype,
@@ -199,7 +202,10 @@ specdec_status_t specdec_verify(
  *   Zeroing: nothing in the scratch has to start at zero; each call writes every entry it reads.
  *   Set-up: the first call with B > 0 on a device looks the array's address up with
  *   cudaGetSymbolAddress (once per device, then cached; SPECDEC_ERR_CUDA if that fails). Make
- *   that first call on each device before any stream capture begins on it.
+ *   that first call on each device before any stream capture begins on it. The cache is keyed
+ *   on the current context's unique id as well: after cudaDeviceReset, or in a context the
+ *   caller created with the driver API, the next call looks the address up again (so make that
+ *   call outside stream capture too).
  *   Concurrency: all calls on a device share the one array. Two calls that overlap in time (on
  *   different streams, or from host threads whose calls are not stream-ordered) race on it, and
  *   the outputs and counters of both are then undefined. Queue such calls on one stream, or use
@@ -289,6 +295,31 @@ specdec_status_t specdec_bitmask_scatter(const int32_t* compact, int64_t compact
  * stream reports an error.
  */
 specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
+
+/*
+ * specdec_set_launch_options -- for comparison and test runs: override the launch choices the
+ * library otherwise makes by itself. No step of the method depends on them; every choice
+ * computes identical results. Process-wide; set it between calls (a call in flight on another
+ * host thread may see either setting). The initial values come once per process from the
+ * environment (SPECDEC_KERNEL=cluster|stream, SPECDEC_CTAS_PER_REQUEST=G,
+ * SPECDEC_SCHEDULE=1|0); no call reads the environment after that.
+ *   kernel            -1: automatic (the streaming kernel); 0: streaming kernel; 1: the
+ *                     slice-resident cluster kernel (a slice of every row kept in shared memory
+ *                     by a cluster of CTAs per request; slower, kept as an independent
+ *                     decomposition of the same computation for cross-checks).
+ *   ctas_per_request  -1: automatic; 1..16: CTAs per request (the cluster size).
+ *   schedule          -1: automatic (when the batch exceeds one wave of resident CTAs);
+ *                     0: never; 1: always, whenever a workspace is given.
+ *   wait_limit_us     -1: 2 s; 0..2000000: the limit, in microseconds, of every wait of the
+ *                     streaming kernel on one of its barriers (a test sets 0 to make the waits
+ *                     expire). When a wait expires the CTA issues no more copies, its other waits
+ *                     give up at once, it waits (at most 1 s more) for the copies already in
+ *                     flight, and the request gets SPECDEC_ST_DEVICE_TIMEOUT; its other outputs
+ *                     are then undefined. Nothing traps or hangs, and later calls are unaffected.
+ * Returns SPECDEC_ERR_INVALID_ARG (nothing changed) for a value outside those ranges.
+ */
+specdec_status_t specdec_set_launch_options(int32_t kernel, int32_t ctas_per_request, int32_t schedule,
+                                            int32_t wait_limit_us);
 
 /* Bytes of workspace specdec_verify uses for B requests of vocabulary size V (0 if B or V <= 0):
  * the request order (int32 per request) and one cost byte per request. */

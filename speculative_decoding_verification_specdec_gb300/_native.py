@@ -31,7 +31,7 @@ ST_BAD_TOP_P = 64
 
 EXPORTED = ("specdec_verify", "specdec_verify_noalloc", "specdec_wait", "specdec_status_string",
             "specdec_launch_config", "specdec_workspace_size", "specdec_ngram_propose",
-            "specdec_bitmask_scatter")
+            "specdec_bitmask_scatter", "specdec_set_launch_options")
 NGRAM_MAX_N = 64                        # SPECDEC_NGRAM_MAX_N
 NOALLOC_MAX_REQUESTS = 16384            # SPECDEC_NOALLOC_MAX_REQUESTS
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specdec_status_string.argtypes = [ctypes.c_int]
     lib.specdec_launch_config.restype = ctypes.c_int
     lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
+    lib.specdec_set_launch_options.restype = ctypes.c_int
+    lib.specdec_set_launch_options.argtypes = [i32, i32, i32, i32]
     _lib = lib
     return lib
 
@@ -87,6 +89,19 @@ def launch_config(V: int, dtype: int, B: int = 1024) -> dict:
         raise SpecdecError(rc, "specdec_launch_config")
     return {"ctas_per_request": c.value, "threads_per_cta": t.value, "smem_bytes": s.value,
             "slice_ids": w.value, "kernels_with_workspace": k.value}
+
+
+_KERNELS = {None: -1, "stream": 0, "cluster": 1}
+
+
+def set_launch_options(kernel: Optional[str] = None, ctas_per_request: Optional[int] = None,
+                       schedule: Optional[bool] = None, wait_limit_us: Optional[int] = None) -> None:
+    """specdec_set_launch_options: None leaves a choice to the library."""
+    rc = load().specdec_set_launch_options(_KERNELS[kernel], -1 if ctas_per_request is None else int(ctas_per_request),
+                                           -1 if schedule is None else int(bool(schedule)),
+                                           -1 if wait_limit_us is None else int(wait_limit_us))
+    if rc != SPECDEC_OK:
+        raise SpecdecError(rc, "specdec_set_launch_options")
 
 
 def workspace_size(B: int, V: int) -> int:

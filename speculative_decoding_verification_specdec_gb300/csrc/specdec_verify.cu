@@ -6,22 +6,30 @@
  * j = 0, 1, ... of the target logits in order -- grammar bitmask, temperature softmax
  * statistics, acceptance of draft j (uniform draw below min(1, p/q), p(x) for a one-hot
  * model-free draft, argmax equality when greedy) -- until the first rejection or the
- * bonus row; there one more pass draws the recovered / bonus token as
- * argmax_i w_i / E_i (exponential race) with w = max(p - q, 0), p without the draft
- * token, or p. Rows after the stop row are never read.
+ * bonus row; there the recovered / bonus token is drawn as argmax_i w_i / E_i (exponential
+ * race) with w = max(p - q, 0), p without the draft token, or p. Only w = max(p - q, 0) needs the
+ * row's normaliser first and takes a second pass over the stop row; the other two fold into the
+ * row's own pass. No output depends on a row after the stop row (the streaming kernel may have
+ * fetched up to two chunks of the next one before the decision; they are discarded).
  *
- * GB300 mapping:
- *   - one thread-block cluster per request; its G CTAs split every vocabulary row into
- *     contiguous slices of `slice_units * 128` ids;
- *   - a CTA stages its slice of a row in shared memory with bulk async copies
- *     (cp.async.bulk, the TMA engine) in kChunks pieces, each completing on its own
- *     mbarrier, so arithmetic starts as soon as the first piece lands; the slice stays
- *     on chip for the draw pass, so the stop row is read from HBM once;
- *   - per-row results (max/sum of the online softmax, the argmax, the draft's logit) are
- *     combined across the cluster through distributed shared memory, and every CTA
- *     takes the same accept/reject decision;
- *   - the draw pass streams only the exponential noise (and q on a rejected draft-model
- *     row) with 128-bit loads, and skips 16-byte groups the bitmask fully forbids.
+ * GB300 mapping (the streaming kernel, used by default):
+ *   - one CTA per request (a thread-block cluster of up to 4 CTAs on small batches, each owning a
+ *     contiguous slice of every row); warp 0 is a producer whose lane 0 streams 32 KB chunks of
+ *     the rows (logits and mask words; logits, noise, q and mask words for a draw) with bulk async
+ *     copies (cp.async.bulk, the TMA engine) into a 3-stage shared-memory ring, each stage with
+ *     "full" and "empty" mbarriers; 8 consumer warps fold each chunk with 128-bit shared-memory
+ *     reads (online max / sum with ex2.approx, lazy argmax ids, the race score w / E);
+ *   - at the end of a row the consumers reduce (redux.sync and shuffles in each warp, then the
+ *     warps' partials in order; DSMEM partials across a cluster), every thread takes the same
+ *     decision, and posts it to the producer, which has already queued the next row's first
+ *     chunks so HBM keeps streaming across the decision;
+ *   - a request whose bitmask allows few ids gathers only the allowed 16-byte groups (cp.async)
+ *     after listing them from the mask words;
+ *   - with a workspace, a one-CTA kernel first orders the requests heaviest first.
+ * The first design, kept as an independent cross-check of the same computation
+ * (specdec_verify_kernel, selected with specdec_set_launch_options): a cluster of CTAs per
+ * request keeps its slices of the current row in shared memory, so the draw pass re-reads only
+ * noise and q; it is about 2x slower and has no top-k / top-p.
  * No tensor cores: nothing here is a contraction. Everything is fp32 (bf16 logits are
  * widened exactly); exp uses the ex2.approx hardware instruction on pre-scaled inputs.
  *
@@ -37,6 +45,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <ctime>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -55,9 +64,16 @@ extern "C" int specdec_trace_set(void* buffer)
     int trace_n_ = 0;                                                                              \
     const bool trace_on_ = (on);                                                                   \
     unsigned long long* trace_ = g_specdec_trace ? g_specdec_trace + (size_t)(req) * 64 : nullptr;
+// -DSPECDEC_TRACE_LIGHT keeps only the first and last stamp of each request (tags 0 and 7), so
+// the timing of the phases in between is not disturbed.
+#ifdef SPECDEC_TRACE_LIGHT
+#define SPECDEC_TRACE_KEEP(tag) ((tag) == 0 || (tag) == 7)
+#else
+#define SPECDEC_TRACE_KEEP(tag) true
+#endif
 #define SPECDEC_STAMP(tag)                                                                         \
     do {                                                                                           \
-        if (trace_on_ && trace_ && trace_n_ < 62) {                                               \
+        if (SPECDEC_TRACE_KEEP(tag) && trace_on_ && trace_ && trace_n_ < 62) {                    \
             unsigned long long t_;                                                                 \
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                 \
             trace_[trace_n_++] = (t_ << 4) | (unsigned long long)(tag);                            \
@@ -81,6 +97,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kTargetSliceBytes = 32 * 1024;
 constexpr int kMaxSliceBytes = 192 * 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // copies in flight after an expired wait
 
 enum : int { kDrawP = 0, kDrawResidualQ = 1, kDrawResidualOneHot = 2 };
 
@@ -111,6 +128,7 @@ struct Args {
     // request schedule: cluster i verifies request order[i] (a permutation of [0, B), heaviest
     // expected work first), or request i when NULL
     const int32_t* order;
+    unsigned long long wait_ns;   // streaming kernel: limit of each wait on an mbarrier
 };
 
 // Partial result of one row pass, combined thread -> warp -> CTA -> cluster.
@@ -212,6 +230,14 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// try_wait: the thread may be suspended inside it for a system-dependent time
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
@@ -222,21 +248,34 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok;
 }
 
-__device__ __forceinline__ unsigned long long global_ns()
+// non-blocking test of a phase
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity)
 {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok;
 }
 
-// Bounded wait for phase `parity` of an mbarrier. Returns false when the time limit expired.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+// Limits below this poll with test_wait (no suspension inside a try, so a limit of 0 expires at
+// the first probe that finds the phase pending); longer ones use try_wait.
+constexpr unsigned long long kPollBelowNs = 1000000ull;
+
+// Bounded wait for phase `parity` of an mbarrier. Returns false when `limit_ns` expired, or as
+// soon as *abort is set (another thread of the CTA gave up on a wait).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs,
+                                                  const volatile int* abort = nullptr)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool poll = limit_ns < kPollBelowNs;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (abort && *abort) return false;
+        if (global_ns() - t0 >= limit_ns) return false;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     }
 }
 
@@ -799,6 +838,7 @@ struct StreamShared {
     uint64_t pbar[2];                      // cluster exchange: partials of the G CTAs landed
     Part wpart[2][kConsumerWarps];
     Part parts[2][kMaxCluster];            // cluster exchange: one partial per CTA of the request
+    Part xres[2];                          // cluster exchange: the folded result, for every consumer
     int32_t scan[kConsumerWarps];
     int32_t xs[SPECDEC_KMAX];
     float us[SPECDEC_KMAX];
@@ -806,6 +846,7 @@ struct StreamShared {
     int32_t g, greedy, qmode, sparse, timed_out, dec_code;
     uint32_t st;
     float c;
+    uint32_t issued;                       // chunks the producer issued (set when it is done)
     // top-k / top-p threshold search: the 256 bins of one pass. Masses are sums of 24-bit
     // integers kept as the sums of their low and high 12 bits (exact in 32 bits for V <= 2^20).
     uint32_t fcnt[256];
@@ -859,13 +900,26 @@ __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t
     return ok;
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ uint32_t mbar_test_wait_cluster(uint32_t bar, uint32_t parity)
 {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, unsigned long long limit_ns,
+                                                          const volatile int* abort)
+{
+    const bool poll = limit_ns < kPollBelowNs;
+    if (poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (*abort) return false;
+        if (global_ns() - t0 >= limit_ns) return false;
+        if (poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity)) return true;
     }
 }
 
@@ -1318,15 +1372,96 @@ __device__ __forceinline__ void combine_any(Part& a, const Part& b, float c)
     else combine(a, b, c);
 }
 
-template <bool kRace>
-__device__ __forceinline__ Part warp_reduce_any(Part p, float c)
+// ---- the end-of-row reduction of the streaming kernel, shallow: a warp takes its maxima (and
+// the lowest index of its best score) with redux.sync on order-preserving images, rescales each
+// lane's sum once to the warp's maximum and adds the sums by shuffles; then every consumer thread
+// folds the warps' partials in warp order, each rescaled once to the CTA's maximum.
+
+// Order-preserving 32-bit image of a float that is not NaN (a < b iff ordered(a) < ordered(b));
+// the map is its own inverse.
+__device__ __forceinline__ int ordered(float f)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        Part o = shfl_part(p, off);
-        combine_any<kRace>(p, o, c);
+    const int i = __float_as_int(f);
+    return i ^ ((i >> 31) & 0x7fffffff);
+}
+
+__device__ __forceinline__ float unordered(int i)
+{
+    return __int_as_float(i ^ ((i >> 31) & 0x7fffffff));
+}
+
+// A race partial's best score rescaled by the power of two f; a score that underflows drops out.
+__device__ __forceinline__ void race_scale_best(float& best, int& idx, float f)
+{
+    best = best > 0.f ? best * f : -INFINITY;
+    if (!(best > 0.f)) { best = -INFINITY; idx = INT_MAX; }
+}
+
+// Every lane of the warp gets the fold of the lanes' partials (bitwise the same in every lane:
+// the butterfly adds commute).
+template <bool kRace>
+__device__ __forceinline__ Part warp_fold(const Part& p, float c)
+{
+    constexpr unsigned kAll = 0xffffffffu;
+    Part r;
+    r.m = unordered(__reduce_max_sync(kAll, ordered(p.m)));
+    r.zx = unordered(__reduce_max_sync(kAll, ordered(p.zx)));
+    float S, best = p.best;
+    int idx = p.idx;
+    if constexpr (kRace) {
+        const bool has = p.m > -INFINITY;
+        const float mc = __int_as_float(p.flag);
+        const float M = unordered(__reduce_max_sync(kAll, ordered(has ? mc : -INFINITY)));
+        const float f = has ? pow2_int(mc - M) : 0.f;
+        S = p.S * f;
+        race_scale_best(best, idx, f);
+        r.flag = __float_as_int(M);
+    } else {
+        S = p.m > -INFINITY ? p.S * ex2((p.m - r.m) * c) : 0.f;
+        r.flag = (int)__reduce_or_sync(kAll, (unsigned)p.flag);
     }
-    return p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(kAll, S, off);
+    r.S = S;
+    const int bi = __reduce_max_sync(kAll, ordered(best));
+    r.best = unordered(bi);
+    r.idx = __reduce_min_sync(kAll, ordered(best) == bi ? idx : INT_MAX);
+    return r;
+}
+
+// Fold of N partials in order (the same result in every thread that calls it).
+template <bool kRace, int N>
+__device__ __forceinline__ Part fold_partials(const Part* wp, float c)
+{
+    Part r;
+    float m = -INFINITY, zx = -INFINITY, M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < N; ++w) {
+        m = fmaxf(m, wp[w].m);
+        zx = fmaxf(zx, wp[w].zx);
+        if constexpr (kRace)
+            if (wp[w].m > -INFINITY) M = fmaxf(M, __int_as_float(wp[w].flag));
+    }
+    float S = 0.f, best = -INFINITY;
+    int idx = INT_MAX, flag = 0;
+#pragma unroll
+    for (int w = 0; w < N; ++w) {
+        const bool has = wp[w].m > -INFINITY;
+        float b = wp[w].best;
+        int i = wp[w].idx;
+        if constexpr (kRace) {
+            const float f = has ? pow2_int(__int_as_float(wp[w].flag) - M) : 0.f;
+            S += wp[w].S * f;
+            race_scale_best(b, i, f);
+        } else {
+            S += has ? wp[w].S * ex2((wp[w].m - m) * c) : 0.f;
+            flag |= wp[w].flag;
+        }
+        if (b > best || (b == best && i < idx)) { best = b; idx = i; }
+    }
+    r.m = m; r.S = S; r.zx = zx; r.best = best; r.idx = idx;
+    r.flag = kRace ? __float_as_int(M) : flag;
+    return r;
 }
 
 template <typename ET>
@@ -1340,12 +1475,18 @@ struct Producer {
     __device__ Producer(const Args& a_, StreamShared& s_, unsigned char* r_, int lane_, int lo_, int hi_)
         : a(a_), sh(s_), ring(r_), lane(lane_), lo(lo_), hi(hi_) {}
 
+    // The next stage, once its consumers released it; -1 (for the whole warp) when a wait of the
+    // CTA has expired: from then on nothing more is issued, so no copy can land in a stage whose
+    // previous copy is still in flight.
     __device__ __forceinline__ int acquire()
     {
         const int s = (int)(it % kStages);
         const uint32_t par = ((it / kStages) & 1u) ^ 1u;
-        if (!mbar_wait_bounded(smem_addr(&sh.empty[s]), par)) sh.timed_out = 1;
-        return s;
+        volatile int* flag = &sh.timed_out;
+        bool ok = !*flag && mbar_wait_bounded(smem_addr(&sh.empty[s]), par, a.wait_ns, flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) *flag = 1;
+        return ok ? s : -1;
     }
 
     // chunk c of the slice of logits row t (+ its mask words)
@@ -1353,6 +1494,7 @@ struct Producer {
     {
         using G = Geom<ET>;
         const int s = acquire();
+        if (s < 0) return;
         unsigned char* st = ring + (size_t)s * kStageBytes;
         const int i0 = lo + c * G::kRowIds;
         const int n = min(G::kRowIds, hi - i0);
@@ -1389,6 +1531,7 @@ struct Producer {
     {
         using G = Geom<ET>;
         const int s = acquire();
+        if (s < 0) return;
         unsigned char* st = ring + (size_t)s * kStageBytes;
         const int ids = G::draw_ids(with_q);
         const int i0 = lo + c * ids;
@@ -1466,6 +1609,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         mbar_init(smem_addr(&sh.pbar[1]), (uint32_t)NC);
         fence_mbar_init();
         sh.timed_out = 0;
+        sh.issued = 0;
     }
     // every CTA of the request has initialised its barriers before any partial is sent
     if (NC > 1) cluster_sync_all(); else __syncthreads();
@@ -1511,15 +1655,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     for (int c = 0; c < spec_r; ++c) issue(j + 1, c);
                     issued_next = spec_r;
                 }
-                if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
-                ++dec_round;
-                int code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                // the consumers' next decision (kDecDone once any wait of the CTA has expired)
+                auto next_code = [&]() -> int {
+                    volatile int* flag = &sh.timed_out;
+                    bool ok = !*flag && mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u, a.wait_ns, flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    ++dec_round;
+                    if (!ok) { *flag = 1; return kDecDone; }
+                    return *reinterpret_cast<volatile int*>(&sh.dec_code);
+                };
+                int code = next_code();
                 if constexpr (kFilt) {
                     while (code == kDecRescan) {             // one more pass of a threshold search
                         for (int c = 0; c < nrow_chunks; ++c) pr.row_chunk(t, c);
-                        if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
-                        ++dec_round;
-                        code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                        code = next_code();
                     }
                 }
                 if (code == kDecNextRow) continue;
@@ -1527,12 +1676,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     const bool wq = (code == kDecDrawQ);
                     const int nd = (hi - lo + G::draw_ids(wq) - 1) / G::draw_ids(wq);
                     for (int c = 0; c < nd; ++c) pr.draw_chunk(t, (int64_t)rs.d0 + j, c, wq);
-                    if (!mbar_wait_bounded(smem_addr(&sh.dec), dec_round & 1u)) sh.timed_out = 1;
-                    ++dec_round;
-                    code = *reinterpret_cast<volatile int*>(&sh.dec_code);
+                    code = next_code();
                 }
                 break;
             }
+            if (lane == 0) sh.issued = pr.it;       // chunks issued, for the drain after an expired wait
         }
     } else {
         // ------------------------------------------------------------------ consumers
@@ -1600,9 +1748,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 
         uint32_t it = 0, xround = 0;
         int par = 0;
+        // (an expired wait marks the CTA before the stage is released: the producer, which acquires
+        // that release, then issues nothing more; the stage's contents are then not used for any
+        // output that counts, the request being reported as timed out)
         auto wait_full = [&]() -> int {
             const int s = (int)(it % kStages);
-            if (!mbar_wait_bounded(smem_addr(&sh.full[s]), (it / kStages) & 1u)) sh.timed_out = 1;
+            volatile int* flag = &sh.timed_out;
+            if (!mbar_wait_bounded(smem_addr(&sh.full[s]), (it / kStages) & 1u, a.wait_ns, flag)) *flag = 1;
             return s;
         };
         auto release = [&](int s) {
@@ -1618,12 +1770,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         // std::integral_constant<bool, ...>)
         auto reduce_cta = [&](Part p, auto race) -> Part {
             constexpr bool kR = decltype(race)::value;
-            p = warp_reduce_any<kR>(p, c);
-            if (lane == 0) sh.wpart[par][cw] = p;
+            const Part w = warp_fold<kR>(p, c);
+            if (lane == 0) sh.wpart[par][cw] = w;
             consumer_sync();
-            Part r = part_identity();
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) combine_any<kR>(r, sh.wpart[par][w], c);
+            const Part r = fold_partials<kR, kConsumerWarps>(sh.wpart[par], c);
             par ^= 1;
             return r;
         };
@@ -1642,11 +1792,20 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 st_cluster_u32(base + 20, (uint32_t)r.flag);
                 mbar_arrive_remote(map_to_rank(smem_addr(&sh.pbar[slot]), (uint32_t)ct));
             }
-            if (!mbar_wait_cluster_bounded(smem_addr(&sh.pbar[slot]), (xround >> 1) & 1u)) sh.timed_out = 1;
+            if (!mbar_wait_cluster_bounded(smem_addr(&sh.pbar[slot]), (xround >> 1) & 1u, a.wait_ns, &sh.timed_out))
+                *reinterpret_cast<volatile int*>(&sh.timed_out) = 1;
             ++xround;
-            Part q = part_identity();
-            for (int i = 0; i < NC; ++i) combine_any<kR>(q, sh.parts[slot][i], c);
-            return q;
+            // one thread folds the partials in rank order and every consumer reads its result after a
+            // barrier: all of them take the same decision even when a wait expired while partials
+            // were still landing (threads reading them one by one could then disagree, and a
+            // disagreement would split them across the consumers' named barriers)
+            if (ct == 0) {
+                Part q = part_identity();
+                for (int i = 0; i < NC; ++i) combine_any<kR>(q, sh.parts[slot][i], c);
+                sh.xres[slot] = q;
+            }
+            consumer_sync();
+            return sh.xres[slot];
         };
         auto reduce = [&](Part p) -> Part { return reduce_any(p, std::false_type{}); };
         auto post = [&](int code) {
@@ -1665,12 +1824,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             const int my0 = w0 + ct * kPer;
             uint32_t words[kPer];
             SPECDEC_STAMP(10);
+            // (loaded twice: for the count, and again after the scan for the list, from L1, so
+            // that the words are not held in registers across the scan's barriers)
+            auto load_words = [&] {
 #pragma unroll
-            for (int q4 = 0; q4 < kPer / 4; ++q4) {
-                const int w = my0 + 4 * q4;               // W and the slice bounds are multiples of 4 words
-                const uint4 u = (w < w1) ? __ldg(mrow + (w >> 2)) : make_uint4(0u, 0u, 0u, 0u);
-                words[4 * q4] = u.x; words[4 * q4 + 1] = u.y; words[4 * q4 + 2] = u.z; words[4 * q4 + 3] = u.w;
-            }
+                for (int q4 = 0; q4 < kPer / 4; ++q4) {
+                    const int w = my0 + 4 * q4;           // W and the slice bounds are multiples of 4 words
+                    const uint4 u = (w < w1) ? __ldg(mrow + (w >> 2)) : make_uint4(0u, 0u, 0u, 0u);
+                    words[4 * q4] = u.x; words[4 * q4 + 1] = u.y; words[4 * q4 + 2] = u.z; words[4 * q4 + 3] = u.w;
+                }
+            };
+            load_words();
             // one bit per 16-byte group (its lowest id's position) when any id of the group is allowed;
             // bits at or above V in the row's last word are dropped first
             const int vtail = a.V & 31;
@@ -1709,6 +1873,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             }
             // fixed trip count (no loop over set bits): allowed ids come in runs, and a loop over
             // set bits would serialise each warp on its densest word
+            load_words();
 #pragma unroll
             for (int q = 0; q < kPer; ++q) {
                 const uint32_t pres = presence(words[q], my0 + q);
@@ -2711,6 +2876,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         }
     }
     __syncthreads();
+    // after an expired wait, bulk copies may still be in flight: wait (bounded, a separate limit)
+    // for the last copy issued into each stage before the CTA leaves, so that none lands in shared
+    // memory the CTA no longer owns
+    if (tid == 0 && sh.timed_out && a.bulk) {
+        const uint32_t issued = sh.issued;
+        for (uint32_t s = 0; s < (uint32_t)kStages && s < issued; ++s) {
+            const uint32_t last = s + ((issued - 1u - s) / kStages) * kStages;
+            (void)mbar_wait_bounded(smem_addr(&sh.full[s]), (last / kStages) & 1u, kDrainLimitNs);
+        }
+    }
     // a copy that missed its deadline marks the request (any CTA of it) after rank 0 wrote status
     if (NC > 1) cluster_sync_all();
     if (tid == 0 && sh.timed_out && a.status) atomicOr(&a.status[b], SPECDEC_ST_DEVICE_TIMEOUT);
@@ -2889,14 +3064,40 @@ int stream_ctas_per_request(int32_t B, int sms)
     return G;
 }
 
+// Launch choices forced for comparison and test runs (-1: the library decides). Initialised once
+// per process from SPECDEC_KERNEL (=cluster: the slice-resident cluster kernel, kept as an
+// independent decomposition of the same computation that parity runs cross-check the streaming
+// kernel against), SPECDEC_CTAS_PER_REQUEST and SPECDEC_SCHEDULE; specdec_set_launch_options
+// changes them afterwards. No call reads the environment.
+struct LaunchOptions {
+    std::atomic<int> kernel{-1};       // 0 streaming, 1 slice-resident cluster kernel
+    std::atomic<int> ctas{-1};         // CTAs per request, 1..kMaxCluster
+    std::atomic<int> schedule{-1};     // 0 off, 1 on (with a workspace)
+    std::atomic<long long> wait_us{-1};  // limit of each wait in the streaming kernel (-1: 2 s)
+};
+
+LaunchOptions& launch_options()
+{
+    static LaunchOptions* o = [] {
+        LaunchOptions* d = new LaunchOptions;
+        if (const char* e = std::getenv("SPECDEC_KERNEL")) d->kernel = std::strcmp(e, "cluster") == 0 ? 1 : 0;
+        if (const char* e = std::getenv("SPECDEC_CTAS_PER_REQUEST")) {
+            const long long v = std::atoll(e);
+            if (v >= 1) d->ctas = (int)(v > kMaxCluster ? kMaxCluster : v);
+        }
+        if (const char* e = std::getenv("SPECDEC_SCHEDULE")) d->schedule = std::strcmp(e, "0") != 0 ? 1 : 0;
+        return d;
+    }();
+    return *o;
+}
+
 specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, int32_t B, LaunchShape* out)
 {
     if (V <= 0 || B < 0) return SPECDEC_ERR_INVALID_ARG;
     if (dt != SPECDEC_F32 && dt != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
     const int es = dt == SPECDEC_F32 ? 4 : 2;
     const long long units = ((long long)V + kUnit - 1) / kUnit;
-    const char* kind = std::getenv("SPECDEC_KERNEL");                // comparison runs
-    const bool cluster = kind && std::strcmp(kind, "cluster") == 0;
+    const bool cluster = launch_options().kernel.load() == 1;
     long long G;
     if (cluster) {
         const long long row_bytes = (long long)V * es;
@@ -2904,10 +3105,8 @@ specdec_status_t shape_for(int32_t V, specdec_dtype_t dt, int32_t B, LaunchShape
     } else {
         G = stream_ctas_per_request(B, device_sms());
     }
-    if (const char* env = std::getenv("SPECDEC_CTAS_PER_REQUEST")) {     // tuning sweeps
-        const long long forced = std::atoll(env);
-        if (forced >= 1) G = forced;
-    }
+    const int forced = launch_options().ctas.load();
+    if (forced >= 1) G = forced;
     if (G < 1) G = 1;
     if (G > kMaxCluster) G = kMaxCluster;
     if (G > units) G = units;
@@ -3035,11 +3234,12 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 inline size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
 
 // Whether a call with a workspace runs the schedule kernel first: only when the grid does not fit
-// in one wave of resident CTAs (with everything resident at once the order changes nothing).
-// SPECDEC_SCHEDULE=1 / 0 forces it on / off (tests and comparison runs).
+// in one wave of resident CTAs (with everything resident at once the order changes nothing),
+// unless the launch options force it on or off.
 bool schedule_wanted(int32_t B, int G)
 {
-    if (const char* env = std::getenv("SPECDEC_SCHEDULE")) return std::strcmp(env, "0") != 0;
+    const int forced = launch_options().schedule.load();
+    if (forced >= 0) return forced == 1;
     return (long long)B * G > (long long)kResidentPerSM * device_sms();
 }
 
@@ -3221,6 +3421,8 @@ extern "C" specdec_status_t specdec_verify(
              (!draft_probs || aligned(draft_probs, 16));
     a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
     a.order = nullptr;
+    const long long wait_us = launch_options().wait_us.load();
+    a.wait_ns = wait_us < 0 ? kWaitLimitNs : (unsigned long long)wait_us * 1000ull;
     const cudaStream_t st = (cudaStream_t)stream;
     if (workspace != nullptr) {
         const ScheduleLayout L = schedule_layout(B);
@@ -3266,6 +3468,21 @@ extern "C" specdec_status_t specdec_verify_noalloc(
                           bitmask, temperature, top_k, top_p, uniforms, exp_noise, out_tokens, out_num_accepted,
                           counters, status, diag_accept_prob, diag_row_stats, telemetry, scratch,
                           scratch ? kNoallocScratchBytes : 0, stream);
+}
+
+extern "C" specdec_status_t specdec_set_launch_options(int32_t kernel, int32_t ctas_per_request, int32_t schedule,
+                                                       int32_t wait_limit_us)
+{
+    if (kernel < -1 || kernel > 1 || schedule < -1 || schedule > 1 || ctas_per_request == 0 ||
+        ctas_per_request < -1 || ctas_per_request > kMaxCluster || wait_limit_us < -1 ||
+        wait_limit_us > 2000000)
+        return SPECDEC_ERR_INVALID_ARG;
+    LaunchOptions& o = launch_options();
+    o.kernel = kernel;
+    o.ctas = ctas_per_request;
+    o.schedule = schedule;
+    o.wait_us = wait_limit_us;
+    return SPECDEC_OK;
 }
 
 extern "C" size_t specdec_workspace_size(int32_t B, int32_t V)

@@ -51,6 +51,7 @@ class Outputs:
     diag_row_stats: Optional[object] = None
     workspace: Optional[object] = None
     telemetry: Optional[object] = None
+    guarded: Optional[list] = None          # (whole allocation, elements in use) per guarded output
 
     def numpy(self) -> Dict[str, np.ndarray]:
         d = {"out_tokens": self.out_tokens, "out_num_accepted": self.out_num_accepted,
@@ -69,26 +70,55 @@ class Outputs:
                 res[k] = t.numpy().view(np.uint32).copy()
             else:
                 res[k] = t.numpy().copy()
+        if self.guarded is not None:
+            res["guards_intact"] = self.guards_intact()
         return res
+
+    def guards_intact(self) -> bool:
+        """Whether the guard elements after every output still hold their fill pattern."""
+        for base, n in self.guarded or []:
+            tail = base.view(-1)[n:].cpu().numpy().view(np.uint8)
+            if tail.size and not (tail == GUARD_BYTE).all():
+                return False
+        return True
+
+
+GUARD_BYTE = 0xA5
 
 
 def alloc_outputs(w: Workload, device="cuda", diag: bool = False, workspace: bool = True,
-                  telemetry: Optional[bool] = None) -> Outputs:
+                  telemetry: Optional[bool] = None, guard: int = 0) -> Outputs:
     """Output tensors (and, with workspace=True, the verify's scratch: the request schedule).
-    The per-position telemetry is allocated when asked for (default: with the diagnostics)."""
+    The per-position telemetry is allocated when asked for (default: with the diagnostics).
+    guard > 0: every output is the front of a larger allocation whose last `guard` elements hold
+    the byte 0xA5, so that Outputs.guards_intact() detects a write past an output's end."""
     import torch
+
+    guarded = [] if guard > 0 else None
+
+    def out(shape, fill, dtype):
+        n = int(np.prod(shape))
+        if not guard:
+            return torch.full(shape, fill, dtype=dtype, device=device)
+        base = torch.empty(n + guard, dtype=dtype, device=device)
+        base.view(torch.uint8).fill_(GUARD_BYTE)
+        t = base[:n].view(shape)
+        t.fill_(fill)
+        guarded.append((base, n))
+        return t
 
     ws_bytes = _native.workspace_size(w.B, w.V) if workspace else 0
     return Outputs(
-        out_tokens=torch.full((w.T,), -7, dtype=torch.int32, device=device),
-        out_num_accepted=torch.full((w.B,), -7, dtype=torch.int32, device=device),
-        counters=torch.zeros(4, dtype=torch.int64, device=device),
-        status=torch.zeros(w.B, dtype=torch.int32, device=device),
-        diag_accept_prob=torch.full((max(w.N, 1),), float("nan"), dtype=torch.float32, device=device) if diag else None,
-        diag_row_stats=torch.full((max(w.T, 1), 2), float("nan"), dtype=torch.float32, device=device) if diag else None,
+        out_tokens=out((w.T,), -7, torch.int32),
+        out_num_accepted=out((w.B,), -7, torch.int32),
+        counters=out((4,), 0, torch.int64),
+        status=out((w.B,), 0, torch.int32),
+        diag_accept_prob=out((max(w.N, 1),), float("nan"), torch.float32) if diag else None,
+        diag_row_stats=out((max(w.T, 1), 2), float("nan"), torch.float32) if diag else None,
         workspace=torch.empty(ws_bytes, dtype=torch.uint8, device=device) if ws_bytes else None,
-        telemetry=(torch.zeros(_native.TELEMETRY_SHAPE, dtype=torch.int64, device=device)
+        telemetry=(out(_native.TELEMETRY_SHAPE, 0, torch.int64)
                    if (diag if telemetry is None else telemetry) else None),
+        guarded=guarded,
     )
 
 
@@ -102,12 +132,13 @@ def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> No
         telemetry=out.telemetry, top_k=dev.get("top_k"), top_p=dev.get("top_p"))
 
 
-def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True) -> Dict[str, np.ndarray]:
-    """Copy, verify, synchronise, and return the outputs as numpy arrays."""
+def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True, guard: int = 0) -> Dict[str, np.ndarray]:
+    """Copy, verify, synchronise, and return the outputs as numpy arrays (with guard > 0 also
+    "guards_intact": whether every output's trailing guard elements are untouched)."""
     import torch
 
     dev = device_tensors(w, device)
-    out = alloc_outputs(w, device, diag=diag, workspace=workspace)
+    out = alloc_outputs(w, device, diag=diag, workspace=workspace, guard=guard)
     verify(w, dev, out)
     torch.cuda.synchronize()
     return out.numpy()

@@ -23,3 +23,21 @@ def pytest_collection_modifyitems(config, items):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture
+def launch_options():
+    """Force the library's launch choices for one test (specdec_set_launch_options): call it with
+    kernel=, ctas_per_request=, schedule= and/or wait_limit_us= (None: the library decides). Every
+    choice is put back to automatic afterwards."""
+    from speculative_decoding_verification_specdec_gb300 import _native
+
+    state = {"kernel": None, "ctas_per_request": None, "schedule": None, "wait_limit_us": None}
+
+    def set_(**kw):
+        state.update(kw)
+        _native.set_launch_options(**state)
+
+    set_()
+    yield set_
+    _native.set_launch_options()

@@ -44,8 +44,8 @@ def test_status_strings(lib):
                                      (151936, 1), (262144, 1), (786432, 0)])
 @pytest.mark.parametrize("kernel", ["stream", "cluster"])
 @pytest.mark.parametrize("B", [1, 64, 128, 1024])
-def test_launch_config_covers_the_row(lib, V, dtype, kernel, B, monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", kernel)
+def test_launch_config_covers_the_row(lib, V, dtype, kernel, B, launch_options):
+    launch_options(kernel=kernel)
     c = _native.launch_config(V, dtype, B=B)
     G, sl = c["ctas_per_request"], c["slice_ids"]
     assert 1 <= G <= 16 and sl % 128 == 0
@@ -61,22 +61,35 @@ def test_launch_config_covers_the_row(lib, V, dtype, kernel, B, monkeypatch):
             assert G == 1                            # enough requests to fill the GPU
 
 
-def test_launch_config_reports_the_schedule(lib, monkeypatch):
+def test_launch_config_reports_the_schedule(lib, launch_options):
     """Two kernels per call with a workspace once the grid exceeds one wave of resident CTAs
     (two per SM; 152 SMs when no device is visible), one otherwise; the override forces either."""
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
-    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)
+    launch_options(kernel="stream")
+    launch_options(schedule=None)
     assert _native.launch_config(151936, 1, B=1024)["kernels_with_workspace"] == 2
     assert _native.launch_config(151936, 0, B=128)["kernels_with_workspace"] == 1
     assert _native.launch_config(32000, 0, B=64)["kernels_with_workspace"] == 1
-    monkeypatch.setenv("SPECDEC_SCHEDULE", "1")
+    launch_options(schedule=True)
     assert _native.launch_config(32000, 0, B=64)["kernels_with_workspace"] == 2
-    monkeypatch.setenv("SPECDEC_SCHEDULE", "0")
+    launch_options(schedule=False)
     assert _native.launch_config(151936, 1, B=1024)["kernels_with_workspace"] == 1
 
 
-def test_launch_config_rejects(lib, monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
+def test_launch_options_validation(lib):
+    """specdec_set_launch_options refuses values outside its ranges and changes nothing then."""
+    E = _native
+    for bad in ((2, -1, -1, -1), (-2, -1, -1, -1), (-1, 0, -1, -1), (-1, 17, -1, -1), (-1, -2, -1, -1),
+                (-1, -1, 2, -1), (-1, -1, -2, -1), (-1, -1, -1, -2), (-1, -1, -1, 2000001)):
+        assert lib.specdec_set_launch_options(*bad) == E.SPECDEC_ERR_INVALID_ARG, bad
+    assert lib.specdec_set_launch_options(-1, 16, 1, 0) == E.SPECDEC_OK
+    assert _native.launch_config(1000, 0, B=4096)["kernels_with_workspace"] == 2
+    assert lib.specdec_set_launch_options(-1, -1, 7, -1) == E.SPECDEC_ERR_INVALID_ARG
+    assert _native.launch_config(1000, 0, B=4096)["kernels_with_workspace"] == 2     # unchanged
+    assert lib.specdec_set_launch_options(-1, -1, -1, -1) == E.SPECDEC_OK
+
+
+def test_launch_config_rejects(lib, launch_options):
+    launch_options(kernel="cluster")
     with pytest.raises(_native.SpecdecError) as e:
         _native.launch_config(0, 0)
     assert e.value.status == _native.SPECDEC_ERR_INVALID_ARG
@@ -86,7 +99,7 @@ def test_launch_config_rejects(lib, monkeypatch):
     with pytest.raises(_native.SpecdecError) as e:
         _native.launch_config(4 * 1024 * 1024, 0)     # a 16 MiB row cannot be staged on chip
     assert e.value.status == _native.SPECDEC_ERR_UNSUPPORTED
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")   # the streaming kernel has no row-size limit
+    launch_options(kernel="stream")   # the streaming kernel has no row-size limit
     assert _native.launch_config(4 * 1024 * 1024, 0, B=1024)["ctas_per_request"] == 1
 
 
@@ -102,8 +115,8 @@ def _call(lib, **over):
                               a["ctr"], a["status"], a["da"], a["dr"], a["tm"], a["ws"], a["ws_bytes"], None)
 
 
-def test_host_validation(lib, monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
+def test_host_validation(lib, launch_options):
+    launch_options(kernel="cluster")
     E = _native
     assert _call(lib, B=0) == E.SPECDEC_OK                        # empty batch: nothing launched
     assert _call(lib, B=-1) == E.SPECDEC_ERR_INVALID_ARG
@@ -124,9 +137,9 @@ def test_host_validation(lib, monkeypatch):
     assert _call(lib, V=4 * 1024 * 1024) == E.SPECDEC_ERR_UNSUPPORTED
 
 
-def test_filter_vocabulary_limit(lib, monkeypatch):
+def test_filter_vocabulary_limit(lib, launch_options):
     # top-k / top-p sum 12-bit mass parts in 32-bit bins: exact up to 2^20 elements per row
-    monkeypatch.delenv("SPECDEC_KERNEL", raising=False)
+    launch_options(kernel=None)
     E = _native
     assert _call(lib, tp=4096, V=(1 << 20) + 1) == E.SPECDEC_ERR_UNSUPPORTED
     assert _call(lib, tk=4096, V=(1 << 20) + 1) == E.SPECDEC_ERR_UNSUPPORTED
@@ -134,13 +147,13 @@ def test_filter_vocabulary_limit(lib, monkeypatch):
     assert _call(lib, V=(1 << 20) + 1, B=0) == E.SPECDEC_OK          # no filter: no limit
 
 
-def test_workspace_size_and_validation(lib, monkeypatch):
+def test_workspace_size_and_validation(lib, launch_options):
     E = _native
     assert _native.workspace_size(0, 1000) == 0 and _native.workspace_size(4, 0) == 0
     small, big = _native.workspace_size(4, 1000), _native.workspace_size(1024, 151936)
     assert small > 0 and big > small and small % 16 == 0 and big % 16 == 0
     assert big <= 5 * 1024 + 32                       # an int32 order and a key byte per request
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    launch_options(kernel="stream")
     # a workspace that is too small or misaligned is refused before anything runs
     assert _call(lib, ws=4096, ws_bytes=small - 16) == E.SPECDEC_ERR_INVALID_ARG
     assert _call(lib, ws=4104, ws_bytes=small) == E.SPECDEC_ERR_INVALID_ARG

@@ -31,9 +31,11 @@ _MODE = {"workspace": True}
 
 
 def check_parity(w, cuda, label=""):
-    got = device.run(w, device=cuda, diag=True, workspace=_MODE["workspace"])
+    # every output is followed by guard elements; a write past any output's end fails the check
+    got = device.run(w, device=cuda, diag=True, workspace=_MODE["workspace"], guard=64)
     ref = oracle.verify(w)
     rep = parity.compare(w, got, ref)
+    assert got["guards_intact"], f"{label or w.name}: a write landed past the end of an output"
     assert not (got["status"] & _native.ST_DEVICE_TIMEOUT).any()
     assert rep.ok, (f"{label or w.name}: {rep.summary()} tokens={rep.token_mismatches[:8]} "
                     f"acc={rep.accepted_mismatches[:8]} status={rep.status_mismatches[:8]} "
@@ -45,12 +47,12 @@ KERNELS = ["stream", "stream_index_order", "cluster"]
 
 
 @pytest.fixture(params=KERNELS)
-def kernel(request, monkeypatch):
+def kernel(request, launch_options):
     """stream: the streaming kernel with a workspace (requests scheduled heaviest first);
     stream_index_order: the same kernel without one (requests in index order); cluster: the
     slice-resident cluster kernel (scheduled)."""
-    monkeypatch.setenv("SPECDEC_KERNEL", "cluster" if request.param == "cluster" else "stream")
-    monkeypatch.setenv("SPECDEC_SCHEDULE", "0" if request.param == "stream_index_order" else "1")
+    launch_options(kernel="cluster" if request.param == "cluster" else "stream")
+    launch_options(schedule=request.param != "stream_index_order")
     _MODE["workspace"] = request.param != "stream_index_order"
     yield request.param
     _MODE["workspace"] = True
@@ -100,9 +102,9 @@ def test_sweep_parity(cuda, case, kernel):
 
 
 @pytest.mark.parametrize("ctas", ["1", "3", "16"])
-def test_forced_cluster_shapes(cuda, ctas, monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", "cluster")
-    monkeypatch.setenv("SPECDEC_CTAS_PER_REQUEST", ctas)
+def test_forced_cluster_shapes(cuda, ctas, launch_options):
+    launch_options(kernel="cluster")
+    launch_options(ctas_per_request=int(ctas))
     w = W.make_batch(200, name=f"ctas{ctas}", B=20, V=9000, k=(0, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
                      mask_density=0.1, mask_run_len=16, forced_invalid_frac=0.2)
@@ -218,6 +220,9 @@ def test_sparse_draft_in_first_group(cuda, kernel, dtype):
 
 
 def test_rows_after_stop_are_never_read(cuda, kernel):
+    """No output depends on a row after a request's stop row: those rows are poisoned with NaN.
+    (The streaming kernel may fetch the first two ring chunks of the row after the stop before the
+    decision, and discards them; the library's diagnostics report exactly rows 0..a_b as read.)"""
     w = W.make_batch(300, B=40, V=3000, k=(2, 6), logits_dtype=W.F32, logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5, mask="half",
                      mask_density=0.2, mask_run_len=16, forced_invalid_frac=0.2)
@@ -332,11 +337,11 @@ def _schedule(w, cuda):
 
 
 @pytest.mark.parametrize("B", [1, 37, 1024, 2500])
-def test_schedule_is_a_stable_descending_permutation(cuda, B, monkeypatch):
+def test_schedule_is_a_stable_descending_permutation(cuda, B, launch_options):
     """The request order the schedule kernel writes: every request exactly once, cost keys
     non-increasing along it, equal keys in index order (one and several 1024-request tiles)."""
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
-    monkeypatch.setenv("SPECDEC_SCHEDULE", "1")        # small batches fit one wave: force it
+    launch_options(kernel="stream")
+    launch_options(schedule=True)        # small batches fit one wave: force it
     w = W.make_batch(23, name=f"sched_B{B}", B=B, V=1024, k=(0, 6), logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
                      mask="half", mask_density=0.05, mask_run_len=16, forced_invalid_frac=0.2)
@@ -350,11 +355,48 @@ def test_schedule_is_a_stable_descending_permutation(cuda, B, monkeypatch):
         assert len(set(keys.tolist())) > 1          # the batch mixes request kinds
 
 
-def test_scheduled_parity_across_tiles(cuda, monkeypatch):
+def test_scheduled_parity_across_tiles(cuda, launch_options):
     """More requests than one schedule tile, mixed kinds: identical to the oracle."""
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
-    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)   # 2100 CTAs: scheduled by default
+    launch_options(kernel="stream")
+    launch_options(schedule=None)   # 2100 CTAs: scheduled by default
     w = W.make_batch(29, name="sched_parity_B2100", B=2100, V=640, k=(0, 5), logit_sigma=3.0,
                      temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
                      mask="half", mask_density=0.1, mask_run_len=8, forced_invalid_frac=0.2)
+    check_parity(w, cuda)
+
+
+def test_wait_times_out_on_a_busy_stream(cuda):
+    """specdec_wait gives up after its host-side limit while the stream is still busy (a device
+    spin of about 0.2 s, which ends by itself), then waits it out without a limit."""
+    import ctypes
+    import time
+
+    import torch
+
+    lib = _native.load()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(400_000_000)             # clock cycles
+    t0 = time.perf_counter()
+    rc = lib.specdec_wait(ctypes.c_void_p(s.cuda_stream), 10)
+    dt = time.perf_counter() - t0
+    assert rc == _native.SPECDEC_ERR_TIMEOUT
+    assert dt < 0.15, dt
+    assert lib.specdec_wait(ctypes.c_void_p(s.cuda_stream), -1) == _native.SPECDEC_OK
+
+
+@pytest.mark.parametrize("ctas", [1, 4])
+def test_device_wait_expiry_is_reported_and_the_context_stays_usable(cuda, ctas, launch_options):
+    """With every wait of the streaming kernel limited to 0 us, waits expire: each request reports
+    SPECDEC_ST_DEVICE_TIMEOUT, the call completes (the CTAs stop issuing copies and drain the ones
+    in flight before they leave), nothing is written past an output, and the same batch then
+    verifies exactly with the default limit."""
+    w = W.make_batch(501, name=f"expiry_G{ctas}", B=12, V=70000, k=(2, 5), logits_dtype=W.BF16,
+                     logit_sigma=3.0, temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5)
+    launch_options(kernel="stream", ctas_per_request=ctas, wait_limit_us=0)
+    got = device.run(w, device=cuda, diag=False, workspace=True, guard=64)
+    assert got["guards_intact"]
+    timed = (got["status"] & _native.ST_DEVICE_TIMEOUT) != 0
+    assert timed.all(), got["status"]
+    launch_options(wait_limit_us=None)
     check_parity(w, cuda)

@@ -27,8 +27,8 @@ def cuda():
 
 
 @pytest.fixture(autouse=True)
-def stream_kernel(monkeypatch):
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+def stream_kernel(launch_options):
+    launch_options(kernel="stream")
 
 
 def _check(w, cuda, workspace=True):

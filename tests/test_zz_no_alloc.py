@@ -35,14 +35,14 @@ def _outputs(w, cuda, workspace):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, monkeypatch):
+def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, launch_options):
     """Two calls in a row through each entry point on one batch large enough to be scheduled
     (1200 requests, mixed kinds): identical tokens, accepted counts, status and diagnostics on
     every call, counters doubled, and equal to the oracle."""
     import torch
 
-    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    launch_options(schedule=None)
+    launch_options(kernel="stream")
     torch.cuda.set_device(0)
     cuda = "cuda:0"
     w = W.make_batch(41, name="noalloc_B1200", B=1200, V=2048, k=(0, 6), logit_sigma=3.0,
@@ -83,13 +83,13 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, monkeypatch):
 
 
 @pytest.mark.gpu
-def test_noalloc_with_top_k_top_p_matches_workspace_entry_point(lib, monkeypatch):
+def test_noalloc_with_top_k_top_p_matches_workspace_entry_point(lib, launch_options):
     """A filtered batch of 400 requests (scheduled: one CTA per filtered request) through both
     entry points: identical outputs, and equal to the oracle."""
     import torch
 
-    monkeypatch.delenv("SPECDEC_SCHEDULE", raising=False)
-    monkeypatch.setenv("SPECDEC_KERNEL", "stream")
+    launch_options(schedule=None)
+    launch_options(kernel="stream")
     torch.cuda.set_device(0)
     cuda = "cuda:0"
     rng = np.random.default_rng(42)
@@ -110,6 +110,41 @@ def test_noalloc_with_top_k_top_p_matches_workspace_entry_point(lib, monkeypatch
         na_out.out_tokens, na_out.out_num_accepted, na_out.counters, na_out.status,
         na_out.diag_accept_prob, na_out.diag_row_stats, telemetry=na_out.telemetry,
         top_k=dev["top_k"], top_p=dev["top_p"])
+    torch.cuda.synchronize()
+    ws, na = ws_out.numpy(), na_out.numpy()
+    for k in ("out_tokens", "out_num_accepted", "status", "counters", "telemetry"):
+        assert np.array_equal(na[k], ws[k]), k
+    for k in ("diag_accept_prob", "diag_row_stats"):
+        assert np.array_equal(na[k], ws[k], equal_nan=True), k
+    rep = parity.compare(w, na, oracle.verify(w))
+    assert rep.ok, rep.summary()
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_largest_batch(lib, launch_options):
+    """B = SPECDEC_NOALLOC_MAX_REQUESTS: the request order and the cost keys fill the array
+    exactly. The schedule is forced on; the outputs equal those of specdec_verify given a
+    workspace of specdec_workspace_size(B, V) bytes, and the oracle's."""
+    import torch
+
+    launch_options(schedule=True)
+    launch_options(kernel="stream")
+    torch.cuda.set_device(0)
+    cuda = "cuda:0"
+    B = _native.NOALLOC_MAX_REQUESTS
+    w = W.make_batch(43, name="noalloc_Bmax", B=B, V=64, k=(0, 2), logit_sigma=3.0,
+                     temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
+                     mask="half", mask_density=0.25, mask_run_len=4, forced_invalid_frac=0.2)
+    dev = device.device_tensors(w, cuda)
+    ws_out = _outputs(w, cuda, workspace=True)
+    assert ws_out.workspace.numel() == _native.workspace_size(B, w.V)
+    na_out = _outputs(w, cuda, workspace=False)
+    device.verify(w, dev, ws_out)
+    _native.specdec_verify_noalloc(
+        dev["logits"], dev["draft_ids"], dev["draft_probs"], dev["has_q"], dev["cu_num_draft"],
+        w.B, w.V, w.max_k, dev["bitmask"], dev["temperature"], dev["uniforms"], dev["exp_noise"],
+        na_out.out_tokens, na_out.out_num_accepted, na_out.counters, na_out.status,
+        na_out.diag_accept_prob, na_out.diag_row_stats, telemetry=na_out.telemetry)
     torch.cuda.synchronize()
     ws, na = ws_out.numpy(), na_out.numpy()
     for k in ("out_tokens", "out_num_accepted", "status", "counters", "telemetry"):
