@@ -731,7 +731,9 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": w.logits_dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "V": w.V, "drafts_per_step": w.N, "rows": w.T,
                        "l2": "flushed between timed steps (268 MB write)",
-                       "launch": {"grid_ctas": w.B * shape["ctas_per_request"], **shape},
+                       "launch": {"grid_ctas": (2 * (shape["split_requests"] + (w.B - shape["split_requests"] + 1) // 2)
+                                                if shape["split_requests"] else w.B * shape["ctas_per_request"]),
+                                  **shape},
                        "per_rank": "independent batch per rank (requests shard with no exchange)"},
             "roofline": {"bound": "hbm", "achieved": achieved_rows, "peak": peak, "unit": "GB/s",
                          "frac": achieved_rows / peak, "traffic": traffic, "peak_kind": peak_kind,

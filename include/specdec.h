@@ -133,7 +133,11 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  time rule: a long request that sits late in the batch no longer runs on alone
  *                  after the rest have finished). The schedule runs only when the batch needs more
  *                  than one wave of resident CTAs (two per SM); the verify kernel then starts as a
- *                  programmatic dependent of it. Without a workspace, requests start in index order.
+ *                  programmatic dependent of it. A batch that exceeds that wave additionally splits
+ *                  its heaviest requests (a sixth of a wave) over clusters of 2 CTAs (their chains
+ *                  of row passes are what set the launch's length) and runs the others two per
+ *                  cluster, one per CTA. Without a workspace, requests start in index order, one
+ *                  CTA each.
  *                  Results are identical either way; only the timing differs. The workspace
  *                  needs no initialisation and holds nothing between calls; calls that share one
  *                  workspace must not overlap in time (use one per stream).
@@ -316,10 +320,15 @@ specdec_status_t specdec_wait(void* stream, int32_t timeout_ms);
  *                     give up at once, it waits (at most 1 s more) for the copies already in
  *                     flight, and the request gets SPECDEC_ST_DEVICE_TIMEOUT; its other outputs
  *                     are then undefined. Nothing traps or hangs, and later calls are unaffected.
+ *   split_requests    -1: automatic; 0: none; n > 0: n. How many of the heaviest requests a
+ *                     scheduled launch of one CTA per request (a workspace, no top-k / top-p)
+ *                     splits over a cluster of 2 CTAs, the other requests then running two per
+ *                     cluster, one per CTA. Automatic: when the batch has more requests than one
+ *                     wave of resident CTAs (two per SM), the heaviest sixth of a wave of them.
  * Returns SPECDEC_ERR_INVALID_ARG (nothing changed) for a value outside those ranges.
  */
 specdec_status_t specdec_set_launch_options(int32_t kernel, int32_t ctas_per_request, int32_t schedule,
-                                            int32_t wait_limit_us);
+                                            int32_t wait_limit_us, int32_t split_requests);
 
 /* Bytes of workspace specdec_verify uses for B requests of vocabulary size V (0 if B or V <= 0):
  * the request order (int32 per request) and one cost byte per request. */
@@ -333,14 +342,17 @@ const char* specdec_status_string(specdec_status_t status);
  * vocabulary size V (host arithmetic; the SM count comes from the current device, 152 when none
  * is visible): CTAs per request (a thread-block cluster that splits every vocabulary row into
  * contiguous slices), threads per CTA, dynamic shared memory per CTA in bytes, vocabulary ids
- * per slice, and the number of kernels one call launches when given a workspace (2 when the
- * request schedule runs, else 1; without a workspace it is always 1). Any output pointer may be
- * NULL. Returns SPECDEC_ERR_INVALID_ARG / SPECDEC_ERR_UNSUPPORTED like specdec_verify.
+ * per slice, the number of kernels one call launches when given a workspace (2 when the
+ * request schedule runs, else 1; without a workspace it is always 1), and how many requests a
+ * call with a workspace and without top-k / top-p splits over clusters of 2 CTAs (0: none; the
+ * others then run two per cluster, one per CTA, and the grid has 2 * (n + ceil((B - n) / 2))
+ * CTAs). Any output pointer may be NULL. Returns SPECDEC_ERR_INVALID_ARG /
+ * SPECDEC_ERR_UNSUPPORTED like specdec_verify.
  */
 specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                        int32_t* ctas_per_request, int32_t* threads_per_cta,
                                        int32_t* smem_bytes, int32_t* slice_ids,
-                                       int32_t* kernels_with_workspace);
+                                       int32_t* kernels_with_workspace, int32_t* split_requests);
 
 #ifdef __cplusplus
 }

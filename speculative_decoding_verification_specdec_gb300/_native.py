@@ -70,9 +70,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.specdec_status_string.restype = ctypes.c_char_p
     lib.specdec_status_string.argtypes = [ctypes.c_int]
     lib.specdec_launch_config.restype = ctypes.c_int
-    lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp, vp]
+    lib.specdec_launch_config.argtypes = [i32, i32, ctypes.c_int, vp, vp, vp, vp, vp, vp]
     lib.specdec_set_launch_options.restype = ctypes.c_int
-    lib.specdec_set_launch_options.argtypes = [i32, i32, i32, i32]
+    lib.specdec_set_launch_options.argtypes = [i32, i32, i32, i32, i32]
     _lib = lib
     return lib
 
@@ -82,24 +82,26 @@ def status_string(status: int) -> str:
 
 
 def launch_config(V: int, dtype: int, B: int = 1024) -> dict:
-    c, t, s, w, k = (ctypes.c_int32() for _ in range(5))
+    c, t, s, w, k, n = (ctypes.c_int32() for _ in range(6))
     rc = load().specdec_launch_config(int(B), int(V), int(dtype), ctypes.byref(c), ctypes.byref(t),
-                                      ctypes.byref(s), ctypes.byref(w), ctypes.byref(k))
+                                      ctypes.byref(s), ctypes.byref(w), ctypes.byref(k), ctypes.byref(n))
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_launch_config")
     return {"ctas_per_request": c.value, "threads_per_cta": t.value, "smem_bytes": s.value,
-            "slice_ids": w.value, "kernels_with_workspace": k.value}
+            "slice_ids": w.value, "kernels_with_workspace": k.value, "split_requests": n.value}
 
 
 _KERNELS = {None: -1, "stream": 0, "cluster": 1}
 
 
 def set_launch_options(kernel: Optional[str] = None, ctas_per_request: Optional[int] = None,
-                       schedule: Optional[bool] = None, wait_limit_us: Optional[int] = None) -> None:
+                       schedule: Optional[bool] = None, wait_limit_us: Optional[int] = None,
+                       split_requests: Optional[int] = None) -> None:
     """specdec_set_launch_options: None leaves a choice to the library."""
     rc = load().specdec_set_launch_options(_KERNELS[kernel], -1 if ctas_per_request is None else int(ctas_per_request),
                                            -1 if schedule is None else int(bool(schedule)),
-                                           -1 if wait_limit_us is None else int(wait_limit_us))
+                                           -1 if wait_limit_us is None else int(wait_limit_us),
+                                           -1 if split_requests is None else int(split_requests))
     if rc != SPECDEC_OK:
         raise SpecdecError(rc, "specdec_set_launch_options")
 

@@ -128,6 +128,9 @@ struct Args {
     // request schedule: cluster i verifies request order[i] (a permutation of [0, B), heaviest
     // expected work first), or request i when NULL
     const int32_t* order;
+    // streaming kernel with clusters of 2 (G = 2): the first split_n requests of the order are split
+    // over both CTAs of a cluster, every later cluster runs two requests, one per CTA; 0: off
+    int32_t split_n;
     unsigned long long wait_ns;   // streaming kernel: limit of each wait on an mbarrier
 };
 
@@ -1589,14 +1592,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
     __shared__ StreamShared sh;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int NC = a.G;                                           // CTAs per request (cluster)
-    const int rank = (int)cluster_ctarank();
-    const int lo = rank * a.slice_units * kUnit;
-    const int hi = min(a.V, lo + a.slice_units * kUnit);
-    const int nrow_chunks = (hi - lo + G::kRowIds - 1) / G::kRowIds;
-    // at least one chunk of the next row is issued only after the pending decision was read,
-    // so consumers can never post two decisions ahead of the producer
-    const int spec = min(kSpec, nrow_chunks - 1);
+    const int NCL = a.G;                                          // CTAs per cluster (launch)
+    const int rank_hw = (int)cluster_ctarank();
 
     if (tid == 0) {
         const uint32_t full_count = a.bulk ? 1u : 32u;
@@ -1605,16 +1602,38 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             mbar_init(smem_addr(&sh.empty[s]), kConsumerWarps);
         }
         mbar_init(smem_addr(&sh.dec), 1);
-        mbar_init(smem_addr(&sh.pbar[0]), (uint32_t)NC);
-        mbar_init(smem_addr(&sh.pbar[1]), (uint32_t)NC);
+        mbar_init(smem_addr(&sh.pbar[0]), (uint32_t)NCL);
+        mbar_init(smem_addr(&sh.pbar[1]), (uint32_t)NCL);
         fence_mbar_init();
         sh.timed_out = 0;
         sh.issued = 0;
     }
-    // every CTA of the request has initialised its barriers before any partial is sent
-    if (NC > 1) cluster_sync_all(); else __syncthreads();
+    // every CTA of the cluster has initialised its barriers before any partial is sent
+    if (NCL > 1) cluster_sync_all(); else __syncthreads();
     grid_dependency_wait();                                        // the request order is ready
-    const int b = a.order ? a.order[cluster_id_x()] : (int)cluster_id_x();
+    // The request and the CTAs that verify it. Normally the cluster's NCL CTAs split request
+    // order[i] (or i). A launch with split_n > 0 (clusters of 2) splits only the first split_n
+    // requests of the order (the heaviest expected chains); every later cluster runs two requests,
+    // one per CTA, independently.
+    const int ci = (int)cluster_id_x();
+    int b, NC, rank;
+    if (a.split_n > 0 && ci >= a.split_n) {
+        const int pos = a.split_n + 2 * (ci - a.split_n) + rank_hw;
+        b = pos < a.B ? a.order[pos] : -1;
+        NC = 1;
+        rank = 0;
+    } else {
+        b = a.order ? a.order[ci] : ci;
+        NC = NCL;
+        rank = rank_hw;
+    }
+    if (b < 0) return;                    // the second CTA of the last pair when B - split_n is odd
+    const int lo = rank * a.slice_units * kUnit;
+    const int hi = NC > 1 ? min(a.V, lo + a.slice_units * kUnit) : a.V;
+    const int nrow_chunks = (hi - lo + G::kRowIds - 1) / G::kRowIds;
+    // at least one chunk of the next row is issued only after the pending decision was read,
+    // so consumers can never post two decisions ahead of the producer
+    const int spec = min(kSpec, nrow_chunks - 1);
 
     const ReqShape rs = request_shape(a, b);
 
@@ -2905,11 +2924,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
 // are the same under any order.
 //
 // One CTA computes an integer cost key per request and a stable counting sort of the keys,
-// descending, into order[B]. The key estimates the request's HBM work in units of 1/16 of a
-// dense logits row, without knowing where it will stop:
-//   rows: (k + 1) * 0.6 (greedy) or * 0.35 (sampled: a rejection ends the chain sooner),
-//   draw: 0.85 * (bytes per id of logits + noise [+ q]) / (bytes per id of logits),
-//   sparse requests (the same test the verify kernel applies): a quarter of that.
+// descending, into order[B]. The key estimates the request's duration in units of 1/16 of a
+// dense logits row pass, without knowing where it will stop:
+//   rows: 1 + 0.6 k for a draft-model request (its drafts are mostly accepted), 1 + 0.3 k for a
+//   greedy one, one race row over logits + noise for a sampled model-free one (accepted with
+//   probability p(x), usually small); a sparse row (the same test the verify kernel applies)
+//   counts 0.65 of a dense one;
+//   a draft-model request's draw over logits, noise and q: 0.85 * (bytes per id of the three) /
+//   (bytes per id of logits) when dense, 0.7 when sparse.
 
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedWarps = kSchedThreads / 32;
@@ -2942,12 +2964,22 @@ __device__ __forceinline__ int request_cost_key(const Args& a, int b)
         sparse = 2 * ones < nw * 32;
     }
     constexpr float es = (float)sizeof(ET);
-    float cost = (float)(rs.k + 1) * (greedy ? 0.6f : 0.35f);
+    // a sparse row gathers a fraction of the bytes but is a chain of dependent steps (mask scan,
+    // list, gathers, fold, reduce): in time it costs about 0.65 of a dense row
+    const float row = sparse ? 0.65f : 1.f;
+    // expected rows by kind: a draft model's drafts are mostly accepted (q close to p); a sampled
+    // model-free draft is accepted with probability p(x), usually small, so such a request is
+    // about one race row over logits + noise; a greedy draft only when it is the argmax
+    float rows;
+    if (greedy) rows = 1.f + 0.3f * (float)rs.k;
+    else if (qmode) rows = 1.f + 0.6f * (float)rs.k;
+    else rows = sparse ? 1.f : 0.85f * (es + 4.f) / es;
+    float cost = rows * row;
     // a top-k / top-p request streams each row once more per digit of each threshold search
     const Filter f = request_filter(a, b);
     if (f.on) cost *= 1.f + (float)(((f.k > 0) + (f.p < 1.f)) * (sizeof(ET) == 2 ? 2 : 4));
-    if (!greedy) cost += 0.85f * (es + 4.f + (qmode ? 4.f : 0.f)) / es;
-    if (sparse) cost *= 0.25f;
+    // a rejected draft-model row: a second pass over logits, noise and q
+    if (!greedy && qmode) cost += sparse ? 0.7f : 0.85f * (es + 8.f) / es;
     return min(kSchedKeys - 1, (int)(cost * 16.f + 0.5f));
 }
 
@@ -3074,6 +3106,7 @@ struct LaunchOptions {
     std::atomic<int> ctas{-1};         // CTAs per request, 1..kMaxCluster
     std::atomic<int> schedule{-1};     // 0 off, 1 on (with a workspace)
     std::atomic<long long> wait_us{-1};  // limit of each wait in the streaming kernel (-1: 2 s)
+    std::atomic<int> split{-1};        // requests split over a cluster of 2 (-1: automatic)
 };
 
 LaunchOptions& launch_options()
@@ -3176,7 +3209,7 @@ int schedulable_cluster(void (*kernel)(Args), int G, int smem, int threads, cuda
 }
 
 template <typename ET>
-specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t stream, bool after_schedule)
+specdec_status_t launch(Args args, LaunchShape sh, int32_t clusters, cudaStream_t stream, bool after_schedule)
 {
     if (configure_kernel_once<ET>() != cudaSuccess) return SPECDEC_ERR_CUDA;
     void (*kernel)(Args) = !sh.stream ? specdec_verify_kernel<ET>
@@ -3205,10 +3238,15 @@ specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t strea
             if (!sh.stream) sh.smem = (int)(su * kUnit * es + su * (kUnit / 32) * 4);
             args.G = sh.G;
             args.slice_units = sh.slice_units;
+            if (args.split_n > 0) {
+                // no cluster of 2 fits: one CTA per request, in the same order
+                clusters = args.B;
+                args.split_n = 0;
+            }
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)B * (unsigned)sh.G, 1, 1);
+    cfg.gridDim = dim3((unsigned)clusters * (unsigned)sh.G, 1, 1);
     cfg.blockDim = dim3((unsigned)sh.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)sh.smem;
     cfg.stream = stream;
@@ -3232,6 +3270,21 @@ specdec_status_t launch(Args args, LaunchShape sh, int32_t B, cudaStream_t strea
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 inline size_t round16(size_t x) { return (x + 15) & ~(size_t)15; }
+
+// How many of the heaviest requests a scheduled one-CTA-per-request launch splits over a cluster of
+// 2 CTAs: automatically, when the batch exceeds one wave of resident CTAs, a sixth of that wave
+// (their pairs of CTAs take a third of it; the rest starts the other requests). Measured on the
+// large mixed batch (1024 requests, 304 resident CTAs): 0 -> 202.6 us, 32 -> 188.4, 48 -> 187.4,
+// 64 -> 188.4, 96 -> 188.4, 128 -> 190.5. The launch options can force a number.
+int32_t split_requests(int32_t B)
+{
+    if (launch_options().schedule.load() == 0) return 0;          // the split follows the schedule
+    const int forced = launch_options().split.load();
+    if (forced >= 0) return forced < B ? forced : B;
+    const long long slots = (long long)kResidentPerSM * device_sms();
+    if ((long long)B <= slots) return 0;
+    return (int32_t)(slots / 6 < B ? slots / 6 : B);
+}
 
 // Whether a call with a workspace runs the schedule kernel first: only when the grid does not fit
 // in one wave of resident CTAs (with everything resident at once the order changes nothing),
@@ -3341,16 +3394,19 @@ void* noalloc_scratch(int dev)
 extern "C" specdec_status_t specdec_launch_config(int32_t B, int32_t V, specdec_dtype_t logits_dtype,
                                                   int32_t* ctas_per_request, int32_t* threads_per_cta,
                                                   int32_t* smem_bytes, int32_t* slice_ids,
-                                                  int32_t* kernels_with_workspace)
+                                                  int32_t* kernels_with_workspace, int32_t* split_requests_out)
 {
     LaunchShape s;
     const specdec_status_t rc = shape_for(V, logits_dtype, B, &s);
     if (rc != SPECDEC_OK) return rc;
+    const long long units = ((long long)V + kUnit - 1) / kUnit;
+    const int32_t split = (B > 0 && s.stream && s.G == 1 && units >= 2) ? split_requests(B) : 0;
     if (ctas_per_request) *ctas_per_request = s.G;
     if (threads_per_cta) *threads_per_cta = s.threads;
     if (smem_bytes) *smem_bytes = s.smem;
     if (slice_ids) *slice_ids = s.slice_units * kUnit;
-    if (kernels_with_workspace) *kernels_with_workspace = (B > 0 && schedule_wanted(B, s.G)) ? 2 : 1;
+    if (kernels_with_workspace) *kernels_with_workspace = (B > 0 && (split > 0 || schedule_wanted(B, s.G))) ? 2 : 1;
+    if (split_requests_out) *split_requests_out = split;
     return SPECDEC_OK;
 }
 
@@ -3421,6 +3477,7 @@ extern "C" specdec_status_t specdec_verify(
              (!draft_probs || aligned(draft_probs, 16));
     a.vec_noise = aligned(exp_noise, 16) && V % 4 == 0 && (!draft_probs || aligned(draft_probs, 16));
     a.order = nullptr;
+    a.split_n = 0;
     const long long wait_us = launch_options().wait_us.load();
     a.wait_ns = wait_us < 0 ? kWaitLimitNs : (unsigned long long)wait_us * 1000ull;
     const cudaStream_t st = (cudaStream_t)stream;
@@ -3428,8 +3485,27 @@ extern "C" specdec_status_t specdec_verify(
         const ScheduleLayout L = schedule_layout(B);
         if (!aligned(workspace, 16) || workspace_bytes < L.bytes) return SPECDEC_ERR_INVALID_ARG;
     }
+    // A batch of more requests than resident CTAs, one CTA per request, scheduled: the chains of
+    // the heaviest requests set the launch's length (they run at one CTA's share of HBM while the
+    // rest fill in behind), so the first split_n requests of the order are split over a cluster
+    // of 2 CTAs and the rest run two per cluster, one per CTA (split_requests()).
+    int32_t clusters = B;
+    const int32_t split = (workspace != nullptr && shape.stream && shape.G == 1 && !top_k && !top_p)
+                              ? split_requests(B) : 0;
+    if (split > 0) {
+        const long long units = ((long long)V + kUnit - 1) / kUnit;
+        const long long su = (units + 1) / 2;
+        if ((units + su - 1) / su == 2) {                 // both CTAs own a non-empty half of every row
+            shape.G = 2;
+            shape.slice_units = (int)su;
+            a.G = 2;
+            a.slice_units = (int)su;
+            a.split_n = split;
+            clusters = split + (B - split + 1) / 2;
+        }
+    }
     // heaviest requests first: the schedule kernel writes the order the verify kernel reads
-    if (workspace != nullptr && schedule_wanted(B, shape.G)) {
+    if (workspace != nullptr && (a.split_n > 0 || schedule_wanted(B, shape.G))) {
         const ScheduleLayout L = schedule_layout(B);
         unsigned char* ws = static_cast<unsigned char*>(workspace);
         int32_t* order = reinterpret_cast<int32_t*>(ws + L.order_off);
@@ -3440,7 +3516,8 @@ extern "C" specdec_status_t specdec_verify(
         a.order = order;
     }
     const bool dep = a.order != nullptr;
-    return logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, B, st, dep) : launch<uint16_t>(a, shape, B, st, dep);
+    return logits_dtype == SPECDEC_F32 ? launch<float>(a, shape, clusters, st, dep)
+                                       : launch<uint16_t>(a, shape, clusters, st, dep);
 }
 
 extern "C" specdec_status_t specdec_verify_noalloc(
@@ -3471,17 +3548,18 @@ extern "C" specdec_status_t specdec_verify_noalloc(
 }
 
 extern "C" specdec_status_t specdec_set_launch_options(int32_t kernel, int32_t ctas_per_request, int32_t schedule,
-                                                       int32_t wait_limit_us)
+                                                       int32_t wait_limit_us, int32_t split_requests)
 {
     if (kernel < -1 || kernel > 1 || schedule < -1 || schedule > 1 || ctas_per_request == 0 ||
         ctas_per_request < -1 || ctas_per_request > kMaxCluster || wait_limit_us < -1 ||
-        wait_limit_us > 2000000)
+        wait_limit_us > 2000000 || split_requests < -1)
         return SPECDEC_ERR_INVALID_ARG;
     LaunchOptions& o = launch_options();
     o.kernel = kernel;
     o.ctas = ctas_per_request;
     o.schedule = schedule;
     o.wait_us = wait_limit_us;
+    o.split = split_requests;
     return SPECDEC_OK;
 }
 

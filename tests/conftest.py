@@ -28,11 +28,13 @@ def oracle_lib():
 @pytest.fixture
 def launch_options():
     """Force the library's launch choices for one test (specdec_set_launch_options): call it with
-    kernel=, ctas_per_request=, schedule= and/or wait_limit_us= (None: the library decides). Every
+    kernel=, ctas_per_request=, schedule=, wait_limit_us= and/or split_requests= (None: the library
+    decides). Every
     choice is put back to automatic afterwards."""
     from speculative_decoding_verification_specdec_gb300 import _native
 
-    state = {"kernel": None, "ctas_per_request": None, "schedule": None, "wait_limit_us": None}
+    state = {"kernel": None, "ctas_per_request": None, "schedule": None, "wait_limit_us": None,
+             "split_requests": None}
 
     def set_(**kw):
         state.update(kw)

@@ -73,19 +73,38 @@ def test_launch_config_reports_the_schedule(lib, launch_options):
     assert _native.launch_config(32000, 0, B=64)["kernels_with_workspace"] == 2
     launch_options(schedule=False)
     assert _native.launch_config(151936, 1, B=1024)["kernels_with_workspace"] == 1
+    assert _native.launch_config(151936, 1, B=1024)["split_requests"] == 0
+
+
+def test_launch_config_reports_the_split(lib, launch_options):
+    """A scheduled batch larger than one wave of resident CTAs (304 when no device is visible) splits
+    its heaviest sixth of a wave over clusters of 2; smaller batches, and forced counts, as set."""
+    launch_options(kernel="stream")
+    assert _native.launch_config(151936, 1, B=1024)["split_requests"] == 50
+    assert _native.launch_config(151936, 1, B=200)["split_requests"] == 0
+    assert _native.launch_config(151936, 0, B=128)["split_requests"] == 0
+    launch_options(split_requests=7)
+    c = _native.launch_config(32000, 0, B=40)
+    assert c["ctas_per_request"] > 1 and c["split_requests"] == 0      # small batches use clusters per request
+    launch_options(ctas_per_request=1, split_requests=7)
+    assert _native.launch_config(32000, 0, B=40)["split_requests"] == 7
+    assert _native.launch_config(32000, 0, B=5)["split_requests"] == 5  # capped at B
+    launch_options(ctas_per_request=1, split_requests=0)
+    assert _native.launch_config(151936, 1, B=1024)["split_requests"] == 0
 
 
 def test_launch_options_validation(lib):
     """specdec_set_launch_options refuses values outside its ranges and changes nothing then."""
     E = _native
-    for bad in ((2, -1, -1, -1), (-2, -1, -1, -1), (-1, 0, -1, -1), (-1, 17, -1, -1), (-1, -2, -1, -1),
-                (-1, -1, 2, -1), (-1, -1, -2, -1), (-1, -1, -1, -2), (-1, -1, -1, 2000001)):
+    for bad in ((2, -1, -1, -1, -1), (-2, -1, -1, -1, -1), (-1, 0, -1, -1, -1), (-1, 17, -1, -1, -1),
+                (-1, -2, -1, -1, -1), (-1, -1, 2, -1, -1), (-1, -1, -2, -1, -1), (-1, -1, -1, -2, -1),
+                (-1, -1, -1, 2000001, -1), (-1, -1, -1, -1, -2)):
         assert lib.specdec_set_launch_options(*bad) == E.SPECDEC_ERR_INVALID_ARG, bad
-    assert lib.specdec_set_launch_options(-1, 16, 1, 0) == E.SPECDEC_OK
+    assert lib.specdec_set_launch_options(-1, 16, 1, 0, 5) == E.SPECDEC_OK
     assert _native.launch_config(1000, 0, B=4096)["kernels_with_workspace"] == 2
-    assert lib.specdec_set_launch_options(-1, -1, 7, -1) == E.SPECDEC_ERR_INVALID_ARG
+    assert lib.specdec_set_launch_options(-1, -1, 7, -1, -1) == E.SPECDEC_ERR_INVALID_ARG
     assert _native.launch_config(1000, 0, B=4096)["kernels_with_workspace"] == 2     # unchanged
-    assert lib.specdec_set_launch_options(-1, -1, -1, -1) == E.SPECDEC_OK
+    assert lib.specdec_set_launch_options(-1, -1, -1, -1, -1) == E.SPECDEC_OK
 
 
 def test_launch_config_rejects(lib, launch_options):

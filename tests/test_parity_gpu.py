@@ -400,3 +400,16 @@ def test_device_wait_expiry_is_reported_and_the_context_stays_usable(cuda, ctas,
     assert timed.all(), got["status"]
     launch_options(wait_limit_us=None)
     check_parity(w, cuda)
+
+
+@pytest.mark.parametrize("split", [1, 4, 40])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_split_heavy_requests_parity(cuda, split, dtype, launch_options):
+    """Clusters of 2 CTAs: the first `split` requests of the schedule are split over both CTAs of a
+    cluster, the others run two per cluster, one per CTA (an odd remainder leaves the last
+    cluster's second CTA without a request). Every request matches the oracle."""
+    launch_options(kernel="stream", ctas_per_request=1, schedule=True, split_requests=split)
+    w = W.make_batch(600 + split, name=f"split{split}_{dtype}", B=40, V=9000, k=(0, 6), logits_dtype=dtype,
+                     logit_sigma=3.0, temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
+                     mask="half", mask_density=0.1, mask_run_len=16, forced_invalid_frac=0.2)
+    check_parity(w, cuda)
