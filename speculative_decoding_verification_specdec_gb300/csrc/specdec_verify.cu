@@ -65,8 +65,11 @@ extern "C" int specdec_trace_set(void* buffer)
     const bool trace_on_ = (on);                                                                   \
     unsigned long long* trace_ = g_specdec_trace ? g_specdec_trace + (size_t)(req) * 64 : nullptr;
 // -DSPECDEC_TRACE_LIGHT keeps only the first and last stamp of each request (tags 0 and 7), so
-// the timing of the phases in between is not disturbed.
-#ifdef SPECDEC_TRACE_LIGHT
+// the timing of the phases in between is not disturbed; -DSPECDEC_TRACE_TAGS=mask keeps the tags
+// whose bits are set.
+#if defined(SPECDEC_TRACE_TAGS)
+#define SPECDEC_TRACE_KEEP(tag) (((SPECDEC_TRACE_TAGS) >> (tag)) & 1)
+#elif defined(SPECDEC_TRACE_LIGHT)
 #define SPECDEC_TRACE_KEEP(tag) ((tag) == 0 || (tag) == 7)
 #else
 #define SPECDEC_TRACE_KEEP(tag) true
@@ -1891,7 +1894,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 return -1;
             }
             // fixed trip count (no loop over set bits): allowed ids come in runs, and a loop over
-            // set bits would serialise each warp on its densest word
+            // set bits would serialise each warp on its densest word (slots from per-word popcount
+            // prefixes instead of the running count measured slower still)
             load_words();
 #pragma unroll
             for (int q = 0; q < kPer; ++q) {
