@@ -413,3 +413,57 @@ def test_split_heavy_requests_parity(cuda, split, dtype, launch_options):
                      logit_sigma=3.0, temperature="half_greedy(0.5,1.2)", q_mode="half", draft_sigma=0.5,
                      mask="half", mask_density=0.1, mask_run_len=16, forced_invalid_frac=0.2)
     check_parity(w, cuda)
+
+
+def _tie_batch(V, dtype, ties, allowed=None, seed=0, name="ties"):
+    """Greedy requests over rows whose maximum (an integer logit, exact in bf16) sits at every
+    position in `ties`: a bonus-only request, a draft on a later copy of the maximum (rejected:
+    the lowest index is the argmax), a draft on the lowest copy (accepted; its bonus row ties
+    too), and two drafts (the second on a later copy)."""
+    rng = np.random.default_rng([seed, V])
+    ks = [0, 1, 1, 2]
+    T = sum(ks) + len(ks)
+    z = rng.integers(-60, 60, size=(T, V)).astype(np.float32)
+    z[:, ties] = 100.0
+    lo, later = ties[0], ties[-1]
+    drafts = [later, lo, lo, later]
+    return batch(V=V, ks=ks, logits=z, draft_ids=drafts, temperature=0.0, allowed=allowed, dtype=dtype,
+                 name=name), lo
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 4])
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_greedy_ties_across_slices_and_chunks(cuda, ctas, dtype, launch_options):
+    """The row maximum occurs in several CTAs' slices of a cluster and in several ring chunks of a
+    slice: every CTA and every chunk folds to its own lowest index, and the fold across them keeps
+    the lowest, so every emitted token is the first copy of the maximum."""
+    launch_options(kernel="stream", ctas_per_request=ctas)
+    V = 40000
+    ties = [11000, 5, 9000, 10500, 19999, 30001, 39990]
+    w, lo = _tie_batch(V, dtype, sorted(ties), name=f"ties_G{ctas}_{dtype}")
+    rep, got, ref = check_parity(w, cuda)
+    cu = w.cu_num_draft
+    assert got["out_tokens"][rows_of(cu, 0, 0)] == lo                 # bonus only
+    assert got["out_tokens"][rows_of(cu, 1, 0)] == lo                 # later copy rejected, lowest emitted
+    assert got["out_num_accepted"][2] == 1 and got["out_tokens"][rows_of(cu, 2, 1)] == lo
+    assert got["out_num_accepted"][3] == 1 and got["out_tokens"][rows_of(cu, 3, 1)] == lo
+
+
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_greedy_ties_across_sparse_list_segments(cuda, dtype, launch_options):
+    """A sparse bitmask over a vocabulary wider than one list segment (5120 mask words): the maximum
+    is allowed in both segments and in several 16-byte groups of each; the lowest allowed copy wins."""
+    launch_options(kernel="stream", ctas_per_request=1)
+    V = 200064                                        # 6252 mask words: two list segments
+    ties = [777, 3001, 120003, 170000, 199999]
+    w0, _ = _tie_batch(V, dtype, ties, name="shape")
+    rng = np.random.default_rng(9)
+    allowed = rng.random((w0.T, V)) < 0.05
+    allowed[:, ties] = True
+    allowed[:, 777] = False                           # the first copy is forbidden: 3001 must win
+    w, _ = _tie_batch(V, dtype, ties, allowed=allowed, name=f"ties_sparse_{dtype}")
+    assert _native.launch_config(V, 1 if dtype == W.BF16 else 0, B=w.B)["ctas_per_request"] == 1
+    rep, got, ref = check_parity(w, cuda)
+    cu = w.cu_num_draft
+    assert got["out_tokens"][rows_of(cu, 0, 0)] == 3001
+    assert got["out_tokens"][rows_of(cu, 1, 0)] == 3001
