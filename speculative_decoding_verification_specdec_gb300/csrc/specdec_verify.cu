@@ -1955,7 +1955,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         softmax_batch<U * VE>(p, mc, z, c);
                     }
                 }
-                consumer_sync();                          // the data region is free again
+                // the data region is free again before the next batch's copies (after the last
+                // batch, the reduction's or the next list's barrier comes before any new copy)
+                if (b0 + kGatherCap < n) consumer_sync();
             }
         };
         // Sparse draw pass over list[0, n) of row t: logits, noise and (q-mode) q of the listed
@@ -2012,7 +2014,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     }
                     draw_batch<U * VE>(dp, z, ev, qv, ids, code, x, c, MC, invS);
                 }
-                consumer_sync();
+                if (b0 + cap < n) consumer_sync();       // (as in sparse_stats)
             }
         };
         // Sparse race pass over list[0, n) of row t (race rows, see race_raise): logits and noise of
@@ -2067,7 +2069,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     }
                     race_batch<U * VE>(p, mc, z, ev, ids, x, c);
                 }
-                consumer_sync();
+                if (b0 + cap < n) consumer_sync();       // (as in sparse_stats)
             }
         };
 
