@@ -429,6 +429,17 @@ template <> struct Elem<uint16_t> {       // bf16 bit patterns
     }
 };
 
+// One logit from global memory, as fp32
+template <typename ET> __device__ __forceinline__ float load_logit(const void* logits, int64_t i);
+template <> __device__ __forceinline__ float load_logit<float>(const void* logits, int64_t i)
+{
+    return __ldg(reinterpret_cast<const float*>(logits) + i);
+}
+template <> __device__ __forceinline__ float load_logit<uint16_t>(const void* logits, int64_t i)
+{
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(logits) + i) << 16);
+}
+
 // Allowed-bits of vector v (VE ids) of the slice; all ones when there is no bitmask.
 template <int VE>
 __device__ __forceinline__ uint32_t vec_bits(const uint32_t* smask, bool has_mask, int v)
@@ -858,14 +869,15 @@ struct StreamShared {
     uint32_t fcnt[256];
     uint32_t flo[256], fhi[256];
     uint32_t fw_cnt[kConsumerWarps], fw_kmin[kConsumerWarps], fw_kmax[kConsumerWarps];  // per-warp partials
+    float fw_a[kConsumerWarps];
     unsigned long long fw_m[kConsumerWarps], fw_m2[kConsumerWarps];
     unsigned long long ftail_m;          // first pass: tail mass in units of 2^-54
     uint32_t fsel_digit;                 // chosen digit (0xffffffff: none)
     uint32_t fsel_pad;
     unsigned long long fsel_cnt;         // count above the chosen digit (this level)
-    double fsel_mass, fsel_at;           // mass above the chosen digit / of the digit itself
-    double ftot_mass;                    // mass of every element counted in this pass
-    double fsel_P;                       // the top-p target mass the choice used
+    unsigned long long fsel_mass, fsel_at;   // mass above the chosen digit / of the digit itself (2^-40)
+    unsigned long long ftot_mass;        // mass of every element counted in this pass (2^-40)
+    unsigned long long fsel_P;           // the top-p target mass the choice used (2^-40)
     unsigned long long fsel_n;           // elements in the chosen digit (first top-p pass: a bound)
     uint32_t fc_kmin, fc_kmax;           // collection pass: the chosen bin's smallest / largest key
     unsigned long long fc_mbin;          // collection pass: the chosen bin's mass (its units)
@@ -1035,11 +1047,19 @@ __device__ __forceinline__ uint32_t mass_units(float e, bool tail)
     return tail ? __float2uint_rn(e * 0x1p54f) : ((__float_as_uint(e) & 0x7fffffu) | 0x800000u);
 }
 
-// 2^(exponent - 23) for the elements of mass bin mb (2^-54 for the tail)
-__device__ __forceinline__ double bin_scale(uint32_t mb)
+// The exponent of mass bin mb's unit: its elements' masses are mass_units times 2^bin_exp
+// (2^(exponent - 23) for bins 8..255, 2^-54 for the tail)
+__device__ __forceinline__ int bin_exp(uint32_t mb)
 {
-    const int ex = mb == 0u ? -54 : (int)((mb - 8u) >> 3) + 97 - 150;
-    return __longlong_as_double((long long)(ex + 1023) << 52);
+    return mb == 0u ? -54 : (int)(mb >> 3) - 54;
+}
+
+// units * 2^e as a fixed-point mass in units of 2^-40 (bits below 2^-40 dropped). Masses are at
+// most 1 each (relative to the row maximum), so sums over up to 2^20 elements stay below 2^60.
+__device__ __forceinline__ unsigned long long fx40(unsigned long long units, int e)
+{
+    const int s = e + 40;
+    return s >= 0 ? (units << s) : (s > -64 ? (units >> -s) : 0ull);
 }
 
 // Order-preserving 32-bit key of a logit (its fp32 bits): a larger logit has a larger key, and
@@ -1236,6 +1256,34 @@ __device__ __forceinline__ void softmax_fold_max(Part& p, float& mc, const float
 #pragma unroll
     for (int i = 0; i < N; ++i) e[i] = ex2_scaled(z[i], c, mc);
     p.S += tree_sum<N>(e);
+}
+
+// softmax_fold_max, and besides the count (cnt) and the mass (A, same reference as p.S) of the
+// elements whose logit is above zx: on a top-k / top-p row these bound the draft token's filtered
+// probability without the threshold search (the acceptance bound in the streaming kernel)
+template <int N>
+__device__ __forceinline__ void softmax_fold_max_above(Part& p, float& mc, float& A, uint32_t& cnt, const float* z,
+                                                       float bm, float c, float zx)
+{
+    if (!(bm > -INFINITY)) return;
+    if (bm > p.m) {
+        const float nmc = bm * c;
+        const float f = (p.m == -INFINITY) ? 0.f : ex2(mc - nmc);
+        p.S = (p.m == -INFINITY) ? 0.f : p.S * f;
+        A = (p.m == -INFINITY) ? 0.f : A * f;
+        p.m = bm;
+        mc = nmc;
+    }
+    float e[N], ea[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        e[i] = ex2_scaled(z[i], c, mc);
+        const bool above = z[i] > zx;
+        ea[i] = above ? e[i] : 0.f;
+        cnt += above ? 1u : 0u;
+    }
+    p.S += tree_sum<N>(e);
+    A += tree_sum<N>(ea);
 }
 
 // Draw fold of NB groups (ids base + u * stride + e); xslot = position of the one-hot draft or -1.
@@ -2248,59 +2296,62 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             };
             // digit choice by consumer warp 0: lane l holds digits 255 - 8l .. 248 - 8l (highest
             // first); per-lane sums, an exclusive scan over lanes, then each lane walks its digits.
-            // Bin masses in fp64 from the exact integer sums: bin_scale per bin in the first pass
-            // (bin0 < 0), the scale of mass bin bin0 in the later ones.
+            // Bin masses are fixed-point integers in units of 2^-40 (fx40 of the exact unit sums:
+            // each bin's own unit in the first pass (bin0 < 0), the unit of mass bin bin0 in the
+            // later ones), so the choice is integer arithmetic throughout.
             // mode 0 (top-k): the digit where the count from the top reaches `need`;
             // mode 1 (top-p): the lowest non-empty digit whose mass above (plus `above`) is below P
             // (P = p_frac of this pass's total when p_frac >= 0).
             // Everything the caller needs is copied to the fsel_ fields before the closing barrier:
             // the next pass clears the bins as soon as a thread reaches it.
-            auto select_digit = [&](int mode, unsigned long long need, double P, double above, int bin0,
-                                    double p_frac) {
+            auto select_digit = [&](int mode, unsigned long long need, unsigned long long P, unsigned long long above,
+                                    int bin0, float p_frac) {
                 if (cw == 0) {
-                    const double pscale = bin0 < 0 ? 0.0 : bin_scale((uint32_t)bin0);
-                    unsigned long long bc[8], lc = 0ull;
-                    double bm[8], lm = 0.0;
+                    const int pexp = bin0 < 0 ? 0 : bin_exp((uint32_t)bin0);
+                    // digit dg's count and mass (read again from the bins where needed: fewer live registers)
+                    auto dmass = [&](int dg) -> unsigned long long {
+                        const unsigned long long u = ((unsigned long long)sh.fhi[dg] << 12) + sh.flo[dg];
+                        if (bin0 >= 0) return fx40(u, pexp);
+                        return dg == 0 ? fx40(sh.ftail_m, -54) : (dg >= 8 ? fx40(u, bin_exp((uint32_t)dg)) : 0ull);
+                    };
+                    unsigned long long lc = 0ull, lm = 0ull;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int dg = 255 - 8 * lane - i;
-                        bc[i] = sh.fcnt[dg];
-                        if (bin0 < 0 && dg == 0) bm[i] = (double)sh.ftail_m * 0x1p-54;
-                        else bm[i] = ((double)sh.fhi[dg] * 4096.0 + (double)sh.flo[dg]) *
-                                     (bin0 < 0 ? (dg >= 8 ? bin_scale((uint32_t)dg) : 0.0) : pscale);
-                        lc += bc[i];
-                        lm += bm[i];
+                        lc += sh.fcnt[dg];
+                        lm += dmass(dg);
                     }
-                    unsigned long long ic = lc;
-                    double im = lm;
+                    unsigned long long ic = lc, im = lm;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const unsigned long long yc = __shfl_up_sync(0xffffffffu, ic, off);
-                        const double ym = __shfl_up_sync(0xffffffffu, im, off);
+                        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
                         if (lane >= off) { ic += yc; im += ym; }
                     }
-                    const double tot_m = __shfl_sync(0xffffffffu, im, 31);
-                    if (p_frac >= 0.0) P = p_frac * tot_m;
+                    const unsigned long long tot_m = __shfl_sync(0xffffffffu, im, 31);
+                    if (p_frac >= 0.f) P = (unsigned long long)((double)p_frac * (double)tot_m);
                     unsigned long long c0 = __shfl_up_sync(0xffffffffu, ic, 1);
-                    double m0 = __shfl_up_sync(0xffffffffu, im, 1);
-                    if (lane == 0) { c0 = 0ull; m0 = 0.0; }
-                    unsigned long long fc = 0ull, fn = 0ull;
-                    double fm = 0.0, fa = 0.0;
+                    unsigned long long m0 = __shfl_up_sync(0xffffffffu, im, 1);
+                    if (lane == 0) { c0 = 0ull; m0 = 0ull; }
+                    unsigned long long fc = 0ull, fn = 0ull, fm = 0ull, fa = 0ull;
                     int found = -1;
-#pragma unroll
+#pragma unroll 1
                     for (int i = 0; i < 8; ++i) {
                         const int dg = 255 - 8 * lane - i;
+                        const unsigned long long bc = sh.fcnt[dg], bm = dmass(dg);
                         // elements in the digit: counted, or (first top-p pass, bins from 8 up) at
                         // most the mass units over 2^23, the smallest significand
                         const unsigned long long n = (bin0 < 0 && mode == 1 && dg >= 8)
-                            ? (((unsigned long long)sh.fhi[dg] << 12) + sh.flo[dg]) >> 23 : bc[i];
+                            ? (((unsigned long long)sh.fhi[dg] << 12) + sh.flo[dg]) >> 23 : bc;
+                        // (a tail too light for 2^-40 is never the choice: its mass above is the total)
+                        const bool nonempty = bc != 0ull || bm != 0ull;
                         if (mode == 0) {
-                            if (found < 0 && c0 + bc[i] >= need) { found = dg; fc = c0; fm = m0; fa = bm[i]; fn = n; }
-                        } else if ((bc[i] != 0ull || bm[i] > 0.0) && above + m0 < P) {
-                            found = dg; fc = c0; fm = m0; fa = bm[i]; fn = n;
+                            if (found < 0 && c0 + bc >= need) { found = dg; fc = c0; fm = m0; fa = bm; fn = n; }
+                        } else if (nonempty && above + m0 < P) {
+                            found = dg; fc = c0; fm = m0; fa = bm; fn = n;
                         }
-                        c0 += bc[i];
-                        m0 += bm[i];
+                        c0 += bc;
+                        m0 += bm;
                     }
                     const unsigned who = __ballot_sync(0xffffffffu, found >= 0);
                     // top-k: the first lane that reaches `need`; top-p: the last lane with a candidate
@@ -2315,43 +2366,53 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 consumer_sync();
             };
             // One more pass for mass bin bc: the smallest and largest key and the mass of its
-            // elements (at or above floor_key), the mass above it (units of 2^-40), and, over the
-            // row (ncand < 0), the keys of its elements (all = false) or of every element from bin
-            // bc up (all = true) appended to the candidates. Returns the number of such elements
-            // (above kCandCap: only the first kCandCap kept). Over the first ncand candidates
-            // (ncand >= 0) nothing is appended and ncand comes back.
-            auto collect_pass = [&](int64_t t, int j, uint32_t bc, bool all, uint32_t floor_key, float MC,
-                                    int ncand) -> int {
+            // elements (at or above floor_key), the mass above it (units of 2^-40; only when
+            // sum_above), and, over the row (ncand < 0), the keys of its elements (all = false) or of
+            // every element from bin bc up (all = true) appended to the candidates. Returns the
+            // number of such elements (above kCandCap: only the first kCandCap kept). Over the first
+            // ncand candidates (ncand >= 0) nothing is appended and ncand comes back.
+            // The exponent argument z*c - MC of an element decides its bin, so a compare of that
+            // argument against the bin's bounds (widened by 1e-3, far more than the error of ex2)
+            // skips, before any other work, the elements that cannot fall in the bin (below it, and
+            // above it when neither their mass nor their keys are wanted).
+            auto collect_pass = [&](int64_t t, int j, uint32_t bc, bool all, bool sum_above, uint32_t floor_key,
+                                    float MC, int ncand) -> int {
                 if (ct == 0 && ncand < 0) sh.fncand = 0u;
                 consumer_sync();
                 SPECDEC_STAMP(10);
                 uint32_t kmn = 0xffffffffu, kmx = 0u;
                 unsigned long long mbin = 0ull, mab = 0ull;
+                const float bexp = (float)((int)(bc >> 3) - 31);           // log2 of the bin's octave
+                const float alo = bc == 0u ? -INFINITY : log2f((float)(8u + (bc & 7u)) * 0.125f) + bexp - 1e-3f;
+                const float ahi = (sum_above || all) ? INFINITY
+                                : (bc == 0u ? -30.f : log2f((float)(9u + (bc & 7u)) * 0.125f) + bexp) + 1e-3f;
                 auto take = [&](const auto& z, uint32_t valid) {
                     constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
-                    uint32_t key[N];
+                    float arg[N];
                     uint32_t in = 0u;
 #pragma unroll
                     for (int i = 0; i < N; ++i) {
-                        key[i] = logit_key(z[i]);
-                        in |= (((valid >> i) & 1u) && key[i] >= floor_key ? 1u : 0u) << i;
+                        arg[i] = fmaf(z[i], c, -MC);
+                        in |= (((valid >> i) & 1u) && arg[i] >= alo && arg[i] <= ahi ? 1u : 0u) << i;
                     }
                     if (in == 0u) return;
+                    uint32_t key[N];
                     float e[N];
                     uint32_t mb[N];
 #pragma unroll
                     for (int i = 0; i < N; ++i) {
-                        e[i] = ex2(fmaf(z[i], c, -MC));
+                        key[i] = logit_key(z[i]);
+                        e[i] = ex2(arg[i]);
                         mb[i] = mass_bin(e[i]);
                     }
 #pragma unroll
                     for (int i = 0; i < N; ++i) {
-                        if (!((in >> i) & 1u) || mb[i] < bc) continue;
+                        if (!((in >> i) & 1u) || key[i] < floor_key || mb[i] < bc) continue;
                         if (mb[i] == bc) {
                             kmn = min(kmn, key[i]);
                             kmx = max(kmx, key[i]);
                             mbin += mass_units(e[i], bc == 0u);
-                        } else {
+                        } else if (sum_above) {
                             mab += __float2ull_rn(e[i] * 0x1p40f);
                         }
                         if (ncand < 0 && (all || mb[i] == bc)) {
@@ -2419,9 +2480,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // then run over those candidates instead of the row. `ncand` >= 0 on entry means the
             // candidates already hold every element at or above floor_key, so the whole search
             // runs on chip; on return it is >= 0 when that holds for this search's kept elements.
-            auto search = [&](int64_t t, int j, int mode, unsigned long long need, double p_frac, uint32_t floor_key,
+            auto search = [&](int64_t t, int j, int mode, unsigned long long need, float p_frac, uint32_t floor_key,
                               float MC, float S, bool keep_above, bool& try_slice, int& ncand, uint32_t& key_out,
-                              double& mass_above, double& mass_at) -> bool {
+                              unsigned long long& mass_above, unsigned long long& mass_at) -> bool {
                 constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
                 int src0 = ncand;
                 // Top-k: first try the top slice of logits whose mass exp2(z*c - MC) is at least
@@ -2439,29 +2500,28 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 // on chip, the first pass takes counts and masses (the candidates are few)
                 hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu, src0,
                           src0 >= 0 ? 3 : (mode == 0 ? 1 : 2));
-                select_digit(mode, need, 0.0, 0.0, -1, mode == 1 ? p_frac : -1.0);
-                const double P = sh.fsel_P;
+                select_digit(mode, need, 0ull, 0ull, -1, mode == 1 ? p_frac : -1.f);
+                const unsigned long long P = sh.fsel_P;
                 const uint32_t b0 = sh.fsel_digit;
                 if (b0 == 0xffffffffu) {                             // top-k covers every element
                     mass_above = sh.ftot_mass;
-                    mass_at = 0.0;
+                    mass_at = 0ull;
                     return false;
                 }
                 const unsigned long long n_above = sh.fsel_cnt, n_bin = sh.fsel_n;
-                double above = sh.fsel_mass;                      // (first top-k pass: not summed)
+                unsigned long long above = sh.fsel_mass;          // (first top-k pass: not summed)
                 need -= n_above;
                 int src = src0;
                 if (top_slice) ncand = src0;             // every element at or above this search's key
                 else if (src0 < 0) ncand = -1;
                 const bool all = src0 < 0 && keep_above && n_above + n_bin <= (unsigned long long)kCandCap;
-                const int n = collect_pass(t, j, b0, all, floor_key, MC, src0);
+                const int n = collect_pass(t, j, b0, all, mode == 0, floor_key, MC, src0);
                 if (src0 < 0 && n <= kCandCap) {
                     src = n;
                     if (all) ncand = n;
                 }
-                const double bscale = bin_scale(b0);
-                if (mode == 0) above = (double)sh.fc_mabove * 0x1p-40;
-                double at = (double)sh.fc_mbin * bscale;
+                if (mode == 0) above = sh.fc_mabove;
+                unsigned long long at = fx40(sh.fc_mbin, bin_exp(b0));
                 uint32_t kmin = sh.fc_kmin;
                 const uint32_t kmax = sh.fc_kmax;
                 // resolve the keys of bin b0 from the highest bit where they differ, 8 bits a pass
@@ -2473,7 +2533,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         const int shift = max(kLowBit, top - 7);
                         const uint32_t width = (1u << (top - shift + 1)) - 1u;
                         hist_pass(t, j, (int)b0, pmask, pval, shift, width, floor_key, MC, kmin, kmax, src, 3);
-                        select_digit(mode, need, P, above, (int)b0, -1.0);
+                        select_digit(mode, need, P, above, (int)b0, -1.f);
                         const uint32_t dg = sh.fsel_digit;           // always found inside the bin
                         above += sh.fsel_mass;
                         at = sh.fsel_at;
@@ -2491,12 +2551,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             };
             auto filter_row = [&](int64_t t, int j, float MC, float S, uint32_t& kt, float& S_keep) -> bool {
                 uint32_t floor_key = 0u;
-                double keep = 0.0, above = 0.0, at = 0.0;
+                unsigned long long keep = 0ull, above = 0ull, at = 0ull;      // masses in units of 2^-40
                 int ncand = -1;                                  // candidates hold every kept element
                 bool cut_k = false;
                 if (fk > 0) {
                     uint32_t key;
-                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.0, 0u, MC, S, fp < 1.f, try_slice, ncand, key,
+                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.f, 0u, MC, S, fp < 1.f, try_slice, ncand, key,
                                    above, at);
                     if (cut_k) { floor_key = key; keep = above + at; }
                 }
@@ -2504,13 +2564,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (fp < 1.f) {
                     uint32_t key;
                     bool no_slice = false;
-                    cut_p = search(t, j, 1, 0ull, (double)fp, floor_key, MC, S, false, no_slice, ncand, key, above,
+                    cut_p = search(t, j, 1, 0ull, fp, floor_key, MC, S, false, no_slice, ncand, key, above,
                                    at);
                     if (cut_p) { floor_key = key; keep = above + at; }
                 }
                 kt = floor_key;
                 SPECDEC_STAMP(12);
-                S_keep = (float)keep;
+                S_keep = (float)keep * 0x1p-40f;
                 return cut_k || cut_p;
             };
 
@@ -2701,6 +2761,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 const bool race = race_req && (bonus || !qmode);
                 Part p = part_identity();
                 float mc = 0.f;                            // running round(m * c) (race rows: a whole number)
+                // acceptance bound of a filtered draft row (dense, one CTA, no per-draft diagnostics):
+                // the count and mass of the logits above the draft token's, from the statistics pass
+                const bool bound_on = kFilt && filt && !sparse && !bonus && j < g && NC == 1 && a.diag_alpha == nullptr;
+                float zxb = INFINITY, mass_above = 0.f;
+                uint32_t cnt_above = 0u;
+                if (bound_on) zxb = load_logit<ET>(a.logits, t * (int64_t)a.V + x);
 
                 if (!sparse && race) {
                     // ---- a2/a3/a5 + a9/a10 dense, one pass: logits, noise and mask words of the slice
@@ -2806,6 +2872,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                                 bm = tree_max<NB * VE>(z);
                             }
                             if (greedy) argmax_lazy<NB, VE>(p, z, bm, i0 + vb * VE, kConsumers * VE);
+                            else if (bound_on) softmax_fold_max_above<NB * VE>(p, mc, mass_above, cnt_above, z, bm, c, zxb);
                             else softmax_fold_max<NB * VE>(p, mc, z, bm, c);
                         }
                         // the draft token's logit, read once by the thread that owns its group
@@ -2865,7 +2932,42 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 uint32_t kt = 0u;
                 float S_keep = 0.f;
                 bool cut = false;
-                if constexpr (kFilt) cut = filt && r.m > -INFINITY && filter_row(t, j, r.m * c, r.S, kt, S_keep);
+                if constexpr (kFilt) {
+                    // Acceptance without the threshold search. Filtering only removes mass, so the kept
+                    // mass is at most the row's S and the filtered p'(x) at least e_x / S: a draft that is
+                    // surely kept and whose uniform lies below that bound's acceptance ratio is accepted
+                    // whatever the threshold is. Kept for sure: fewer than k logits above x (top-k),
+                    // and the mass above x below p of the total (top-p) or, after a top-k cut, below p
+                    // of the mass of x and everything above it (a lower bound of the top-k mass).
+                    // The fp32 sums here differ from the search's exact integer sums by far less than
+                    // the 1e-4 margins; a row the bound does not settle takes the search as before.
+                    bool sure = false;
+                    if (bound_on && r.m > -INFINITY && r.zx > -INFINITY) {
+                        const float MCb = r.m * c;
+                        float av = (p.m > -INFINITY) ? mass_above * ex2(mc - MCb) : 0.f;
+                        uint32_t cv = cnt_above;
+#pragma unroll
+                        for (int off = 16; off >= 1; off >>= 1) {
+                            av += __shfl_xor_sync(0xffffffffu, av, off);
+                            cv += __shfl_xor_sync(0xffffffffu, cv, off);
+                        }
+                        if (lane == 0) { sh.fw_a[cw] = av; sh.fw_cnt[cw] = cv; }
+                        consumer_sync();
+                        float A = 0.f;
+                        unsigned long long C = 0ull;
+#pragma unroll
+                        for (int w = 0; w < kConsumerWarps; ++w) { A += sh.fw_a[w]; C += sh.fw_cnt[w]; }
+                        const float Smc = fmaf(r.S, fmaf(r.m, c, -MCb) * 0.69314718f, r.S);
+                        const float ex = ex2_scaled(r.zx, c, MCb);
+                        constexpr float kLo = 1.f - 1e-4f, kHi = 1.f + 1e-4f;
+                        bool kept = fk <= 0 || C < (unsigned long long)fk;
+                        if (fp < 1.f) kept = kept && A * kHi < fp * (fk > 0 ? A + ex : Smc) * kLo;
+                        const float px_lo = ex / Smc * kLo;
+                        const float alpha_lo = !qmode ? px_lo : (px_lo >= sh.qxs[j] ? 1.f : px_lo / sh.qxs[j] * kLo);
+                        sure = kept && px_lo > 0.f && sh.us[j] < alpha_lo;
+                    }
+                    cut = filt && !sure && r.m > -INFINITY && filter_row(t, j, r.m * c, r.S, kt, S_keep);
+                }
                 bool stop;
                 float MC, S_mc;
                 const int code = decide(j, r, stop, MC, S_mc, cut, kt, S_keep);

@@ -132,13 +132,14 @@ def verify(w: Workload, dev: Dict[str, object], out: Outputs, stream=None) -> No
         telemetry=out.telemetry, top_k=dev.get("top_k"), top_p=dev.get("top_p"))
 
 
-def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True, guard: int = 0) -> Dict[str, np.ndarray]:
+def run(w: Workload, device="cuda", diag: bool = True, workspace: bool = True, guard: int = 0,
+        telemetry: Optional[bool] = None) -> Dict[str, np.ndarray]:
     """Copy, verify, synchronise, and return the outputs as numpy arrays (with guard > 0 also
     "guards_intact": whether every output's trailing guard elements are untouched)."""
     import torch
 
     dev = device_tensors(w, device)
-    out = alloc_outputs(w, device, diag=diag, workspace=workspace, guard=guard)
+    out = alloc_outputs(w, device, diag=diag, workspace=workspace, guard=guard, telemetry=telemetry)
     verify(w, dev, out)
     torch.cuda.synchronize()
     return out.numpy()
