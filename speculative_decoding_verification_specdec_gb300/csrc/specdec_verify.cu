@@ -865,7 +865,8 @@ struct StreamShared {
     float c;
     uint32_t issued;                       // chunks the producer issued (set when it is done)
     // top-k / top-p threshold search: the 256 bins of one pass. Masses are sums of 24-bit
-    // integers kept as the sums of their low and high 12 bits (exact in 32 bits for V <= 2^20).
+    // integers kept as the sums of their low and high 12 bits (exact in 32 bits for V <= 2^20;
+    // two 32-bit shared atomics measured far faster than one 64-bit one under contention).
     uint32_t fcnt[256];
     uint32_t flo[256], fhi[256];
     uint32_t fw_cnt[kConsumerWarps], fw_kmin[kConsumerWarps], fw_kmax[kConsumerWarps];  // per-warp partials
@@ -2122,7 +2123,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
         };
 
         int acc_len = 0, emitted = -1;
-        bool try_slice = true;          // top-k: try the top-slice pass first (off after a miss)
+        int slice_oct = 0;              // top-k: octaves of the top slice below its base level (-1: off)
         if (rs.skip == 0) {
             acc_len = k;
             int listed_row = -1, listed_n = 0;            // row whose whole slice list is in `list`
@@ -2135,8 +2136,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // integer sums (the result does not depend on the order of the additions). Dense rows
             // are streamed again through the ring; sparse rows reuse their gathered groups when the
             // row's list fit one gather batch, else gather again.
-            // The visitors call f(z, valid) for every vector of element slots of the row (z: VE
-            // logits; bit e of valid: slot e holds an allowed id with a finite logit).
+            // The visitors call f(z, valid, id0) for every vector of element slots of the row (z: VE
+            // logits of ids id0 .. id0 + VE - 1; bit e of valid: slot e holds an allowed id with a
+            // finite logit).
             auto gather_and_visit = [&](int64_t t, int n, auto&& f) {
                 const unsigned char* lrow = reinterpret_cast<const unsigned char*>(a.logits) + t * (int64_t)a.V * G::ES;
                 const uint32_t dbase = smem_addr(ring + kDataOff);
@@ -2153,7 +2155,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         float z[VE];
                         unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
                         const uint32_t bits = in ? (list[b0 + e] & 0xffu) : 0u;
-                        f(z, bits & finite_bits<VE>(z));
+                        f(z, bits & finite_bits<VE>(z), in ? (int)(list[b0 + e] >> 8) * VE : 0);
                     }
                     consumer_sync();
                 }
@@ -2184,7 +2186,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             for (int u = 0; u < NB; ++u) {
                                 float z[VE];
                                 unpack_raw<ET>(raw[u], z);
-                                f(z, bits[u] & finite_bits<VE>(z));
+                                f(z, bits[u] & finite_bits<VE>(z), i0 + (vb + lane + u * kConsumers) * VE);
                             }
                         }
                         release(s);
@@ -2198,7 +2200,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         float z[VE];
                         unpack_raw<ET>(in ? data[e] : make_uint4(0u, 0u, 0u, 0u), z);
                         const uint32_t bits = in ? (list[e] & 0xffu) : 0u;
-                        f(z, bits & finite_bits<VE>(z));
+                        f(z, bits & finite_bits<VE>(z), in ? (int)(list[e] >> 8) * VE : 0);
                     }
                 } else if (listed_row == j) {
                     gather_and_visit(t, listed_n, f);
@@ -2244,7 +2246,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 uint32_t tcnt = 0u;
                 unsigned long long tm = 0ull;
                 const uint32_t kfloor = max(floor_key, klo);
-                auto bin = [&](const auto& z, uint32_t valid) {
+                auto bin = [&](const auto& z, uint32_t valid, int) {
                     constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
                     uint32_t key[N];
                     uint32_t in = 0u;
@@ -2284,7 +2286,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 else
                     for (int i = ct; i < ncand; i += kConsumers) {
                         const float z1[1] = {key_logit(sh.fcand[i])};
-                        bin(z1, 1u);
+                        bin(z1, 1u, 0);
                     }
                 SPECDEC_STAMP(14);
                 if (bin0 < 0) {
@@ -2386,7 +2388,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 const float alo = bc == 0u ? -INFINITY : log2f((float)(8u + (bc & 7u)) * 0.125f) + bexp - 1e-3f;
                 const float ahi = (sum_above || all) ? INFINITY
                                 : (bc == 0u ? -30.f : log2f((float)(9u + (bc & 7u)) * 0.125f) + bexp) + 1e-3f;
-                auto take = [&](const auto& z, uint32_t valid) {
+                auto take = [&](const auto& z, uint32_t valid, int) {
                     constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
                     float arg[N];
                     uint32_t in = 0u;
@@ -2425,7 +2427,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 else
                     for (int i = ct; i < ncand; i += kConsumers) {
                         const float z1[1] = {key_logit(sh.fcand[i])};
-                        take(z1, 1u);
+                        take(z1, 1u, 0);
                     }
                 SPECDEC_STAMP(11);
 #pragma unroll
@@ -2451,7 +2453,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (ct == 0) sh.fncand = 0u;
                 consumer_sync();
                 SPECDEC_STAMP(10);
-                visit_row(t, j, [&](const auto& z, uint32_t valid) {
+                visit_row(t, j, [&](const auto& z, uint32_t valid, int) {
                     constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
                     uint32_t take = 0u;
 #pragma unroll
@@ -2481,21 +2483,27 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // candidates already hold every element at or above floor_key, so the whole search
             // runs on chip; on return it is >= 0 when that holds for this search's kept elements.
             auto search = [&](int64_t t, int j, int mode, unsigned long long need, float p_frac, uint32_t floor_key,
-                              float MC, float S, bool keep_above, bool& try_slice, int& ncand, uint32_t& key_out,
+                              float MC, float S, bool keep_above, int& slice_oct, int& ncand, uint32_t& key_out,
                               unsigned long long& mass_above, unsigned long long& mass_at) -> bool {
                 constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
                 int src0 = ncand;
                 // Top-k: first try the top slice of logits whose mass exp2(z*c - MC) is at least
-                // 1.0625 S / kCandCap (at most about kCandCap of them, S the row's softmax sum): when it
-                // holds k elements it holds the k-th largest and everything above it, and the whole
-                // search (and a top-p search after it) runs on chip. Else (too few, or too many) the
-                // row is searched as below, and the request stops trying.
+                // 1.0625 S / kCandCap (at most about kCandCap of them, S the row's softmax sum), lowered
+                // by slice_oct octaves: when it holds k elements (and no more than fit) it holds the
+                // k-th largest and everything above it, and the whole search (and a top-p search after
+                // it) runs on chip. A slice with too few elements is tried once more 16x lower, one with
+                // too many 4x higher; the level that worked is where the request's next row starts.
+                // After two misses the row is searched as below, and the request stops trying.
                 bool top_slice = false;
-                if (src0 < 0 && mode == 0 && try_slice && need * 17 <= (unsigned long long)kCandCap * 16) {
-                    const float zt = (__log2f(S * (1.0625f / (float)kCandCap)) + MC) / c;
-                    const int n = slice_pass(t, j, zt);
-                    if (n <= kCandCap && (unsigned long long)n >= need) { src0 = n; top_slice = true; }
-                    else try_slice = false;
+                if (src0 < 0 && mode == 0 && slice_oct >= 0 && need * 17 <= (unsigned long long)kCandCap * 16) {
+                    for (int attempt = 0; attempt < 2 && !top_slice; ++attempt) {
+                        const float zt = (__log2f(S * (1.0625f / (float)kCandCap)) - (float)slice_oct + MC) / c;
+                        const int n = slice_pass(t, j, zt);
+                        if (n <= kCandCap && (unsigned long long)n >= need) { src0 = n; top_slice = true; }
+                        else if (n > kCandCap) slice_oct = max(0, slice_oct - 2);
+                        else slice_oct += 4;
+                    }
+                    if (!top_slice) slice_oct = -1;
                 }
                 // on chip, the first pass takes counts and masses (the candidates are few)
                 hist_pass(t, j, -1, 0u, 0u, 0, 0u, floor_key, MC, 0u, 0xffffffffu, src0,
@@ -2556,14 +2564,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 bool cut_k = false;
                 if (fk > 0) {
                     uint32_t key;
-                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.f, 0u, MC, S, fp < 1.f, try_slice, ncand, key,
+                    cut_k = search(t, j, 0, (unsigned long long)fk, 0.f, 0u, MC, S, fp < 1.f, slice_oct, ncand, key,
                                    above, at);
                     if (cut_k) { floor_key = key; keep = above + at; }
                 }
                 bool cut_p = false;
                 if (fp < 1.f) {
                     uint32_t key;
-                    bool no_slice = false;
+                    int no_slice = -1;
                     cut_p = search(t, j, 1, 0ull, fp, floor_key, MC, S, false, no_slice, ncand, key, above,
                                    at);
                     if (cut_p) { floor_key = key; keep = above + at; }
@@ -2749,6 +2757,63 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     post(kDecDone);
                     break;
                 }
+            };
+
+            // ---- draw over the kept ids only (top-k requests): one more pass over the row's logits
+            // lists the ids at or above the threshold key kt (at most k plus ties) in the candidate
+            // slots; each is then drawn from its own logit, noise and q, loaded one by one, instead of
+            // streaming the noise and q rows as draw_row does. The per-id terms and the tie rule
+            // (the lowest id on equal scores) are draw_lazy's, so the token is the one draw_row
+            // would emit. Returns false, with the draw code posted, when the ids do not fit (the
+            // caller then runs draw_row).
+            auto draw_kept = [&](int j, int code, float MC, float S_mc, uint32_t kt) -> bool {
+                const int64_t t = rs.row0 + j;
+                const int64_t d = (int64_t)rs.d0 + j;
+                const int x = (j == k) ? -1 : sh.xs[j];
+                if (ct == 0) sh.fncand = 0u;
+                consumer_sync();
+                SPECDEC_STAMP(10);
+                visit_row(t, j, [&](const auto& z, uint32_t valid, int id0) {
+                    constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
+#pragma unroll
+                    for (int i = 0; i < N; ++i)
+                        if (((valid >> i) & 1u) && logit_key(z[i]) >= kt) {
+                            const uint32_t pos = atomicAdd(&sh.fncand, 1u);
+                            if (pos < (uint32_t)kCandCap) sh.fcand[pos] = (uint32_t)(id0 + i);
+                        }
+                });
+                consumer_sync();
+                SPECDEC_STAMP(11);
+                const int n = (int)sh.fncand;
+                if (n > kCandCap) { post(code); return false; }
+                while (true) {
+                    SPECDEC_STAMP(5);
+                    const float invS = 1.f / S_mc;
+                    const bool wq = (code == kDecDrawQ);
+                    Part dp = part_identity();
+                    for (int i = ct; i < n; i += kConsumers) {
+                        const int id = (int)sh.fcand[i];
+                        const float z = load_logit<ET>(a.logits, t * (int64_t)a.V + id);
+                        const float E = __ldg(a.noise + t * (int64_t)a.V + id);
+                        const float q = wq ? __ldg(a.q + d * (int64_t)a.V + id) : 0.f;
+                        const float pe = ex2_scaled(z, c, MC) * invS;
+                        float w = pe;
+                        if (wq) w = fmaxf(pe - q, 0.f);
+                        else if (code == kDecDrawOneHot && id == x) w = 0.f;
+                        if (w > 0.f && z > -INFINITY) {
+                            dp.flag = 1;
+                            const float sc = w * fast_rcp(E);
+                            if (sc > 0.f && (sc > dp.best || (sc == dp.best && id < dp.idx))) { dp.best = sc; dp.idx = id; }
+                        }
+                    }
+                    SPECDEC_STAMP(6);
+                    const Part dr = reduce(dp);
+                    if (code == kDecDrawQ && !dr.flag) { code = kDecDrawP; continue; }   // empty residual
+                    emitted = dr.idx == INT_MAX ? -1 : dr.idx;
+                    break;
+                }
+                post(kDecDone);
+                return true;
             };
 
             // race rows (see race_raise; the producer applies the same test): the bonus row of an
@@ -2971,13 +3036,25 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 bool stop;
                 float MC, S_mc;
                 const int code = decide(j, r, stop, MC, S_mc, cut, kt, S_keep);
-                post(code);
+                // a filtered stop row with few kept ids draws over those ids only: at most k of them
+                // for top-k without ties, and at most S_keep / e(kt) in any case (each kept id has
+                // mass at least e(kt), the threshold logit's)
+                bool kept_draw = false;
+                if constexpr (kFilt) {
+                    if (stop && cut && kt != 0u && (code == kDecDrawP || code == kDecDrawQ || code == kDecDrawOneHot)) {
+                        const float ekt = ex2_scaled(key_logit(kt), c, MC);
+                        const float nmax = ekt > 0.f ? S_keep / ekt : INFINITY;
+                        kept_draw = (fk > 0 && fk <= kCandCap - 64) || nmax <= (float)(kCandCap - 64);
+                    }
+                }
+                if (!kept_draw) post(code);
                 if (!stop) continue;
 
                 // drain the chunks of row j+1 the producer queued before this decision
                 if (!sparse && j < k && !filt)
                     for (int ch = 0; ch < spec; ++ch) release(wait_full());
-                draw_row(j, code, MC, S_mc, cut ? kt : 0u);
+                if (!kept_draw || !draw_kept(j, code, MC, S_mc, kt))
+                    draw_row(j, code, MC, S_mc, cut ? kt : 0u);
                 acc_len = j;
                 break;
             }

@@ -34,3 +34,16 @@ def shard_bounds(cu_num_draft: Sequence[int], world: int) -> List[Tuple[int, int
 
 def merge_counters(per_rank: Sequence[Sequence[int]]) -> np.ndarray:
     return np.sum(np.asarray(per_rank, dtype=np.uint64), axis=0, dtype=np.uint64)
+
+
+def merge_outputs(per_rank: Sequence[dict]) -> dict:
+    """One batch's outputs from its shards' outputs, in rank order: per-row and per-request arrays
+    concatenate (the shards are contiguous request ranges), counters and telemetry add up."""
+    merged = {}
+    for key in ("out_tokens", "out_num_accepted", "status"):
+        merged[key] = np.concatenate([np.asarray(r[key]) for r in per_rank])
+    merged["counters"] = merge_counters([r["counters"] for r in per_rank])
+    if all(r.get("telemetry") is not None for r in per_rank):
+        merged["telemetry"] = np.sum([np.asarray(r["telemetry"], dtype=np.uint64) for r in per_rank], axis=0,
+                                     dtype=np.uint64)
+    return merged

@@ -78,6 +78,25 @@ def test_ties_at_the_boundary(cuda, dtype):
     _check(w, cuda)
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16])
+def test_top_k_ties_beyond_the_kept_id_slots(cuda, dtype):
+    """Top-k 5 on rows whose maximum logit occurs about 3000 times: every copy is kept (ties at the
+    threshold), more ids than the kept-id draw can list, so the stop row's draw streams the row as
+    usual; top-k 3 on rows with a few copies takes the kept-id draw. Both against the oracle."""
+    B, V = 24, 40000
+    w = W.make_batch(65, name=f"topk_wide_ties_{dtype}", B=B, V=V, k=(1, 4), logits_dtype=dtype, logit_sigma=1.0,
+                     temperature="uniform(0.7,1.3)", q_mode="half", draft_sigma=0.5,
+                     top_k=np.where(np.arange(B) % 2 == 0, 5, 3).astype(np.int32))
+    z = W.bf16_bits_to_f32(w.logits) if dtype == W.BF16 else w.logits
+    scale = np.where((np.arange(w.T) % 2) == 0, 0.35, 3.0).astype(np.float32)[:, None]   # wide ties / few ties
+    grid = np.round(z * scale).astype(np.float32)
+    logits = W.f32_to_bf16_bits(grid) if dtype == W.BF16 else grid
+    w = dataclasses.replace(w, logits=np.ascontiguousarray(logits))
+    top = grid.max(axis=1, keepdims=True)
+    assert ((grid == top).sum(axis=1) > 2048).any()
+    _check(w, cuda)
+
+
 def test_random_draft_model_batch_with_filters(cuda):
     """The benchmark's filtered batch: B=256, k=4, V=128256, fp32, per-request top-k / top-p."""
     _check(W.top_k_top_p_batch(), cuda)
