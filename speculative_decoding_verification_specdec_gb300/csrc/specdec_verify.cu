@@ -991,6 +991,15 @@ struct Filter {
     bool bad_p, on;
 };
 
+// What a draft row's statistics pass knows about the draft token x (the acceptance bound of the
+// streaming kernel): whether fewer than k logits lie above it (cok), the mass above it (A) and its
+// own mass (ex), both against the row's reference, its q and uniform. A top-p search may accept the
+// row as soon as its kept mass is bounded tightly enough (on: the data is valid).
+struct Settle {
+    bool on, cok, qmode;
+    float A, ex, qx, u;
+};
+
 __device__ __forceinline__ bool request_greedy(const Args& a, int b)
 {
     const float T = a.temperature[b];
@@ -2246,14 +2255,17 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 uint32_t tcnt = 0u;
                 unsigned long long tm = 0ull;
                 const uint32_t kfloor = max(floor_key, klo);
+                // (a first pass with no floor tests no key: every allowed element counts)
+                const bool plain = bin0 < 0 && kfloor == 0u;
                 auto bin = [&](const auto& z, uint32_t valid, int) {
                     constexpr int N = (int)(sizeof(z) / sizeof(z[0]));
-                    uint32_t key[N];
-                    uint32_t in = 0u;
+                    uint32_t in = valid;
+                    if (!plain) {
 #pragma unroll
-                    for (int i = 0; i < N; ++i) {
-                        key[i] = logit_key(z[i]);
-                        in |= (((valid >> i) & 1u) && key[i] >= kfloor && key[i] <= khi && (key[i] & pmask) == pval ? 1u : 0u) << i;
+                        for (int i = 0; i < N; ++i) {
+                            const uint32_t kk = logit_key(z[i]);
+                            if (!(kk >= kfloor && kk <= khi && (kk & pmask) == pval)) in &= ~(1u << i);
+                        }
                     }
                     if (in == 0u) return;
                     float e[N];
@@ -2272,7 +2284,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                             dg = mb[i];
                         } else {
                             if ((int)mb[i] != bin0) continue;
-                            dg = (key[i] >> shift) & width;
+                            dg = (logit_key(z[i]) >> shift) & width;
                         }
                         if (wcnt) atomicAdd(&sh.fcnt[dg], 1u);
                         if (wmass) {
@@ -2484,7 +2496,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
             // runs on chip; on return it is >= 0 when that holds for this search's kept elements.
             auto search = [&](int64_t t, int j, int mode, unsigned long long need, float p_frac, uint32_t floor_key,
                               float MC, float S, bool keep_above, int& slice_oct, int& ncand, uint32_t& key_out,
-                              unsigned long long& mass_above, unsigned long long& mass_at) -> bool {
+                              unsigned long long& mass_above, unsigned long long& mass_at, const Settle& st) -> bool {
                 constexpr int kLowBit = (sizeof(ET) == 2) ? 16 : 0;
                 int src0 = ncand;
                 // Top-k: first try the top slice of logits whose mass exp2(z*c - MC) is at least
@@ -2515,6 +2527,24 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     mass_above = sh.ftot_mass;
                     mass_at = 0ull;
                     return false;
+                }
+                if (mode == 1 && st.on) {
+                    // The threshold lies in mass bin b0, so the kept mass is at most the mass of b0 and
+                    // everything above it: an accepted row of a surely kept draft whose uniform lies
+                    // below the ratio that bound gives needs no more passes. It returns no threshold
+                    // (key 0) and that bound as the kept mass, with which the acceptance test passes.
+                    constexpr float kLo = 1.f - 1e-4f, kHi = 1.f + 1e-4f;
+                    const unsigned long long hi = sh.fsel_mass + sh.fsel_at + 256ull;   // (+ the fx40 truncations)
+                    const float S_hi = (float)hi * 0x1p-40f;
+                    const bool kept = st.cok && st.A * kHi < (float)P * 0x1p-40f * kLo;
+                    const float px_lo = st.ex / S_hi * kLo;
+                    const float alpha_lo = !st.qmode ? px_lo : (px_lo >= st.qx ? 1.f : px_lo / st.qx * kLo);
+                    if (kept && px_lo > 0.f && st.u < alpha_lo) {
+                        key_out = 0u;
+                        mass_above = hi;
+                        mass_at = 0ull;
+                        return true;
+                    }
                 }
                 const unsigned long long n_above = sh.fsel_cnt, n_bin = sh.fsel_n;
                 unsigned long long above = sh.fsel_mass;          // (first top-k pass: not summed)
@@ -2557,7 +2587,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 mass_at = at;
                 return true;
             };
-            auto filter_row = [&](int64_t t, int j, float MC, float S, uint32_t& kt, float& S_keep) -> bool {
+            auto filter_row = [&](int64_t t, int j, float MC, float S, uint32_t& kt, float& S_keep, const Settle& st) -> bool {
                 uint32_t floor_key = 0u;
                 unsigned long long keep = 0ull, above = 0ull, at = 0ull;      // masses in units of 2^-40
                 int ncand = -1;                                  // candidates hold every kept element
@@ -2565,7 +2595,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                 if (fk > 0) {
                     uint32_t key;
                     cut_k = search(t, j, 0, (unsigned long long)fk, 0.f, 0u, MC, S, fp < 1.f, slice_oct, ncand, key,
-                                   above, at);
+                                   above, at, Settle{});
                     if (cut_k) { floor_key = key; keep = above + at; }
                 }
                 bool cut_p = false;
@@ -2573,7 +2603,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     uint32_t key;
                     int no_slice = -1;
                     cut_p = search(t, j, 1, 0ull, fp, floor_key, MC, S, false, no_slice, ncand, key, above,
-                                   at);
+                                   at, st);
                     if (cut_p) { floor_key = key; keep = above + at; }
                 }
                 kt = floor_key;
@@ -3007,6 +3037,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                     // The fp32 sums here differ from the search's exact integer sums by far less than
                     // the 1e-4 margins; a row the bound does not settle takes the search as before.
                     bool sure = false;
+                    Settle st{};
                     if (bound_on && r.m > -INFINITY && r.zx > -INFINITY) {
                         const float MCb = r.m * c;
                         float av = (p.m > -INFINITY) ? mass_above * ex2(mc - MCb) : 0.f;
@@ -3030,8 +3061,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) specdec_verify_stream_kerne
                         const float px_lo = ex / Smc * kLo;
                         const float alpha_lo = !qmode ? px_lo : (px_lo >= sh.qxs[j] ? 1.f : px_lo / sh.qxs[j] * kLo);
                         sure = kept && px_lo > 0.f && sh.us[j] < alpha_lo;
+                        st = Settle{true, fk <= 0 || C < (unsigned long long)fk, qmode, A, ex, sh.qxs[j], sh.us[j]};
                     }
-                    cut = filt && !sure && r.m > -INFINITY && filter_row(t, j, r.m * c, r.S, kt, S_keep);
+                    cut = filt && !sure && r.m > -INFINITY && filter_row(t, j, r.m * c, r.S, kt, S_keep, st);
                 }
                 bool stop;
                 float MC, S_mc;
