@@ -81,3 +81,24 @@ def test_two_rank_gloo_sharded_verify_matches_unsharded():
         assert p.exitcode == 0
     assert res["tokens_equal"] and res["acc_equal"] and res["status_equal"] and res["counters_equal"], res
     assert res["max_time"] == 2.0
+
+
+def test_merge_outputs_concatenates_in_rank_order_and_sums():
+    """The oracle's outputs for three contiguous request ranges, merged, equal its outputs for the
+    whole batch: per-row tokens and per-request arrays concatenate, counters and telemetry add up."""
+    import oracle
+
+    w = W.make_batch(11, B=23, V=300, k=(0, 5), logit_sigma=2.5, temperature="half_greedy(0.5,1.2)",
+                     q_mode="half", draft_sigma=0.5, mask="half", mask_density=0.3, mask_run_len=4)
+    parts = []
+    for b0, b1 in shard.shard_bounds(w.cu_num_draft, 3):
+        r = oracle.verify(w.subset(range(b0, b1)))
+        parts.append({"out_tokens": r.out_tokens, "out_num_accepted": r.out_num_accepted, "status": r.status,
+                      "counters": r.counters, "telemetry": r.telemetry})
+    merged = shard.merge_outputs(parts)
+    full = oracle.verify(w)
+    assert np.array_equal(merged["out_tokens"], full.out_tokens)
+    assert np.array_equal(merged["out_num_accepted"], full.out_num_accepted)
+    assert np.array_equal(merged["status"], full.status)
+    assert np.array_equal(merged["counters"].astype(np.int64), np.asarray(full.counters, dtype=np.int64))
+    assert np.array_equal(merged["telemetry"].astype(np.int64), np.asarray(full.telemetry, dtype=np.int64))
