@@ -92,16 +92,21 @@ typedef enum { SPECDEC_F32 = 0, SPECDEC_BF16 = 1 } specdec_dtype_t;
  *                  ids are those whose (top-k renormalised) mass of strictly larger logits is
  *                  below top_p (ties kept); p is renormalised over the kept ids. A value that is
  *                  not a number in (0, 1] sets SPECDEC_ST_BAD_TOP_P and is ignored. With top_k or
- *                  top_p given, the streaming kernel runs one CTA per request. A top-k search
+ *                  top_p given, the streaming kernel runs one CTA per request. A draft that is
+ *                  surely kept and whose uniform lies below e_x / (S q(x)) (S the row's whole
+ *                  softmax sum, a lower bound of the filtered ratio) is accepted without a
+ *                  threshold search, unless diag_accept_prob is given (every filtered row then
+ *                  searches, so that the exact filtered alpha can be reported). A top-k search
  *                  (k <= 1927) first streams a filtered row once more to take its top slice of
- *                  logits (the elements carrying at least 1.0625 S / 2048 of the mass); when that
- *                  holds k elements the top-k search, and a top-p search after it, run on chip.
- *                  Otherwise a search streams the row to bin its logits by mass and once more to
- *                  collect the chosen bin (on chip when it holds at most 2048 elements, else one
- *                  more pass per 8-bit digit of its keys: at most 2 for bf16 logits, 4 for fp32).
- *                  The result does not depend on the route. V > 2^20, or the slice-resident
- *                  cluster kernel (specdec_set_launch_options), with either of them:
- *                  SPECDEC_ERR_UNSUPPORTED.
+ *                  logits (the elements carrying at least 1.0625 S / 2048 of the mass, or 16x less
+ *                  on a retry); when that holds k elements the top-k search, and a top-p search
+ *                  after it, run on chip. Otherwise a search streams the row to bin its logits by
+ *                  mass (an accepted top-p row may be settled there) and once more to collect the
+ *                  chosen bin (on chip when it holds at most 2048 elements, else one more pass per
+ *                  8-bit digit of its keys: at most 2 for bf16 logits, 4 for fp32). A stop row
+ *                  with few kept ids draws from those ids only. The outputs do not depend on the
+ *                  route. V > 2^20, or the slice-resident cluster kernel
+ *                  (specdec_set_launch_options), with either of them: SPECDEC_ERR_UNSUPPORTED.
  *   uniforms       [T] fp32 in [0, 1); draft j of request b is accepted iff
  *                  uniforms[t(b,j)] < alpha (strict). Entries at bonus rows are unused.
  *   exp_noise      [T, V] fp32 Exp(1) samples > 0; the token drawn from weights w at row t
